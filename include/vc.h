@@ -1,0 +1,243 @@
+/*
+ * vc.h -- C ABI of the VeriCache attention-step library (libvc.so, sm_103a).
+ *
+ * VeriCache ("VeriCache: Making Lossy KV Compression Exact", section "The
+ * Core Idea") drafts x tokens autoregressively with a lossy compressed KV
+ * cache (KV_comp), checks them in ONE pass over the full cache (KV_full)
+ * that yields x + 1 greedy predictions, and emits the longest matching
+ * prefix plus the verifier's correction (or bonus) token, so the output is
+ * identical to greedy decoding with the full cache.  This library holds the
+ * four data-parallel operations of that attention step:
+ *
+ *   vc_compress     KV_full -> KV_comp: gather by a kept-index list and/or
+ *                   asymmetric 2/3/4-bit group quantisation ("VeriCache
+ *                   Guide", "The Uniform Compressor Interface": token
+ *                   eviction and low-bit quantisation behind one compress()).
+ *   vc_draft_attn   one decode query per request over KV_comp (the drafting
+ *                   step, "The Core Idea" items 1-2; memory-bandwidth bound,
+ *                   "Verifying Without Giving Back the Speedup").
+ *   vc_verify_attn  the drafted block's queries over KV_full, causal inside
+ *                   the block ("The Core Idea" items 3-5).
+ *   vc_accept       LM-head argmax over the verifier's rows, longest
+ *                   matching prefix + correction / bonus (the accept step
+ *                   and its worked example in "The Core Idea").
+ * plus the host-to-device staging of KV_full on a side stream ("VeriCache
+ * Guide", the dual-stream engine and "Best Practice 2: pinned memory") and a
+ * single launch mixing drafting and verifying requests (cross-resource
+ * staggering, "Verifying Without Giving Back the Speedup", Figure 2).
+ *
+ * Conventions
+ *  - Every pointer argument named as "device" must point to device memory of
+ *    the current device; "host" pointers to host memory.  The caller owns and
+ *    allocates every buffer, including workspaces (sizes from the
+ *    vc_*_workspace_bytes queries).  The library allocates nothing.
+ *  - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  Argument errors are returned synchronously
+ *    (nothing is launched); a failed launch returns VC_ERR_CUDA.  Errors in
+ *    device-resident data (a page id or kept index out of range, a wait that
+ *    timed out) are written to the optional device word `dev_status` (first
+ *    error wins; the caller zeroes it and reads it after synchronising); the
+ *    offending element is skipped, never read or written out of bounds.
+ *  - No C++ exception crosses this interface.
+ *
+ * Paged KV layout (page = 16 tokens, separate K and V pools)
+ *  - A pool is an array of pages; page p starts at byte p * vc_page_bytes().
+ *    Inside a page, kv head h owns a contiguous block of vc_head_block_bytes()
+ *    bytes starting at h * vc_head_block_bytes(); token slot s = position % 16.
+ *  - bits == 16 (bf16, KV_full or token-drop KV_comp):
+ *      block = bf16 [16][head_dim]                              (32 * D bytes)
+ *  - bits in {2, 3, 4} (quantised KV_comp), D = head_dim, G = D / 32 groups:
+ *      codes  uint8 [16][D * bits / 8]   token slot s, channel i uses bits
+ *                                        [bits*i, bits*i + bits) of the slot's
+ *                                        little-endian byte string
+ *      scales fp16  [16][G]              per token and 32-channel group
+ *      zeros  fp16  [16][G]
+ *                                        (2 * D * (bits + 1) bytes in all)
+ *    Quantisation of one group x[0..31] (bf16 values, fp32 arithmetic, every
+ *    operation rounded to nearest even, no contraction):
+ *      mn = min x (a -0 minimum is stored as +0), mx = max x
+ *      scale = fp16(sat((mx - mn) / (2^bits - 1))), zero = fp16(sat(mn))
+ *      code_i = 0 if scale == 0 else clamp(rint((x_i - zero) / scale), 0, 2^bits-1)
+ *    where sat() clamps to [-65504, 65504].  Dequantised value: scale * code + zero.
+ *  - block_table: device int32 [batch][max_blocks]; entry j of row b is the
+ *    page holding positions [16 j, 16 j + 16) of request b.
+ *  - seq_lens: device int32 [batch]; tokens present for each request.
+ */
+#ifndef VC_H
+#define VC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define VC_API __attribute__((visibility("default")))
+#else
+#define VC_API
+#endif
+
+#define VC_PAGE_TOKENS 16
+#define VC_GROUP 32
+#define VC_MAX_HEAD_DIM 256
+#define VC_MAX_GQA_GROUP 8
+#define VC_MAX_VERIFY_QUERIES 64
+
+typedef enum {
+    VC_OK = 0,
+    VC_ERR_INVALID_ARG = 1, /* null pointer, negative size, mismatched formats  */
+    VC_ERR_UNSUPPORTED = 2, /* bits / head_dim / GQA group outside the support  */
+    VC_ERR_BAD_INDEX = 3,   /* (device status) page id or kept index out of range */
+    VC_ERR_CUDA = 4,        /* a CUDA launch or copy failed                       */
+    VC_ERR_STAGING = 5,     /* staging source not in page-locked host memory      */
+    VC_ERR_TIMEOUT = 6,     /* (device status) a bounded wait gave up             */
+    VC_ERR_WORKSPACE = 7    /* workspace null or smaller than the size query      */
+} vc_status;
+
+typedef void *vc_stream_t; /* cudaStream_t */
+typedef void *vc_event_t;  /* cudaEvent_t  */
+
+typedef struct {
+    int32_t num_kv_heads; /* >= 1                                   */
+    int32_t head_dim;     /* multiple of 32, 32..256 (draft / verify: 64 or 128) */
+    int32_t bits;         /* 16 (bf16), 4, 3 or 2                    */
+} vc_kv_format;
+
+typedef struct {
+    void *k_pages;               /* device: K page pool                       */
+    void *v_pages;               /* device: V page pool                       */
+    int64_t num_pages;           /* pages in each pool (page ids < this)      */
+    const int32_t *block_table;  /* device int32 [batch][max_blocks]          */
+    const int32_t *seq_lens;     /* device int32 [batch]                      */
+    int32_t batch;
+    int32_t max_blocks;
+    vc_kv_format fmt;
+} vc_paged_kv;
+
+/* Bytes of one page (all kv heads) and of one kv head's block in a page. */
+VC_API size_t vc_page_bytes(const vc_kv_format *fmt);
+VC_API size_t vc_head_block_bytes(const vc_kv_format *fmt);
+
+/*
+ * vc_compress -- KV_comp entries from KV_full ("VeriCache Guide", "The
+ * Uniform Compressor Interface"; the guide's compressor gathers K and V with
+ * one sorted index list shared by all heads).
+ *  full          bits == 16 cache; positions read must be < full->seq_lens[b].
+ *  kept_offsets  device int32 [batch + 1], CSR offsets into kept_idx.
+ *  kept_idx      device int32 positions in KV_full, in the order they are
+ *                stored (ascending for a token-drop list).
+ *  comp_start    device int32 [batch] or NULL (= 0): slot of KV_comp where
+ *                request b's first kept entry goes.  Appending the drafted
+ *                tokens' K/V passes the current KV_comp length here.
+ *  max_kept      host: upper bound of any request's kept count (grid size).
+ *  comp          bits in {2, 3, 4, 16}; same num_kv_heads / head_dim as full;
+ *                slots comp_start[b] + j must be covered by its block table.
+ *                comp->seq_lens is not read or written (the caller sets it).
+ * Entry (b, j) is written for every kv head: bits 16 copies the bf16 rows,
+ * bits < 16 quantises K and V rows with the rule in the layout notes above.
+ */
+VC_API vc_status vc_compress(const vc_paged_kv *full, const int32_t *kept_offsets,
+                      const int32_t *kept_idx, const int32_t *comp_start, int32_t max_kept,
+                      const vc_paged_kv *comp, int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * vc_draft_attn -- one decode query per query head over KV_comp:
+ *   out[b][h] = sum_t softmax_t(scale * <q[b][h], k_t>) v_t
+ * over the comp->seq_lens[b] entries of request b, k_t / v_t the dequantised
+ * rows of kv head h / (num_q_heads / num_kv_heads).  Split over context
+ * chunks (partials in `workspace`), then combined by a second launch.
+ *  q            device bf16 [batch][num_q_heads][head_dim]
+ *  out          device fp32 [batch][num_q_heads][head_dim]
+ *  max_seq_len  host: bound of every comp->seq_lens[b] (grid size)
+ *  workspace    device, >= vc_draft_workspace_bytes(comp, num_q_heads,
+ *               max_seq_len) bytes (0 when the format is unsupported)
+ * Requires num_q_heads / num_kv_heads <= 8, head_dim in {64, 128}.  A request
+ * with seq_len 0 gets zeros.  q must be finite and, for bits < 16, within the
+ * fp16 range (|q| <= 65504).
+ */
+VC_API size_t vc_draft_workspace_bytes(const vc_paged_kv *comp, int32_t num_q_heads,
+                                int32_t max_seq_len);
+VC_API vc_status vc_draft_attn(const void *q, int32_t num_q_heads, const vc_paged_kv *comp,
+                        float softmax_scale, float *out, int32_t max_seq_len, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * vc_verify_attn -- the verification pass over KV_full.  Request b holds
+ * L = full->seq_lens[b] tokens, the last n_q of which form the block being
+ * verified; query i sits at position L - n_q + i and attends to positions
+ * 0 .. L - n_q + i (causal inside the block).
+ *  q    device bf16 [batch][n_q][num_q_heads][head_dim]
+ *  out  device fp32 [batch][n_q][num_q_heads][head_dim]
+ * 1 <= n_q <= 64, num_q_heads / num_kv_heads <= 8, head_dim in {64, 128},
+ * full->fmt.bits == 16, L >= n_q (a request with L < n_q gets
+ * VC_ERR_BAD_INDEX in dev_status and zero output).  The split over context
+ * chunks is fixed by position (1024 keys), so a query's result does not
+ * depend on n_q, its place in the block, or the batch.
+ */
+VC_API size_t vc_verify_workspace_bytes(const vc_paged_kv *full, int32_t n_q, int32_t num_q_heads,
+                                 int32_t max_seq_len);
+VC_API vc_status vc_verify_attn(const void *q, int32_t n_q, int32_t num_q_heads,
+                         const vc_paged_kv *full, float softmax_scale, float *out,
+                         int32_t max_seq_len, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * vc_accept -- greedy acceptance ("The Core Idea": compare left to right;
+ * at the first mismatch emit the verified prefix and the verifier's token;
+ * if all x drafts match emit them plus the bonus prediction).
+ *  hidden        device fp32 [batch][n_pred][hidden_group][d]; prediction
+ *                i's hidden vector is the mean of its hidden_group vectors
+ *                ((fp32 sum in index order) / hidden_group; 1 = as given).
+ *  lm_head       device fp32 [d][vocab].
+ *  logits        fp32, one fused multiply-add per term in increasing k
+ *                (the same value for a row whatever batch / n_pred).
+ *  drafts        device int32 [batch][x]
+ *  verified      device int32 [batch][n_pred]: argmax, lowest id on ties
+ *  accept_len    device int32 [batch]: a = first i < x with a mismatch, else x
+ *  emitted       device int32 [batch][x + 1]: drafts[0:a] then verified[a]
+ *                when a < n_pred; remaining slots -1.
+ * n_pred is x + 1 (bonus available) or x (no bonus); 1 <= n_pred.
+ */
+VC_API size_t vc_accept_workspace_bytes(int32_t batch, int32_t n_pred, int32_t vocab);
+VC_API vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t hidden_group,
+                    const float *lm_head, int32_t d, int32_t vocab, const int32_t *drafts,
+                    int32_t x, int32_t *verified, int32_t *accept_len, int32_t *emitted,
+                    void *workspace, size_t workspace_bytes, vc_stream_t stream);
+
+/*
+ * vc_stage_async -- copy `bytes` from page-locked host memory to device
+ * memory on the side stream `side` and record `done` (may be NULL) after it,
+ * so a verify launch on another stream can wait for the staged KV_full
+ * ("VeriCache Guide": full KV reloaded on a swap stream while drafting
+ * continues; pinned memory for full DMA bandwidth).  Returns VC_ERR_STAGING
+ * when src is not page-locked (or registered) host memory.
+ */
+VC_API vc_status vc_stage_async(void *dev_dst, const void *pinned_src, size_t bytes,
+                         vc_stream_t side, vc_event_t done);
+
+/*
+ * vc_mixed_attn -- one launch in which requests with role[b] == 0 run the
+ * draft attention over `comp` and requests with role[b] == 1 run the
+ * verification attention of an n_q block over `full` (cross-resource
+ * staggering: some requests draft while others verify).  Arguments are
+ * those of vc_draft_attn / vc_verify_attn; both caches describe the same
+ * batch; role is device int32 [batch].  Outputs of a request are written
+ * only to the buffer of its role.  Workspace: vc_mixed_workspace_bytes.
+ */
+VC_API size_t vc_mixed_workspace_bytes(const vc_paged_kv *comp, const vc_paged_kv *full, int32_t n_q,
+                                int32_t num_q_heads, int32_t max_seq_len);
+VC_API vc_status vc_mixed_attn(const int32_t *role, const void *q_draft, const vc_paged_kv *comp,
+                        float *out_draft, const void *q_verify, int32_t n_q,
+                        const vc_paged_kv *full, float *out_verify, int32_t num_q_heads,
+                        float softmax_scale, int32_t max_seq_len, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
+
+VC_API const char *vc_status_string(vc_status s);
+VC_API const char *vc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VC_H */

@@ -1,0 +1,227 @@
+"""VeriCache attention step for GB300 (sm_103a): Python binding of libvc.so.
+
+The C ABI is declared in include/vc.h.  This module only marshals torch
+tensors (device memory owned by the caller) and CUDA streams into that ABI;
+every step of the computation runs in the library's CUDA kernels.  There is
+no fallback: importing raises when libvc.so has not been built
+(``python lossless_compressed_kv_gb300/build.py``).
+
+Operations (see the header for their exact definitions and the pages they
+follow): ``compress`` (KV_full -> KV_comp gather / 2-3-4-bit quantisation),
+``draft_attn`` (decode attention over KV_comp), ``verify_attn`` (causal
+block attention over KV_full), ``accept`` (argmax + longest matching prefix
++ correction / bonus), ``stage_async`` (pinned host -> device copy on a side
+stream) and ``mixed_attn`` (draft and verify requests in one launch).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvc.so")
+PAGE = 16
+GROUP = 32
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libvc.so is not built: run `python lossless_compressed_kv_gb300/build.py`")
+
+
+class KVFormat(C.Structure):
+    _fields_ = [("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("bits", C.c_int32)]
+
+
+class PagedKVStruct(C.Structure):
+    _fields_ = [("k_pages", C.c_void_p), ("v_pages", C.c_void_p), ("num_pages", C.c_int64),
+                ("block_table", C.c_void_p), ("seq_lens", C.c_void_p), ("batch", C.c_int32),
+                ("max_blocks", C.c_int32), ("fmt", KVFormat)]
+
+
+_P = C.c_void_p
+_lib = C.CDLL(LIB_PATH)
+_SIG = {
+    "vc_page_bytes": (C.c_size_t, [C.POINTER(KVFormat)]),
+    "vc_head_block_bytes": (C.c_size_t, [C.POINTER(KVFormat)]),
+    "vc_compress": (C.c_int, [C.POINTER(PagedKVStruct), _P, _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P, _P]),
+    "vc_draft_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32]),
+    "vc_draft_attn": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32, _P,
+                                C.c_size_t, _P, _P]),
+    "vc_verify_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32, C.c_int32]),
+    "vc_verify_attn": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32,
+                                 _P, C.c_size_t, _P, _P]),
+    "vc_accept_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32]),
+    "vc_accept": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
+                            _P, _P, C.c_size_t, _P]),
+    "vc_stage_async": (C.c_int, [_P, _P, C.c_size_t, _P, _P]),
+    "vc_mixed_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.POINTER(PagedKVStruct), C.c_int32,
+                                              C.c_int32, C.c_int32]),
+    "vc_mixed_attn": (C.c_int, [_P, _P, C.POINTER(PagedKVStruct), _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P,
+                                C.c_int32, C.c_float, C.c_int32, _P, C.c_size_t, _P, _P]),
+    "vc_status_string": (C.c_char_p, [C.c_int]),
+    "vc_version": (C.c_char_p, []),
+}
+for _n, (_r, _a) in _SIG.items():
+    _f = getattr(_lib, _n)
+    _f.restype = _r
+    _f.argtypes = _a
+
+STATUS = {0: "VC_OK", 1: "VC_ERR_INVALID_ARG", 2: "VC_ERR_UNSUPPORTED", 3: "VC_ERR_BAD_INDEX",
+          4: "VC_ERR_CUDA", 5: "VC_ERR_STAGING", 6: "VC_ERR_TIMEOUT", 7: "VC_ERR_WORKSPACE"}
+
+
+class VCError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (%s)" % (where, STATUS.get(code, code),
+                                          _lib.vc_status_string(code).decode()))
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise VCError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(s):
+    if s is None:
+        s = torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def version() -> str:
+    return _lib.vc_version().decode()
+
+
+def library():
+    """The loaded ctypes handle (for ABI tests)."""
+    return _lib
+
+
+def head_block_bytes(head_dim: int, bits: int) -> int:
+    f = KVFormat(1, head_dim, bits)
+    return int(_lib.vc_head_block_bytes(C.byref(f)))
+
+
+def page_bytes(num_kv_heads: int, head_dim: int, bits: int) -> int:
+    f = KVFormat(num_kv_heads, head_dim, bits)
+    return int(_lib.vc_page_bytes(C.byref(f)))
+
+
+@dataclass
+class PagedKV:
+    """A paged K/V cache in the layout of include/vc.h.
+
+    k_pages / v_pages: uint8 device tensors [num_pages, page_bytes];
+    block_table: int32 [batch, max_blocks]; seq_lens: int32 [batch]."""
+    k_pages: torch.Tensor
+    v_pages: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    num_kv_heads: int
+    head_dim: int
+    bits: int
+
+    @property
+    def batch(self) -> int:
+        return int(self.block_table.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    def struct(self) -> PagedKVStruct:
+        for t, dt in ((self.block_table, torch.int32), (self.seq_lens, torch.int32)):
+            if t.dtype != dt or not t.is_contiguous():
+                raise ValueError("block_table / seq_lens must be contiguous int32")
+        for t in (self.k_pages, self.v_pages):
+            if not t.is_contiguous():
+                raise ValueError("page pools must be contiguous")
+        return PagedKVStruct(self.k_pages.data_ptr(), self.v_pages.data_ptr(), self.num_pages,
+                             self.block_table.data_ptr(), self.seq_lens.data_ptr(), self.batch,
+                             int(self.block_table.shape[1]), KVFormat(self.num_kv_heads, self.head_dim, self.bits))
+
+    @staticmethod
+    def allocate(num_pages: int, num_kv_heads: int, head_dim: int, bits: int, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, device="cuda", zero: bool = False) -> "PagedKV":
+        pb = page_bytes(num_kv_heads, head_dim, bits)
+        mk = torch.zeros if zero else torch.empty
+        return PagedKV(mk((num_pages, pb), dtype=torch.uint8, device=device),
+                       mk((num_pages, pb), dtype=torch.uint8, device=device),
+                       block_table, seq_lens, num_kv_heads, head_dim, bits)
+
+
+def compress(full: PagedKV, kept_offsets, kept_idx, comp: PagedKV, max_kept: int, comp_start=None,
+             status=None, stream=None):
+    fs, cs = full.struct(), comp.struct()
+    _check(_lib.vc_compress(C.byref(fs), _ptr(kept_offsets), _ptr(kept_idx), _ptr(comp_start), int(max_kept),
+                            C.byref(cs), _ptr(status), _stream(stream)), "vc_compress")
+
+
+def draft_workspace_bytes(comp: PagedKV, num_q_heads: int, max_seq_len: int) -> int:
+    cs = comp.struct()
+    return int(_lib.vc_draft_workspace_bytes(C.byref(cs), num_q_heads, int(max_seq_len)))
+
+
+def draft_attn(q, comp: PagedKV, softmax_scale: float, out, max_seq_len: int, workspace, status=None,
+               stream=None):
+    cs = comp.struct()
+    _check(_lib.vc_draft_attn(_ptr(q), int(q.shape[-2]), C.byref(cs), float(softmax_scale), _ptr(out),
+                              int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _ptr(status), _stream(stream)), "vc_draft_attn")
+
+
+def verify_workspace_bytes(full: PagedKV, n_q: int, num_q_heads: int, max_seq_len: int) -> int:
+    fs = full.struct()
+    return int(_lib.vc_verify_workspace_bytes(C.byref(fs), n_q, num_q_heads, int(max_seq_len)))
+
+
+def verify_attn(q, full: PagedKV, softmax_scale: float, out, max_seq_len: int, workspace, status=None,
+                stream=None):
+    fs = full.struct()
+    _check(_lib.vc_verify_attn(_ptr(q), int(q.shape[1]), int(q.shape[2]), C.byref(fs), float(softmax_scale),
+                               _ptr(out), int(max_seq_len), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "vc_verify_attn")
+
+
+def accept_workspace_bytes(batch: int, n_pred: int, vocab: int) -> int:
+    return int(_lib.vc_accept_workspace_bytes(batch, n_pred, vocab))
+
+
+def accept(hidden, lm_head, drafts, verified, accept_len, emitted, workspace, hidden_group: int = 1,
+           stream=None):
+    """hidden [B][n_pred][hidden_group][d] (or [B][n_pred][d]) fp32; lm_head [d][V] fp32."""
+    b, n_pred = int(hidden.shape[0]), int(hidden.shape[1])
+    d, vocab = int(lm_head.shape[0]), int(lm_head.shape[1])
+    x = int(drafts.shape[1]) if drafts is not None and drafts.dim() == 2 else 0
+    _check(_lib.vc_accept(_ptr(hidden), b, n_pred, int(hidden_group), _ptr(lm_head), d, vocab,
+                          _ptr(drafts) if x else None, x, _ptr(verified), _ptr(accept_len), _ptr(emitted),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "vc_accept")
+
+
+def stage_async(dst, pinned_src, nbytes: int, side_stream, done_event=None):
+    ev = None if done_event is None else C.c_void_p(done_event.cuda_event)
+    _check(_lib.vc_stage_async(C.c_void_p(dst.data_ptr()), C.c_void_p(pinned_src.data_ptr()), int(nbytes),
+                               C.c_void_p(side_stream.cuda_stream), ev), "vc_stage_async")
+
+
+def mixed_workspace_bytes(comp: PagedKV, full: PagedKV, n_q: int, num_q_heads: int, max_seq_len: int) -> int:
+    cs, fs = comp.struct(), full.struct()
+    return int(_lib.vc_mixed_workspace_bytes(C.byref(cs), C.byref(fs), n_q, num_q_heads, int(max_seq_len)))
+
+
+def mixed_attn(role, q_draft, comp: PagedKV, out_draft, q_verify, full: PagedKV, out_verify,
+               softmax_scale: float, max_seq_len: int, workspace, status=None, stream=None):
+    cs, fs = comp.struct(), full.struct()
+    _check(_lib.vc_mixed_attn(_ptr(role), _ptr(q_draft), C.byref(cs), _ptr(out_draft), _ptr(q_verify),
+                              int(q_verify.shape[1]), C.byref(fs), _ptr(out_verify), int(q_draft.shape[1]),
+                              float(softmax_scale), int(max_seq_len), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "vc_mixed_attn")

@@ -1,0 +1,220 @@
+// vc_compress: KV_full (bf16 pages) -> KV_comp entries.
+//
+// "VeriCache Guide", section "The Uniform Compressor Interface" (token
+// eviction and low-bit quantisation behind one compress()) and the guide's
+// compressor (K and V gathered with one sorted index list shared by all
+// heads).  The bit format (asymmetric 32-channel groups, fp16 scale and
+// zero, little-endian packing) is the library's reading; see vc.h.
+//
+// One warp per (kept entry, kv head): 32 lanes each own D/32 consecutive
+// channels (a lane's channels never straddle a group), min/max of a group is
+// a shuffle reduction over the lanes of that group, codes are staged in
+// shared memory and packed into 32-bit words by the first D*bits/32 lanes.
+#include "vc_internal.cuh"
+
+namespace vc {
+namespace {
+
+constexpr int kWarps = 8;
+
+struct CompressArgs {
+    const uint8_t *fk, *fv;  // full pools
+    int64_t f_pages;
+    const int32_t *f_table, *f_lens;
+    int f_maxb;
+    uint8_t *ck, *cv;  // comp pools
+    int64_t c_pages;
+    const int32_t *c_table;
+    int c_maxb;
+    const int32_t *offs, *idx, *start;
+    int hkv;
+    int32_t *status;
+};
+
+__device__ inline uint16_t f16_store(float f) {  // saturate to +-65504, round to nearest even
+    f = fminf(fmaxf(f, -65504.0f), 65504.0f);
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+// Quantise one row (D channels) held CPL per lane; write codes, scales, zeros.
+template <int BITS, int D>
+__device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t *codes_smem, uint8_t *dst_codes,
+                             uint16_t *dst_scales, uint16_t *dst_zeros, int lane) {
+    constexpr int CPL = D / 32;             // channels per lane
+    constexpr int LPG = kGroup / CPL;       // lanes per group
+    constexpr int QMAX = (1 << BITS) - 1;
+    float v[CPL];
+    float mn, mx;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) v[i] = bf16_bits_to_f32(x[i]);
+    mn = v[0];
+    mx = v[0];
+#pragma unroll
+    for (int i = 1; i < CPL; ++i) {
+        mn = fminf(mn, v[i]);
+        mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int o = 1; o < LPG; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    mn = __fadd_rn(mn, 0.0f);  // -0 -> +0
+    const float range = __fsub_rn(mx, mn);
+    const float sdot = __fdiv_rn(range, (float)QMAX);
+    const uint16_t sh = f16_store(sdot);
+    const uint16_t zh = f16_store(mn);
+    const float s = __half2float(__ushort_as_half(sh));
+    const float z = __half2float(__ushort_as_half(zh));
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        int c = 0;
+        if (s != 0.0f) {
+            float t = __fdiv_rn(__fsub_rn(v[i], z), s);
+            float r = rintf(t);
+            r = fminf(fmaxf(r, 0.0f), (float)QMAX);
+            c = (int)r;
+        }
+        codes_smem[lane * CPL + i] = (uint8_t)c;
+    }
+    if (lane % LPG == 0) {
+        const int grp = lane / LPG;
+        dst_scales[grp] = sh;
+        dst_zeros[grp] = zh;
+    }
+    __syncwarp();
+    constexpr int WORDS = D * BITS / 32;
+    if (lane < WORDS) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int bit = lane * 32 + k;
+            const int ch = bit / BITS;
+            const int off = bit % BITS;
+            w |= (uint32_t)((codes_smem[ch] >> off) & 1) << k;
+        }
+        reinterpret_cast<uint32_t *>(dst_codes)[lane] = w;
+    }
+    __syncwarp();
+}
+
+template <int BITS, int D>
+__global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
+    constexpr int CPL = D / 32;
+    __shared__ __align__(16) uint8_t codes[kWarps][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int item = blockIdx.x * kWarps + warp;  // (entry, head) pair
+    const int j = item / a.hkv, h = item % a.hkv;
+    const int o0 = a.offs[b], o1 = a.offs[b + 1];
+    if (o0 + j >= o1) return;
+    const int t = a.idx[o0 + j];
+    const int slot = (a.start ? a.start[b] : 0) + j;
+    // bounds of every index read
+    if (t < 0 || t >= a.f_lens[b] || t / kPage >= a.f_maxb || slot < 0 || slot / kPage >= a.c_maxb) {
+        if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    const int fp = a.f_table[(int64_t)b * a.f_maxb + t / kPage];
+    const int cp = a.c_table[(int64_t)b * a.c_maxb + slot / kPage];
+    if (fp < 0 || fp >= a.f_pages || cp < 0 || cp >= a.c_pages) {
+        if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    const int fhb = head_block_bytes(16, D), chb = head_block_bytes(BITS, D);
+    const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
+    const int64_t cbase = ((int64_t)cp * a.hkv + h) * chb;
+    const int s = slot % kPage;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t *src = (kv ? a.fv : a.fk) + fbase;
+        uint8_t *dst = (kv ? a.cv : a.ck) + cbase;
+        uint16_t x[CPL];
+        // CPL bf16 = 2*CPL bytes per lane, contiguous across the warp
+        if constexpr (CPL == 4) {
+            uint2 u = reinterpret_cast<const uint2 *>(src)[lane];
+            x[0] = u.x & 0xffff; x[1] = u.x >> 16; x[2] = u.y & 0xffff; x[3] = u.y >> 16;
+        } else if constexpr (CPL == 2) {
+            uint32_t u = reinterpret_cast<const uint32_t *>(src)[lane];
+            x[0] = u & 0xffff; x[1] = u >> 16;
+        } else {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) x[i] = reinterpret_cast<const uint16_t *>(src)[lane * CPL + i];
+        }
+        if constexpr (BITS == 16) {
+            uint16_t *d16 = reinterpret_cast<uint16_t *>(dst + (int64_t)s * D * 2);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) d16[lane * CPL + i] = x[i];
+        } else {
+            constexpr int CB = D * BITS / 8, NG = D / kGroup;
+            uint8_t *dc = dst + s * CB;
+            uint16_t *dsc = reinterpret_cast<uint16_t *>(dst + kPage * CB) + s * NG;
+            uint16_t *dz = reinterpret_cast<uint16_t *>(dst + kPage * CB + kPage * NG * 2) + s * NG;
+            quantize_row<BITS, D>(x, codes[warp], dc, dsc, dz, lane);
+        }
+    }
+}
+
+template <int BITS, int D>
+cudaError_t launch_bd(const CompressArgs &a, int batch, int max_kept, cudaStream_t st) {
+    dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
+    compress_kernel<BITS, D><<<grid, kWarps * 32, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_b(int d, const CompressArgs &a, int batch, int max_kept, cudaStream_t st) {
+    switch (d) {
+        case 32: return launch_bd<BITS, 32>(a, batch, max_kept, st);
+        case 64: return launch_bd<BITS, 64>(a, batch, max_kept, st);
+        case 128: return launch_bd<BITS, 128>(a, batch, max_kept, st);
+        case 256: return launch_bd<BITS, 256>(a, batch, max_kept, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+vc_status compress(const vc_paged_kv *full, const int32_t *kept_offsets, const int32_t *kept_idx,
+                   const int32_t *comp_start, int32_t max_kept, const vc_paged_kv *comp,
+                   int32_t *dev_status, cudaStream_t st) {
+    if (!full || !comp || !kept_offsets || !kept_idx || max_kept < 0) return VC_ERR_INVALID_ARG;
+    if (full->fmt.bits != 16) return VC_ERR_UNSUPPORTED;
+    const int d = full->fmt.head_dim, hkv = full->fmt.num_kv_heads, bits = comp->fmt.bits;
+    if (comp->fmt.head_dim != d || comp->fmt.num_kv_heads != hkv || full->batch != comp->batch)
+        return VC_ERR_INVALID_ARG;
+    if (!(d == 32 || d == 64 || d == 128 || d == 256) || hkv < 1) return VC_ERR_UNSUPPORTED;
+    if (!(bits == 2 || bits == 3 || bits == 4 || bits == 16)) return VC_ERR_UNSUPPORTED;
+    if (!full->k_pages || !full->v_pages || !full->block_table || !full->seq_lens || !comp->k_pages ||
+        !comp->v_pages || !comp->block_table || full->batch < 0 || full->max_blocks < 1 ||
+        comp->max_blocks < 1)
+        return VC_ERR_INVALID_ARG;
+    if (full->batch == 0 || max_kept == 0) return VC_OK;
+    CompressArgs a;
+    a.fk = (const uint8_t *)full->k_pages;
+    a.fv = (const uint8_t *)full->v_pages;
+    a.f_pages = full->num_pages;
+    a.f_table = full->block_table;
+    a.f_lens = full->seq_lens;
+    a.f_maxb = full->max_blocks;
+    a.ck = (uint8_t *)comp->k_pages;
+    a.cv = (uint8_t *)comp->v_pages;
+    a.c_pages = comp->num_pages;
+    a.c_table = comp->block_table;
+    a.c_maxb = comp->max_blocks;
+    a.offs = kept_offsets;
+    a.idx = kept_idx;
+    a.start = comp_start;
+    a.hkv = hkv;
+    a.status = dev_status;
+    cudaError_t e;
+    switch (bits) {
+        case 2: e = launch_b<2>(d, a, full->batch, max_kept, st); break;
+        case 3: e = launch_b<3>(d, a, full->batch, max_kept, st); break;
+        case 4: e = launch_b<4>(d, a, full->batch, max_kept, st); break;
+        default: e = launch_b<16>(d, a, full->batch, max_kept, st); break;
+    }
+    return e == cudaSuccess ? VC_OK : VC_ERR_CUDA;
+}
+
+}  // namespace vc

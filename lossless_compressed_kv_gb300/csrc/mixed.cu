@@ -1,0 +1,162 @@
+// vc_mixed_attn: drafting and verifying requests in one launch.
+//
+// "VeriCache: Making Lossy KV Compression Exact", section "Verifying Without
+// Giving Back the Speedup", Figure 2 (cross-resource staggering): instead of
+// all requests drafting and then all verifying, some requests verify against
+// their full cache while the others keep drafting from the compressed one.
+// Drafting is HBM-bandwidth bound, verification brings dense tensor work, so
+// one grid holding both keeps both busy.  Blocks [0, Nv) run the
+// verification body for requests with role 1, blocks [Nv, Nv + Nd) the
+// draft body (8 warps) for requests with role 0; a block whose request has
+// the other role exits at once.  One combine launch finishes both.
+#include "draft_impl.cuh"
+#include "verify_impl.cuh"
+
+namespace vc {
+int verify_splits(int max_seq_len);
+void verify_args(verify::VerifyArgs &a, const void *q, int n_q, int hq, const vc_paged_kv &f, float scale,
+                 int max_seq_len, void *ws, int32_t *status);
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDraftWarps = kThreads / 32;
+
+struct MixedArgs {
+    draft::DraftArgs d;
+    verify::VerifyArgs v;
+    const int32_t *role;
+    int n_verify_blocks, rb;
+};
+
+template <int BITS, int D>
+struct MCfg {
+    static constexpr int DS = draft::Cfg<BITS, D, kDraftWarps>::SMEM;
+    static constexpr int VS = verify::VCfg<D>::SMEM;
+    static constexpr int SMEM = DS > VS ? DS : VS;
+};
+
+template <int BITS, int D>
+__global__ void __launch_bounds__(kThreads) mixed_kernel(MixedArgs m) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    int bid = blockIdx.x;
+    if (bid < m.n_verify_blocks) {
+        const int split = bid % m.v.n_splits;
+        const int rest = bid / m.v.n_splits;
+        const int rb = rest % m.rb, bk = rest / m.rb;
+        if (m.role[bk / m.v.hkv] != 1) return;
+        verify::verify_block<D>(m.v, split, rb, bk, smem);
+    } else {
+        bid -= m.n_verify_blocks;
+        const int split = bid % m.d.n_splits;
+        const int rest = bid / m.d.n_splits;
+        const int kvh = rest % m.d.hkv, b = rest / m.d.hkv;
+        if (m.role[b] != 0) return;
+        draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, smem);
+    }
+}
+
+template <int D>
+__global__ void mixed_reduce_kernel(MixedArgs m, float *out_draft, float *out_verify, int draft_rows) {
+    const int row = blockIdx.x;
+    if (row < draft_rows) {  // row = b * Hq + h
+        if (m.role[row / m.d.hq] != 0) return;
+        draft::reduce_row<D>(m.d.ws_o, m.d.ws_ml, m.d.n_splits, row, out_draft, threadIdx.x, blockDim.x);
+    } else {  // ((b * n_q + i) * Hq + h)
+        const int r = row - draft_rows;
+        if (m.role[r / (m.v.n_q * m.v.hq)] != 1) return;
+        verify::reduce_row<D>(m.v.ws_o, m.v.ws_ml, m.v.n_splits, r, out_verify, threadIdx.x, blockDim.x);
+    }
+}
+
+int sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n < 1) n = 1;
+    }
+    return n;
+}
+
+// Draft chunking of the mixed launch: about two draft blocks per SM over the
+// whole batch (blocks of verifying requests exit at once).
+void draft_plan(int batch, int hkv, int max_seq_len, int &chunk, int &splits) {
+    const int max_pages = ceil_div(max_seq_len, kPage);
+    const int64_t units = (int64_t)batch * hkv;
+    int s = (int)((2LL * sms() + units - 1) / units);
+    s = max(1, min(s, ceil_div(max_pages, kDraftWarps)));
+    chunk = ceil_div(max_pages, s);
+    chunk = max(kDraftWarps, ceil_div(chunk, kDraftWarps) * kDraftWarps);
+    splits = max(1, ceil_div(max_pages, chunk));
+}
+
+size_t draft_part(const vc_paged_kv &comp, int hq, int max_seq_len) {
+    int chunk, splits;
+    draft_plan(comp.batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
+    return (size_t)comp.batch * hq * splits * (comp.fmt.head_dim + 2) * sizeof(float);
+}
+
+template <int BITS, int D>
+cudaError_t launch(const MixedArgs &m, int batch, float *out_draft, float *out_verify, cudaStream_t st) {
+    using C = MCfg<BITS, D>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(mixed_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        attr = true;
+    }
+    const int nd = m.d.n_splits * m.d.hkv * batch;
+    mixed_kernel<BITS, D><<<m.n_verify_blocks + nd, kThreads, C::SMEM, st>>>(m);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int draft_rows = batch * m.d.hq, verify_rows = batch * m.v.n_q * m.v.hq;
+    mixed_reduce_kernel<D><<<draft_rows + verify_rows, D, 0, st>>>(m, out_draft, out_verify, draft_rows);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t mixed_workspace(const vc_paged_kv &comp, const vc_paged_kv &full, int n_q, int hq, int max_seq_len) {
+    if (max_seq_len <= 0) return 0;
+    const size_t v = (size_t)full.batch * n_q * hq * verify_splits(max_seq_len) * (full.fmt.head_dim + 2) *
+                     sizeof(float);
+    return draft_part(comp, hq, max_seq_len) + v;
+}
+
+cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_paged_kv &comp, float *out_draft,
+                         const void *q_verify, int n_q, const vc_paged_kv &full, float *out_verify, int hq,
+                         float scale, int max_seq_len, void *ws, int32_t *status, cudaStream_t st) {
+    MixedArgs m;
+    const int d = comp.fmt.head_dim, bits = comp.fmt.bits, batch = comp.batch;
+    int chunk, splits;
+    draft_plan(batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
+    m.d.q = (const uint16_t *)q_draft;
+    m.d.kp = (const uint8_t *)comp.k_pages;
+    m.d.vp = (const uint8_t *)comp.v_pages;
+    m.d.n_pages = comp.num_pages;
+    m.d.table = comp.block_table;
+    m.d.lens = comp.seq_lens;
+    m.d.maxb = comp.max_blocks;
+    m.d.hq = hq;
+    m.d.hkv = comp.fmt.num_kv_heads;
+    m.d.grp = hq / m.d.hkv;
+    m.d.scale_log2 = scale * 1.4426950408889634f;
+    m.d.chunk_pages = chunk;
+    m.d.n_splits = splits;
+    m.d.ws_o = (float *)ws;
+    m.d.ws_ml = m.d.ws_o + (size_t)batch * hq * splits * d;
+    m.d.status = status;
+    void *vws = (uint8_t *)ws + draft_part(comp, hq, max_seq_len);
+    verify_args(m.v, q_verify, n_q, hq, full, scale, max_seq_len, vws, status);
+    m.role = role;
+    m.rb = ceil_div(n_q * m.v.grp, verify::kRows);
+    m.n_verify_blocks = m.v.n_splits * m.rb * batch * m.v.hkv;
+#define VC_L(B_, D_) launch<B_, D_>(m, batch, out_draft, out_verify, st)
+    if (d == 64)
+        return bits == 2 ? VC_L(2, 64) : bits == 3 ? VC_L(3, 64) : bits == 4 ? VC_L(4, 64) : VC_L(16, 64);
+    return bits == 2 ? VC_L(2, 128) : bits == 3 ? VC_L(3, 128) : bits == 4 ? VC_L(4, 128) : VC_L(16, 128);
+#undef VC_L
+}
+
+}  // namespace vc

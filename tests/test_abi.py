@@ -1,0 +1,94 @@
+"""The C-ABI library loads, exports every entry point include/vc.h declares,
+and rejects bad arguments on the host before any CUDA work (no GPU needed:
+these paths return before touching the device)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vc.h")
+
+
+def _build():
+    import __graft_entry__
+    return __graft_entry__._builder().build()
+
+
+@pytest.fixture(scope="module")
+def vc():
+    _build()
+    import lossless_compressed_kv_gb300 as m
+    return m
+
+
+def declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"VC_API[^;(]*?\b(vc_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared()
+    for n in ("vc_compress", "vc_draft_attn", "vc_verify_attn", "vc_accept"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(vc):
+    out = subprocess.run(["nm", "-D", "--defined-only", vc.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(vc_\w+)", out))
+    missing = [n for n in declared() if n not in exported]
+    assert not missing, missing
+    for n in declared():
+        getattr(vc.library(), n)
+
+
+def test_page_sizes_follow_the_layout(vc):
+    # bf16: 16 x D x 2 bytes per head; b bits: codes 16*D*b/8 + scales/zeros 2*16*D/32*2
+    assert vc.head_block_bytes(128, 16) == 4096
+    assert vc.head_block_bytes(128, 2) == 768
+    assert vc.head_block_bytes(128, 3) == 1024
+    assert vc.head_block_bytes(128, 4) == 1280
+    assert vc.head_block_bytes(64, 4) == 640
+    assert vc.page_bytes(8, 128, 2) == 8 * 768
+    assert vc.head_block_bytes(128, 5) == 0          # unsupported width
+
+
+def test_struct_layout_matches_c(vc):
+    assert C.sizeof(vc.KVFormat) == 12
+    assert C.sizeof(vc.PagedKVStruct) == 64
+
+
+def test_host_side_argument_errors(vc):
+    L = vc.library()
+    assert L.vc_compress(None, None, None, None, 0, None, None, None) == 1
+    assert L.vc_draft_attn(None, 4, None, 1.0, None, 0, None, 0, None, None) == 1
+    assert L.vc_verify_attn(None, 1, 4, None, 1.0, None, 0, None, 0, None, None) == 1
+    assert L.vc_accept(None, 1, 1, 1, None, 1, 1, None, 0, None, None, None, None, 0, None) == 1
+    fake = C.c_void_p(16)   # never dereferenced: validation fails first
+    fmt = vc.KVFormat(2, 128, 5)                      # 5 bits: unsupported
+    s = vc.PagedKVStruct(fake.value, fake.value, 4, fake.value, fake.value, 1, 1, fmt)
+    assert L.vc_draft_attn(fake, 4, C.byref(s), 1.0, fake, 16, fake, 1 << 20, None, None) == 2
+    fmt = vc.KVFormat(2, 128, 16)
+    s = vc.PagedKVStruct(fake.value, fake.value, 4, fake.value, fake.value, 1, 1, fmt)
+    assert L.vc_verify_attn(fake, 65, 4, C.byref(s), 1.0, fake, 16, fake, 1 << 20, None, None) == 2  # n_q > 64
+    assert L.vc_verify_attn(fake, 4, 5, C.byref(s), 1.0, fake, 16, fake, 1 << 20, None, None) == 2   # 5 % 2 != 0
+    # accept: n_pred must be x or x + 1
+    assert L.vc_accept(fake, 1, 5, 1, fake, 4, 10, fake, 2, fake, fake, fake, fake, 1 << 20, None) == 1
+    assert vc.STATUS[L.vc_accept(fake, 1, 3, 1, fake, 4, 10, fake, 2, fake, fake, fake, None, 0, None)] \
+        == "VC_ERR_WORKSPACE"
+    assert L.vc_status_string(7) == b"workspace missing or too small"
+
+
+def test_oracle_and_library_share_no_code():
+    """The CUDA sources and the oracle do not include or import each other."""
+    csrc = os.path.join(ROOT, "lossless_compressed_kv_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert "oracle" not in open(os.path.join(csrc, f)).read().lower()
+    for f in ("vc_oracle.c", "__init__.py"):
+        txt = open(os.path.join(ROOT, "oracle", f)).read()
+        assert not re.search(r"(import|from)\s+lossless_compressed_kv_gb300", txt)
+        assert "#include \"vc" not in txt and "libvc.so" not in txt
+    pkg = open(os.path.join(ROOT, "lossless_compressed_kv_gb300", "__init__.py")).read()
+    assert "import oracle" not in pkg and "from oracle" not in pkg

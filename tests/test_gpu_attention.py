@@ -1,0 +1,290 @@
+"""GPU vc_draft_attn / vc_verify_attn / vc_mixed_attn against the oracle.
+
+Tolerance (attention outputs, fp32 accumulation over bf16 / dequantised
+inputs): per output row max_i |o_gpu - o_ref| <= 2e-3 * ||o_ref||_2.
+Shapes span several pages, context chunks and a ragged tail; the edge cases
+are a single token, an exact page, an empty request and every GQA group
+size up to 8.  The full-size workloads are checked on every draft row and on
+sampled verification rows."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import vc_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def vc():
+    import lossless_compressed_kv_gb300 as m
+    return m
+
+
+def compress_all(full, comp, kept_lists):
+    offs, idx = synth.csr(kept_lists)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vc().compress(full, H.to_dev(offs), H.to_dev(idx), comp, max(1, max(len(k) for k in kept_lists)), status=st)
+    comp.seq_lens.copy_(torch.tensor([len(k) for k in kept_lists], dtype=torch.int32))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+
+def gpu_draft(comp, q, scale, max_len):
+    m = vc()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, m.draft_workspace_bytes(comp, q.shape[1], max_len)), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.draft_attn(q, comp, scale, out, max_len, ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return out.cpu().numpy()
+
+
+def gpu_verify(full, q, scale, max_len):
+    m = vc()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, m.verify_workspace_bytes(full, q.shape[1], q.shape[2], max_len)), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.verify_attn(q, full, scale, out, max_len, ws, status=st)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(st.item())
+
+
+def q_bf16(rng, shape):
+    qn = synth.normal_bf16(rng, shape)
+    return qn, H.to_dev(qn.view(np.int16)).view(torch.bfloat16)
+
+
+# --------------------------------------------------------------- draft
+
+DRAFT_CASES = [
+    # bits, d, hkv, grp, lens
+    (2, 128, 2, 4, [1, 16, 17, 700, 5000]),
+    (3, 128, 2, 4, [33, 4097]),
+    (4, 128, 1, 8, [300, 64]),
+    (16, 128, 2, 8, [2100, 15]),
+    (2, 64, 3, 1, [90, 1000]),
+    (3, 64, 1, 2, [129]),
+    (4, 64, 2, 4, [1, 2, 3]),
+    (16, 64, 1, 4, [513, 31]),
+]
+
+
+@pytest.mark.parametrize("bits,d,hkv,grp,lens", DRAFT_CASES)
+def test_draft_matches_oracle(bits, d, hkv, grp, lens):
+    rng = np.random.default_rng(bits * 1000 + d + hkv * 10 + grp)
+    full, hf = H.full_cache(rng, lens, hkv, d, synth.outlier_channels(rng, d, 2), 8.0)
+    kept = [np.arange(n, dtype=np.int32) if n < 100 else
+            np.sort(rng.choice(n, size=n // 2, replace=False)).astype(np.int32) for n in lens]
+    comp, ctable = H.comp_cache(rng, len(lens), [len(k) for k in kept], hkv, d, bits)
+    compress_all(full, comp, kept)
+    hq = hkv * grp
+    qn, qd = q_bf16(rng, (len(lens), hq, d))
+    scale = 1.0 / math.sqrt(d)
+    got = gpu_draft(comp, qd, scale, max(len(k) for k in kept))
+    for b in range(len(lens)):
+        k, v = H.logical_full(hf, b)
+        ref = oracle.draft_attn(qn[b], oracle.compress(k, v, kept[b], bits), float(np.float32(scale)))
+        assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
+
+
+def test_draft_empty_request_gives_zeros():
+    rng = np.random.default_rng(5)
+    full, hf = H.full_cache(rng, [40, 40], 1, 64)
+    comp, _ = H.comp_cache(rng, 2, 64, 1, 64, 4)
+    compress_all(full, comp, [np.arange(40, dtype=np.int32), np.zeros(0, np.int32)])
+    qn, qd = q_bf16(rng, (2, 4, 64))
+    got = gpu_draft(comp, qd, 0.125, 40)
+    assert np.all(got[1] == 0) and np.all(np.isfinite(got[0]))
+
+
+def test_draft_bad_page_id_reported():
+    rng = np.random.default_rng(6)
+    full, hf = H.full_cache(rng, [64], 1, 64)
+    comp, ctable = H.comp_cache(rng, 1, 64, 1, 64, 2)
+    compress_all(full, comp, [np.arange(64, dtype=np.int32)])
+    bt = comp.block_table.clone()
+    bt[0, 2] = comp.num_pages + 5                       # out of range: must be skipped, not read
+    bad = vc().PagedKV(comp.k_pages, comp.v_pages, bt, comp.seq_lens, 1, 64, 2)
+    qn, qd = q_bf16(rng, (1, 4, 64))
+    m = vc()
+    out = torch.empty((1, 4, 64), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.draft_workspace_bytes(bad, 4, 64), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.draft_attn(qd, bad, 0.125, out, 64, ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 3 and torch.isfinite(out).all()
+
+
+def test_draft_tiny_workload():
+    w = synth.WORKLOADS["tiny"]
+    rng = synth.rng_for("tiny")
+    oc = synth.outlier_channels(rng, w["d"], w["outliers"])
+    full, hf = H.full_cache(rng, [w["ctx"]], w["hkv"], w["d"], oc, w["outlier_scale"])
+    kept = [synth.kept_sink_recent_random(rng, w["ctx"], w["sink"], w["recent"], w["n_random"])]
+    comp, _ = H.comp_cache(rng, 1, 128, w["hkv"], w["d"], w["bits"])
+    compress_all(full, comp, kept)
+    qn, qd = q_bf16(rng, (1, w["hq"], w["d"]))
+    scale = 1.0 / math.sqrt(w["d"])
+    got = gpu_draft(comp, qd, scale, 128)
+    k, v = H.logical_full(hf, 0)
+    ref = oracle.draft_attn(qn[0], oracle.compress(k, v, kept[0], w["bits"]), float(np.float32(scale)))
+    assert H.row_err(got[0], ref) <= H.TOL
+
+
+@pytest.mark.parametrize("name", ["8b_32k_2bit", "70b_128k_drop4"])
+def test_draft_full_size_workloads(name):
+    """Every row of the full-size workloads (the launch configuration the
+    benchmark times), against the oracle over the same KV_comp."""
+    from concurrent.futures import ThreadPoolExecutor
+    w = synth.WORKLOADS[name]
+    rng = synth.rng_for(name)
+    oc = synth.outlier_channels(rng, w["d"], w["outliers"]) if w["outliers"] else ()
+    lens = [w["ctx"]] * w["batch"]
+    full, hf = H.full_cache(rng, lens, w["hkv"], w["d"], oc, w["outlier_scale"])
+    if w["bits"] == 16:
+        kept = [synth.kept_sink_recent_topk(rng, w["ctx"], w["sink"], w["recent"], w["kept_total"])
+                for _ in lens]
+    else:
+        kept = [np.arange(w["ctx"], dtype=np.int32)] * w["batch"]
+    comp, _ = H.comp_cache(rng, w["batch"], len(kept[0]), w["hkv"], w["d"], w["bits"])
+    compress_all(full, comp, kept)
+    qn, qd = q_bf16(rng, (w["batch"], w["hq"], w["d"]))
+    scale = 1.0 / math.sqrt(w["d"])
+    got = gpu_draft(comp, qd, scale, len(kept[0]))
+    del full, comp
+    with ThreadPoolExecutor(oracle.threads()) as pool:
+        for b in range(w["batch"]):
+            k, v = H.logical_full(hf, b)
+            ref = oracle.draft_attn(qn[b], oracle.compress(k, v, kept[b], w["bits"]), float(np.float32(scale)),
+                                    pool=pool)
+            assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
+
+
+# --------------------------------------------------------------- verify
+
+VERIFY_CASES = [
+    # d, hkv, grp, n_q, lens
+    (128, 2, 4, 8, [8, 9, 100, 4200]),
+    (128, 1, 8, 40, [40, 41, 1300]),
+    (128, 2, 4, 25, [25, 8193]),
+    (64, 1, 4, 9, [512, 9, 16]),
+    (64, 2, 2, 1, [1, 17, 4096, 4097]),
+    (128, 3, 1, 33, [700]),
+    (64, 1, 8, 64, [64, 200]),
+]
+
+
+@pytest.mark.parametrize("d,hkv,grp,n_q,lens", VERIFY_CASES)
+def test_verify_matches_oracle(d, hkv, grp, n_q, lens):
+    rng = np.random.default_rng(d + hkv * 3 + grp * 17 + n_q)
+    full, hf = H.full_cache(rng, lens, hkv, d, synth.outlier_channels(rng, d, 2), 8.0)
+    hq = hkv * grp
+    qn, qd = q_bf16(rng, (len(lens), n_q, hq, d))
+    scale = 1.0 / math.sqrt(d)
+    got, st = gpu_verify(full, qd, scale, max(lens))
+    assert st == 0
+    for b in range(len(lens)):
+        k, v = H.logical_full(hf, b)
+        ref = oracle.verify_attn_block(qn[b], k, v, float(np.float32(scale)))
+        assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
+
+
+def test_verify_short_request_reports_bad_index():
+    rng = np.random.default_rng(3)
+    full, hf = H.full_cache(rng, [4, 30], 1, 64)
+    qn, qd = q_bf16(rng, (2, 8, 4, 64))
+    got, st = gpu_verify(full, qd, 0.125, 30)
+    assert st == 3 and np.all(got[0] == 0) and np.all(np.isfinite(got[1]))
+
+
+def test_verify_rows_invariant_to_block_and_batch():
+    """A query's output is the same bits whether it is verified alone (n_q =
+    1, batch 1) or as row i of a block of 33 in a batch of 3: split
+    boundaries are fixed by position and rows are independent."""
+    rng = np.random.default_rng(11)
+    d, hkv, grp, n_q = 128, 2, 4, 33
+    lens = [5000, 9000, 333]
+    full, hf = H.full_cache(rng, lens, hkv, d)
+    qn, qd = q_bf16(rng, (3, n_q, hkv * grp, d))
+    blk, _ = gpu_verify(full, qd, 0.088, max(lens))
+    m = vc()
+    for i in (0, 7, 32):
+        # request 1 alone, truncated so that query i is the last position
+        L = lens[1] - n_q + i + 1
+        one = m.PagedKV(full.k_pages, full.v_pages, full.block_table[1:2].contiguous(),
+                        torch.tensor([L], dtype=torch.int32, device="cuda"), hkv, d, 16)
+        alone, st = gpu_verify(one, qd[1:2, i:i + 1].contiguous(), 0.088, L)
+        assert st == 0
+        assert np.array_equal(alone[0, 0], blk[1, i])
+
+
+@pytest.mark.parametrize("name,n_q", [("8b_32k_2bit", 32), ("8b_32k_2bit", 33), ("70b_128k_drop4", 40)])
+def test_verify_full_size_sampled(name, n_q):
+    """Full-size verification in the benchmark's launch configuration; 48
+    seeded (request, query, head) rows are recomputed one by one."""
+    from concurrent.futures import ThreadPoolExecutor
+    w = synth.WORKLOADS[name]
+    rng = synth.rng_for(name, 1)
+    lens = [w["ctx"] + n_q] * w["batch"]
+    full, hf = H.full_cache(rng, lens, w["hkv"], w["d"])
+    qn, qd = q_bf16(rng, (w["batch"], n_q, w["hq"], w["d"]))
+    scale = 1.0 / math.sqrt(w["d"])
+    got, st = gpu_verify(full, qd, scale, max(lens))
+    assert st == 0
+    del full
+    samp = np.random.default_rng(0)
+    with ThreadPoolExecutor(oracle.threads()) as pool:
+        for b in range(w["batch"]):
+            k, v = H.logical_full(hf, b)
+            qs = sorted(set([0, n_q - 1] + list(samp.integers(0, n_q, 2))))
+            hs = sorted(set(samp.integers(0, w["hq"], 3)))
+            ref = oracle.verify_attn(qn[b], k, v, float(np.float32(scale)), heads=hs, queries=qs, pool=pool)
+            for i in qs:
+                for h in hs:
+                    e = H.row_err(got[b, i, h], ref[i, h])
+                    assert e <= H.TOL, (b, i, h, e)
+
+
+# --------------------------------------------------------------- mixed
+
+def test_mixed_launch_matches_oracle_and_standalone():
+    """Staggered batch: even requests draft over 3-bit KV_comp, odd requests
+    verify x = 25 over KV_full, in one launch.  Draft rows match the oracle;
+    verify rows are bit-identical to the standalone verification kernel."""
+    rng = np.random.default_rng(44)
+    d, hkv, grp, n_q, bits = 128, 2, 4, 25, 3
+    lens = [3000, 2100, 700, 4500, 1234, 90]
+    role = np.array([b % 2 for b in range(len(lens))], np.int32)
+    full, hf = H.full_cache(rng, lens, hkv, d)
+    kept = [np.arange(n, dtype=np.int32) for n in lens]
+    comp, _ = H.comp_cache(rng, len(lens), lens, hkv, d, bits)
+    compress_all(full, comp, kept)
+    hq = hkv * grp
+    qdn, qdd = q_bf16(rng, (len(lens), hq, d))
+    qvn, qvd = q_bf16(rng, (len(lens), n_q, hq, d))
+    scale = 1.0 / math.sqrt(d)
+    m = vc()
+    od = torch.full((len(lens), hq, d), 7.0, device="cuda")
+    ov = torch.full((len(lens), n_q, hq, d), 7.0, device="cuda")
+    ws = torch.empty(m.mixed_workspace_bytes(comp, full, n_q, hq, max(lens)), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.mixed_attn(H.to_dev(role), qdd, comp, od, qvd, full, ov, scale, max(lens), ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    od, ov = od.cpu().numpy(), ov.cpu().numpy()
+    alone, _ = gpu_verify(full, qvd, scale, max(lens))
+    for b in range(len(lens)):
+        if role[b] == 0:
+            k, v = H.logical_full(hf, b)
+            ref = oracle.draft_attn(qdn[b], oracle.compress(k, v, kept[b], bits), float(np.float32(scale)))
+            assert H.row_err(od[b], ref) <= H.TOL
+            assert np.all(ov[b] == 7.0)           # other role's buffer untouched
+        else:
+            assert np.array_equal(ov[b], alone[b])
+            assert np.all(od[b] == 7.0)
