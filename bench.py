@@ -234,7 +234,7 @@ def draft_bytes(w, n_entries):
 # CPU oracle leg
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, st, seconds_target=12.0, max_requests=8):
+def oracle_sample(w, st, seconds_target=12.0, max_requests=64):
     """Time the oracle's draft attention on whole requests of the same
     workload (KV_comp built by the oracle's own compress from the same
     KV_full) until about `seconds_target` of CPU work."""
@@ -245,7 +245,18 @@ def oracle_sample(w, st, seconds_target=12.0, max_requests=8):
     full = st["full"]
     done, t_total, n_threads = 0, 0.0, oracle.threads()
     with ThreadPoolExecutor(n_threads) as pool:
-        for b in range(max_requests):
+        cache = {}
+        for it in range(max_requests):
+            b = it % w["batch"]
+            if b in cache:
+                q, comp = cache[b]
+                t0 = time.perf_counter()
+                oracle.draft_attn(q, comp, float(np.float32(1 / math.sqrt(d))), pool=pool)
+                t_total += time.perf_counter() - t0
+                done += 1
+                if t_total >= seconds_target:
+                    break
+                continue
             pages = full.block_table[b, :N // 16].long()
             k = full.k_pages[pages].view(torch.int16).view(-1, hkv, 16, d).permute(0, 2, 1, 3).reshape(N, hkv, d)
             v = full.v_pages[pages].view(torch.int16).view(-1, hkv, 16, d).permute(0, 2, 1, 3).reshape(N, hkv, d)
@@ -253,6 +264,7 @@ def oracle_sample(w, st, seconds_target=12.0, max_requests=8):
             v = v.cpu().numpy().view(np.uint16)
             q = st["q"][0, b].view(torch.int16).cpu().numpy().view(np.uint16)
             comp = oracle.compress(k, v, np.arange(N, dtype=np.int32), w["bits"])
+            cache[b] = (q, comp)
             t0 = time.perf_counter()
             oracle.draft_attn(q, comp, float(np.float32(1 / math.sqrt(d))), pool=pool)
             t_total += time.perf_counter() - t0
@@ -260,7 +272,7 @@ def oracle_sample(w, st, seconds_target=12.0, max_requests=8):
             if t_total >= seconds_target:
                 break
     return {"value": done / t_total, "unit": "tokens/s", "cores": n_threads, "kind": "oracle",
-            "sample": "%d request(s) x 1 draft step (32 query heads over 32768 2-bit KV_comp entries); "
+            "sample": "%d request-steps (cycling over the 8 requests) x 1 draft step (32 query heads over 32768 2-bit KV_comp entries); "
                       "KV_comp from the oracle's own compress; %.1f s of CPU time" % (done, t_total)}
 
 
@@ -361,7 +373,7 @@ def main():
         cpu = oracle_sample(w, st)
     traffic = None
     try:
-        with open(os.path.join(ROOT, "profiles", "draft_attn_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "draft_attn_traffic.txt")) as f:
             tj = json.load(f)
         if tj.get("kernel_source_hash") == source_hash():
             traffic = tj["bytes_per_launch"]

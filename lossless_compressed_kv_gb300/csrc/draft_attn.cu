@@ -78,10 +78,11 @@ int num_sms() {
 
 template <int BITS, int D>
 Plan plan(int batch, int hkv, int max_seq_len) {
+    // one full wave: at most SMs x resident CTAs work items, equal chunks
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
-    const int64_t target = (int64_t)num_sms() * occupancy<BITS, D>();
-    int splits = (int)((target + units - 1) / units);
+    const int64_t slots = (int64_t)num_sms() * occupancy<BITS, D>();
+    int splits = (int)(slots / units);
     splits = max(1, min(splits, ceil_div(max_pages, kWarps)));
     int chunk = ceil_div(max_pages, splits);
     chunk = max(kWarps, ceil_div(chunk, kWarps) * kWarps);
