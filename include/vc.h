@@ -84,6 +84,7 @@ extern "C" {
 #define VC_MAX_HEAD_DIM 256
 #define VC_MAX_GQA_GROUP 8
 #define VC_MAX_VERIFY_QUERIES 64
+#define VC_STATIC_SCRATCH_BYTES (8u << 20)
 
 typedef enum {
     VC_OK = 0,
@@ -162,6 +163,31 @@ VC_API size_t vc_draft_workspace_bytes(const vc_paged_kv *comp, int32_t num_q_he
 VC_API vc_status vc_draft_attn(const void *q, int32_t num_q_heads, const vc_paged_kv *comp,
                         float softmax_scale, float *out, int32_t max_seq_len, void *workspace,
                         size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * vc_draft_attn_static -- vc_draft_attn without a caller workspace.
+ * The pages have no counterpart of this entry point.  It is for callers that
+ * cannot allocate device memory where they call the library: a plugin run by
+ * a host engine that owns every device allocation and hands out no scratch
+ * buffer, or a latency-critical path that must not call cudaMalloc (which can
+ * synchronise the device).  Arguments and result are those of vc_draft_attn
+ * without the workspace; the caller still passes q, the cache and out.
+ * The split partials go to one fixed array of VC_STATIC_SCRATCH_BYTES (8 MiB)
+ * inside the library, held on every GPU that loads the library until the
+ * process exits.  The first call on a device looks up that array's device
+ * address (a one-time set-up per device); make that first call before any
+ * stream capture.  All calls share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU (several streams or threads) race,
+ * so the caller must serialise them.  Nothing in it needs clearing: a call
+ * writes every partial before it reads it.  A call that would need more
+ * than the array (vc_draft_workspace_bytes(comp, num_q_heads, max_seq_len) >
+ * VC_STATIC_SCRATCH_BYTES) returns VC_ERR_WORKSPACE and launches nothing.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+VC_API vc_status vc_draft_attn_static(const void *q, int32_t num_q_heads, const vc_paged_kv *comp,
+                                      float softmax_scale, float *out, int32_t max_seq_len,
+                                      int32_t *dev_status, vc_stream_t stream);
+VC_API size_t vc_static_scratch_bytes(void);
 
 /*
  * vc_verify_attn -- the verification pass over KV_full.  Request b holds
