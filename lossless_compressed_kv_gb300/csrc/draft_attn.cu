@@ -34,7 +34,7 @@ using draft::DraftArgs;
 constexpr int kWarps = 4;
 
 template <int BITS, int D>
-__global__ void __launch_bounds__(kWarps * 32) draft_kernel(DraftArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 4) draft_kernel(DraftArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     draft::draft_block<BITS, D, kWarps>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }

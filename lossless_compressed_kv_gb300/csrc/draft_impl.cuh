@@ -62,22 +62,46 @@ __device__ inline uint64_t win3(const uint32_t (&w)[WPR], int j) {
     return (j & 1) ? (x >> 16) : x;
 }
 
-// K operand (A, rows = tokens) for k-step ks, row token words w; the k-slot
-// to channel map of each bit width is mirrored by q_channel().
+// Codes enter the MMA as f16 subnormals: a code c masked in place at bit p
+// of a 16-bit half is the f16 value c * 2^(p - 24), exact (the tensor cores
+// do not flush subnormal operands).  The query operand of those k-slots is
+// pre-scaled by 2^-p, so every product is c * q * 2^-24 and the group scale
+// carries the 2^24.  Per-thread shift s and in-half positions (pl for
+// k-slots 2t, 2t+1; ph for 2t+8, 2t+9) keep every masked code below 2^10.
+template <int BITS>
+struct KPos {
+    int s, pl, ph;
+    __device__ explicit KPos(int t) {
+        if constexpr (BITS == 2) {
+            s = t < 2 ? 0 : (t == 2 ? 2 : 6);
+            pl = 4 * t - s;
+            ph = pl + 2;
+        } else if constexpr (BITS == 4) {
+            s = t < 2 ? 0 : 4 * t - 4;
+            pl = ph = 4 * t - s;
+        } else {
+            s = 0;
+            pl = ph = 0;
+        }
+    }
+};
+
+// K operand (A, rows = tokens) for k-step ks from one token row's words; the
+// k-slot -> channel map of each bit width is mirrored by q_channel().
 template <int BITS, int WPR>
-__device__ inline void k_pair(const uint32_t (&w)[WPR], int ks, int t, uint32_t &lo, uint32_t &hi) {
+__device__ inline void k_pair(const uint32_t (&w)[WPR], int ks, int t, const KPos<BITS> &kp, uint32_t &lo,
+                              uint32_t &hi) {
     if constexpr (BITS == 2) {
-        lo = codes_to_f16x2((w[ks] >> (4 * t)) & 0x00030003u);
-        hi = codes_to_f16x2((w[ks] >> (4 * t + 2)) & 0x00030003u);
+        const uint32_t y = w[ks] >> kp.s;  // channels (2t, 2t+8) at pl, (2t+1, 2t+9) at ph
+        lo = y & (0x00030003u << kp.pl);
+        hi = y & (0x00030003u << kp.ph);
     } else if constexpr (BITS == 4) {
-        lo = codes_to_f16x2((w[2 * ks] >> (4 * t)) & 0x000F000Fu);
-        hi = codes_to_f16x2((w[2 * ks + 1] >> (4 * t)) & 0x000F000Fu);
+        lo = (w[2 * ks] >> kp.s) & (0x000F000Fu << kp.pl);      // channels (t, t+4)
+        hi = (w[2 * ks + 1] >> kp.s) & (0x000F000Fu << kp.pl);  // channels (8+t, 12+t)
     } else {  // 3
         const uint64_t x = win3<WPR>(w, ks);
-        const uint32_t a = (uint32_t)((x >> (6 * t)) & 7u) | ((uint32_t)((x >> (6 * t + 24)) & 7u) << 16);
-        const uint32_t b = (uint32_t)((x >> (6 * t + 3)) & 7u) | ((uint32_t)((x >> (6 * t + 27)) & 7u) << 16);
-        lo = codes_to_f16x2(a);
-        hi = codes_to_f16x2(b);
+        lo = (uint32_t)((x >> (6 * t)) & 7u) | ((uint32_t)((x >> (6 * t + 24)) & 7u) << 16);
+        hi = (uint32_t)((x >> (6 * t + 3)) & 7u) | ((uint32_t)((x >> (6 * t + 27)) & 7u) << 16);
     }
 }
 
@@ -98,27 +122,53 @@ __device__ inline int q_channel(int ks, int slot) {
     }
 }
 
-// V operand (A, rows = channels of m-tile mt, columns = token pair (a, b)).
-// wa/wb: code rows of tokens a and b.  row_lo -> channel 16 mt + g,
-// row_hi -> channel 16 mt + 8 + g.
+// V operand (A, rows = channels of m-tile mt, k-slot pair = tokens (a, b)):
+// row_lo -> channel 16 mt + g, row_hi -> channel 16 mt + 8 + g.  A byte
+// permute brings the byte holding channel g of both tokens into the two
+// halves, a mask keeps the code in place (f16 subnormal c * 2^(vp - 24),
+// vp = v_pos(g)); the thread's output rows are rescaled by 2^(24 - vp).
+template <int BITS>
+__device__ inline int v_pos(int g) {
+    return BITS == 2 ? 2 * (g & 3) : BITS == 4 ? 4 * (g & 1) : 0;
+}
 template <int BITS, int WPR>
 __device__ inline void v_pair(const uint32_t (&wa)[WPR], const uint32_t (&wb)[WPR], int mt, int g,
                               uint32_t &row_lo, uint32_t &row_hi) {
     if constexpr (BITS == 2) {
-        const uint32_t x = __byte_perm(wa[mt], wb[mt], 0x5410);
-        const uint32_t y = __byte_perm(wa[mt], wb[mt], 0x7632);
-        row_lo = codes_to_f16x2((x >> (2 * g)) & 0x00030003u);
-        row_hi = codes_to_f16x2((y >> (2 * g)) & 0x00030003u);
+        const uint32_t bi = g >> 2, bh = bi + 2;
+        const uint32_t sl = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
+        const uint32_t sh = bh | (bh << 4) | ((4 + bh) << 8) | ((4 + bh) << 12);
+        const uint32_t m = 0x00030003u << (2 * (g & 3));
+        row_lo = __byte_perm(wa[mt], wb[mt], sl) & m;
+        row_hi = __byte_perm(wa[mt], wb[mt], sh) & m;
     } else if constexpr (BITS == 4) {
-        const uint32_t sel = g < 4 ? 0x5410u : 0x7632u;
-        const int sh = 4 * (g & 3);
-        row_lo = codes_to_f16x2((__byte_perm(wa[2 * mt], wb[2 * mt], sel) >> sh) & 0x000F000Fu);
-        row_hi = codes_to_f16x2((__byte_perm(wa[2 * mt + 1], wb[2 * mt + 1], sel) >> sh) & 0x000F000Fu);
+        const uint32_t bi = g >> 1;
+        const uint32_t sl = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
+        const uint32_t m = 0x000F000Fu << (4 * (g & 1));
+        row_lo = __byte_perm(wa[2 * mt], wb[2 * mt], sl) & m;
+        row_hi = __byte_perm(wa[2 * mt + 1], wb[2 * mt + 1], sl) & m;
     } else {
         const uint64_t xa = win3<WPR>(wa, mt), xb = win3<WPR>(wb, mt);
-        row_lo = codes_to_f16x2((uint32_t)((xa >> (3 * g)) & 7u) | ((uint32_t)((xb >> (3 * g)) & 7u) << 16));
-        row_hi = codes_to_f16x2((uint32_t)((xa >> (24 + 3 * g)) & 7u) |
-                                ((uint32_t)((xb >> (24 + 3 * g)) & 7u) << 16));
+        row_lo = (uint32_t)((xa >> (3 * g)) & 7u) | ((uint32_t)((xb >> (3 * g)) & 7u) << 16);
+        row_hi = (uint32_t)((xa >> (24 + 3 * g)) & 7u) | ((uint32_t)((xb >> (24 + 3 * g)) & 7u) << 16);
+    }
+}
+
+// NG fp16 values (one token's scales or zeros) as floats.
+template <int NG>
+__device__ inline void load_halves(const __half *p, float (&f)[NG]) {
+    if constexpr (NG == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else if constexpr (NG == 2) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u));
+        f[0] = a.x; f[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < NG; ++i) f[i] = __half2float(p[i]);
     }
 }
 
@@ -169,6 +219,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     // ---- query fragments (B operand of S^T = K Q^T), row n = head g ----
     const bool head_ok = g < a.grp;
     const uint16_t *qrow = a.q + ((int64_t)b * a.hq + kvh * a.grp + (head_ok ? g : 0)) * D;
+    const KPos<BITS> kpos(t);
     uint32_t bq[C::NT][2];
 #pragma unroll
     for (int ks = 0; ks < C::NT; ++ks) {
@@ -182,8 +233,10 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             bq[ks][0] = pack_bf16(v[0], v[1]);
             bq[ks][1] = pack_bf16(v[2], v[3]);
         } else {
-            bq[ks][0] = pack_f16(v[0], v[1]);
-            bq[ks][1] = pack_f16(v[2], v[3]);
+            const float fl = __uint_as_float((uint32_t)(127 - kpos.pl) << 23);  // 2^-pl
+            const float fh = __uint_as_float((uint32_t)(127 - kpos.ph) << 23);
+            bq[ks][0] = pack_f16(v[0] * fl, v[1] * fl);
+            bq[ks][1] = pack_f16(v[2] * fh, v[3] * fh);
         }
     }
     // per-group query sums of the two head columns this thread accumulates
@@ -247,8 +300,13 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             load_row<C::CB>(w1, kb + slot1 * C::CB);
             const __half *scl = reinterpret_cast<const __half *>(kb + kPage * C::CB);
             const __half *zer = scl + kPage * C::NG;
+            float sc0[C::NG], sc1[C::NG], zr0[C::NG], zr1[C::NG];
+            load_halves<C::NG>(scl + slot0 * C::NG, sc0);
+            load_halves<C::NG>(scl + slot1 * C::NG, sc1);
+            load_halves<C::NG>(zer + slot0 * C::NG, zr0);
+            load_halves<C::NG>(zer + slot1 * C::NG, zr1);
+            const float kscale = a.scale_log2 * 16777216.0f;  // products carry 2^-24
             s[0] = s[1] = s[2] = s[3] = 0.0f;
-            float sc0, sc1, zr0, zr1;
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -256,19 +314,15 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int ks = 2 * gr + h2;
                     uint32_t af[4];
-                    k_pair<BITS, C::WPR>(w0, ks, t, af[0], af[2]);
-                    k_pair<BITS, C::WPR>(w1, ks, t, af[1], af[3]);
+                    k_pair<BITS, C::WPR>(w0, ks, t, kpos, af[0], af[2]);
+                    k_pair<BITS, C::WPR>(w1, ks, t, kpos, af[1], af[3]);
                     mma_f16(acc, af, bq[ks][0], bq[ks][1]);
                 }
-                sc0 = __half2float(scl[slot0 * C::NG + gr]);
-                sc1 = __half2float(scl[slot1 * C::NG + gr]);
-                zr0 = __half2float(zer[slot0 * C::NG + gr]);
-                zr1 = __half2float(zer[slot1 * C::NG + gr]);
-                const float f0 = sc0 * a.scale_log2, f1 = sc1 * a.scale_log2;
-                s[0] = fmaf(f0, acc[0], fmaf(zr0, qg[gr][0], s[0]));
-                s[1] = fmaf(f0, acc[1], fmaf(zr0, qg[gr][1], s[1]));
-                s[2] = fmaf(f1, acc[2], fmaf(zr1, qg[gr][0], s[2]));
-                s[3] = fmaf(f1, acc[3], fmaf(zr1, qg[gr][1], s[3]));
+                const float f0 = sc0[gr] * kscale, f1 = sc1[gr] * kscale;
+                s[0] = fmaf(f0, acc[0], fmaf(zr0[gr], qg[gr][0], s[0]));
+                s[1] = fmaf(f0, acc[1], fmaf(zr0[gr], qg[gr][1], s[1]));
+                s[2] = fmaf(f1, acc[2], fmaf(zr1[gr], qg[gr][0], s[2]));
+                s[3] = fmaf(f1, acc[3], fmaf(zr1[gr], qg[gr][1], s[3]));
             }
         }
         // mask positions past the request length (their slots may hold garbage)
@@ -331,14 +385,17 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             load_row<C::CB>(wd, vb + (2 * t + 9) * C::CB);
             const __half *vscl = reinterpret_cast<const __half *>(vb + kPage * C::CB);
             const __half *vzer = vscl + kPage * C::NG;
+            // V scale / zero of this thread's tokens (slot0, slot1); slots past
+            // the end contribute exactly nothing, whatever their bytes hold
+            float vsc0[C::NG], vsc1[C::NG], vze0[C::NG], vze1[C::NG];
+            load_halves<C::NG>(vscl + slot0 * C::NG, vsc0);
+            load_halves<C::NG>(vscl + slot1 * C::NG, vsc1);
+            load_halves<C::NG>(vzer + slot0 * C::NG, vze0);
+            load_halves<C::NG>(vzer + slot1 * C::NG, vze1);
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
-                // V scale / zero of this thread's tokens (slot0, slot1); slots past
-                // the end contribute exactly nothing, whatever their bytes hold
-                const float vs0 = valid0 ? __half2float(vscl[slot0 * C::NG + gr]) : 0.0f;
-                const float vs1 = valid1 ? __half2float(vscl[slot1 * C::NG + gr]) : 0.0f;
-                const float vz0 = valid0 ? __half2float(vzer[slot0 * C::NG + gr]) : 0.0f;
-                const float vz1 = valid1 ? __half2float(vzer[slot1 * C::NG + gr]) : 0.0f;
+                const float vs0 = valid0 ? vsc0[gr] : 0.0f, vs1 = valid1 ? vsc1[gr] : 0.0f;
+                const float vz0 = valid0 ? vze0[gr] : 0.0f, vz1 = valid1 ? vze1[gr] : 0.0f;
                 zacc[gr][0] = fmaf(p[0], vz0, fmaf(p[2], vz1, zacc[gr][0]));
                 zacc[gr][1] = fmaf(p[1], vz0, fmaf(p[3], vz1, zacc[gr][1]));
                 const uint32_t e = pack_f16(p[0] * vs0, p[2] * vs1), od = pack_f16(p[1] * vs0, p[3] * vs1);
@@ -374,11 +431,14 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 zacc[gr][1] += __shfl_xor_sync(0xffffffffu, zacc[gr][1], off);
             }
         }
+        const float osc = __uint_as_float((uint32_t)(127 + 24 - v_pos<BITS>(g)) << 23);  // 2^(24 - vp)
 #pragma unroll
         for (int mt = 0; mt < C::NT; ++mt) {
             const int gr = mt / 2;
-            o[mt][0] += zacc[gr][0]; o[mt][2] += zacc[gr][0];
-            o[mt][1] += zacc[gr][1]; o[mt][3] += zacc[gr][1];
+            o[mt][0] = fmaf(o[mt][0], osc, zacc[gr][0]);
+            o[mt][2] = fmaf(o[mt][2], osc, zacc[gr][0]);
+            o[mt][1] = fmaf(o[mt][1], osc, zacc[gr][1]);
+            o[mt][3] = fmaf(o[mt][3], osc, zacc[gr][1]);
         }
     }
     // ---- combine the 4 warps of the CTA in shared memory ----
