@@ -260,6 +260,39 @@ VC_API vc_status vc_mixed_attn(const int32_t *role, const void *q_draft, const v
                         float softmax_scale, int32_t max_seq_len, void *workspace,
                         size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
 
+/*
+ * Decoder-layer operations for the end-to-end greedy loop (prefill, draft
+ * steps, verification pass).  "VeriCache: Making Lossy KV Compression
+ * Exact", "The Core Idea": drafter and verifier run the same model and
+ * weights, only the KV cache differs.  Every operation computes each row from
+ * that row alone with a fixed reduction order, so a token's results are the
+ * same bits whether it is processed alone, in a verification block or in a
+ * prefill chunk (this is what makes the loop reproduce full-cache greedy
+ * decoding exactly).  All pointers are device pointers; rows are m.
+ *  vc_embed          out[r] = table[ids[r]]  (fp32 [vocab][d]; a bad id gives
+ *                    zeros and VC_ERR_BAD_INDEX in dev_status)
+ *  vc_rmsnorm        out[r] = x[r] / sqrt(mean(x[r]^2) + eps) * weight (fp32)
+ *  vc_linear         out[r][n] (+)= sum_k bf16(x[r][k]) * W[k][n]: x fp32 [m][k]
+ *                    rounded to bf16 on load (activations are stored as bf16
+ *                    between layers), W bf16 [k][n], fp32 FMAs in increasing k;
+ *                    accumulate != 0 adds to out (residual connection)
+ *  vc_swiglu         out[r][c] = silu(gu[r][c]) * gu[r][f + c]  (fp32 [m][2f] -> [m][f])
+ *  vc_rope_kv_write  qkv fp32 [m][(Hq + 2 Hkv) D] -> q bf16 [m][Hq][D] after a
+ *                    rotary embedding (channel i pairs with i + D/2, angle
+ *                    pos * theta^(-2i/D)), and the row's rotated K and its V
+ *                    written as bf16 into `full` at (row_req[r], row_pos[r]).
+ */
+VC_API vc_status vc_embed(const int32_t *ids, int32_t m, const float *table, int32_t d, int32_t vocab,
+                          float *out, int32_t *dev_status, vc_stream_t stream);
+VC_API vc_status vc_rmsnorm(const float *x, int32_t m, int32_t d, const float *weight, float eps, float *out,
+                            vc_stream_t stream);
+VC_API vc_status vc_linear(const float *x, const void *w_bf16, float *out, int32_t m, int32_t k, int32_t n,
+                           int32_t accumulate, vc_stream_t stream);
+VC_API vc_status vc_swiglu(const float *gu, int32_t m, int32_t f, float *out, vc_stream_t stream);
+VC_API vc_status vc_rope_kv_write(const float *qkv, int32_t m, const int32_t *row_req, const int32_t *row_pos,
+                                  int32_t num_q_heads, float rope_theta, void *q_out, const vc_paged_kv *full,
+                                  int32_t *dev_status, vc_stream_t stream);
+
 VC_API const char *vc_status_string(vc_status s);
 VC_API const char *vc_version(void);
 

@@ -60,6 +60,14 @@ _SIG = {
                                               C.c_int32, C.c_int32]),
     "vc_mixed_attn": (C.c_int, [_P, _P, C.POINTER(PagedKVStruct), _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P,
                                 C.c_int32, C.c_float, C.c_int32, _P, C.c_size_t, _P, _P]),
+    "vc_embed": (C.c_int, [_P, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P, _P]),
+    "vc_rmsnorm": (C.c_int, [_P, C.c_int32, C.c_int32, _P, C.c_float, _P, _P]),
+    "vc_linear": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P]),
+    "vc_swiglu": (C.c_int, [_P, C.c_int32, C.c_int32, _P, _P]),
+    "vc_rope_kv_write": (C.c_int, [_P, C.c_int32, _P, _P, C.c_int32, C.c_float, _P, C.POINTER(PagedKVStruct), _P,
+                                   _P]),
+    "vc_draft_attn_static": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32, _P, _P]),
+    "vc_static_scratch_bytes": (C.c_size_t, []),
     "vc_status_string": (C.c_char_p, [C.c_int]),
     "vc_version": (C.c_char_p, []),
 }
@@ -225,3 +233,36 @@ def mixed_attn(role, q_draft, comp: PagedKV, out_draft, q_verify, full: PagedKV,
                               float(softmax_scale), int(max_seq_len), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
            "vc_mixed_attn")
+
+
+# ---------------------------------------------------------------------------
+# decoder-layer operations (end-to-end loop)
+# ---------------------------------------------------------------------------
+
+def embed(ids, table, out, status=None, stream=None):
+    _check(_lib.vc_embed(_ptr(ids), int(ids.numel()), _ptr(table), int(table.shape[1]), int(table.shape[0]),
+                         _ptr(out), _ptr(status), _stream(stream)), "vc_embed")
+
+
+def rmsnorm(x, weight, out, eps: float = 1e-5, stream=None):
+    _check(_lib.vc_rmsnorm(_ptr(x), int(x.shape[0]), int(x.shape[1]), _ptr(weight), float(eps), _ptr(out),
+                           _stream(stream)), "vc_rmsnorm")
+
+
+def linear(x, w_bf16, out, accumulate: bool = False, stream=None):
+    """out[m][n] (+)= bf16(x) @ W, x fp32 [m][k], W bf16 [k][n], out fp32."""
+    m, k = int(x.shape[0]), int(x.shape[1])
+    _check(_lib.vc_linear(_ptr(x), _ptr(w_bf16), _ptr(out), m, k, int(w_bf16.shape[1]), int(bool(accumulate)),
+                          _stream(stream)), "vc_linear")
+
+
+def swiglu(gu, out, stream=None):
+    _check(_lib.vc_swiglu(_ptr(gu), int(gu.shape[0]), int(out.shape[1]), _ptr(out), _stream(stream)), "vc_swiglu")
+
+
+def rope_kv_write(qkv, row_req, row_pos, num_q_heads: int, theta: float, q_out, full: PagedKV, status=None,
+                  stream=None):
+    fs = full.struct()
+    _check(_lib.vc_rope_kv_write(_ptr(qkv), int(qkv.shape[0]), _ptr(row_req), _ptr(row_pos), int(num_q_heads),
+                                 float(theta), _ptr(q_out), C.byref(fs), _ptr(status), _stream(stream)),
+           "vc_rope_kv_write")

@@ -100,7 +100,9 @@ __device__ __forceinline__ void verify_block(const VerifyArgs &a, int split, int
             const int row = rem / C::CHUNKS, ch = rem % C::CHUNKS;
             const uint8_t *src = (kv ? a.vp : a.kp) + off + row * D * 2 + ch * 16;
             uint8_t *dst = st + kv * C::TILE + swz<D>(row, ch);
-            if (ok) cp_async16(dst, src); else cp_async_zero16(dst, src);
+            // slots past the request length are zero-filled: their bytes may be
+            // anything (even NaN patterns) and 0 * NaN would leak into P V
+            if (ok && pg * kPage + row < len) cp_async16(dst, src); else cp_async_zero16(dst, src);
         }
     };
 

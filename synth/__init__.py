@@ -214,3 +214,22 @@ WORKLOADS = {
 
 def rng_for(name: str, salt: int = 0) -> np.random.Generator:
     return np.random.default_rng([WORKLOADS[name]["seed"], salt])
+
+
+def toy_weights(rng, w: dict) -> dict:
+    """Random-init weights of the toy decoder, N(0, w_std): bf16 projection
+    matrices [in][out], fp32 embedding table and LM head, unit norm weights."""
+    dm, hq, hkv, d, f, vocab, std = w["d_model"], w["hq"], w["hkv"], w["d"], w["ffn"], w["vocab"], w["w_std"]
+    out = {"embed": (rng.standard_normal((vocab, dm), dtype=np.float32) * np.float32(std)).astype(np.float32),
+           "lm_head": (rng.standard_normal((dm, vocab), dtype=np.float32) * np.float32(std)).astype(np.float32),
+           "final_norm": np.ones(dm, np.float32), "layers": []}
+    for _ in range(w["layers"]):
+        out["layers"].append({
+            "attn_norm": np.ones(dm, np.float32),
+            "wqkv": normal_bf16(rng, (dm, (hq + 2 * hkv) * d), std),
+            "wo": normal_bf16(rng, (hq * d, dm), std),
+            "mlp_norm": np.ones(dm, np.float32),
+            "wgu": normal_bf16(rng, (dm, 2 * f), std),
+            "wd": normal_bf16(rng, (f, dm), std),
+        })
+    return out

@@ -288,3 +288,44 @@ def test_mixed_launch_matches_oracle_and_standalone():
         else:
             assert np.array_equal(ov[b], alone[b])
             assert np.all(od[b] == 7.0)
+
+
+@pytest.mark.parametrize("bits", [2, 16])
+def test_garbage_past_the_end_never_leaks(bits):
+    """Slots past a request's length may hold any bytes (memory reused from
+    earlier work): fill them with NaN bit patterns and check that draft and
+    verification outputs stay finite and match the oracle."""
+    rng = np.random.default_rng(77)
+    d, hkv, grp, n_q = 128, 2, 4, 9
+    lens = [37, 100, 16 * 9 + 3]
+    full, hf = H.full_cache(rng, lens, hkv, d)
+    # poison every slot of the last page past each request's length
+    for b, n in enumerate(lens):
+        page = int(hf["table"][b][(n - 1) // 16])
+        for pool in (full.k_pages, full.v_pages):
+            blk = pool[page].view(torch.int16).view(hkv, 16, d)
+            blk[:, n % 16 or 16:, :] = -1          # 0xFFFF = bf16 NaN
+    qn, qd = q_bf16(rng, (len(lens), n_q, hkv * grp, d))
+    got, st = gpu_verify(full, qd, 0.088, max(lens))
+    assert st == 0 and np.isfinite(got).all()
+    for b in range(len(lens)):
+        k, v = H.logical_full(hf, b)
+        ref = oracle.verify_attn_block(qn[b], k, v, float(np.float32(0.088)))
+        assert H.row_err(got[b], ref) <= H.TOL
+    kept = [np.arange(n, dtype=np.int32) for n in lens]
+    comp, ctable = H.comp_cache(rng, len(lens), lens, hkv, d, bits)
+    compress_all(full, comp, kept)
+    for b, n in enumerate(lens):                    # poison KV_comp tails too
+        if n % 16:
+            page = int(ctable[b][(n - 1) // 16])
+            comp.k_pages[page].fill_(255)
+            comp.v_pages[page].fill_(255)
+    # re-write the valid slots of the poisoned pages, leaving the tails poisoned
+    compress_all(full, comp, kept)
+    qdn, qdd = q_bf16(rng, (len(lens), hkv * grp, d))
+    gd = gpu_draft(comp, qdd, 0.088, max(lens))
+    assert np.isfinite(gd).all()
+    for b in range(len(lens)):
+        k, v = H.logical_full(hf, b)
+        ref = oracle.draft_attn(qdn[b], oracle.compress(k, v, kept[b], bits), float(np.float32(0.088)))
+        assert H.row_err(gd[b], ref) <= H.TOL
