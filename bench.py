@@ -322,10 +322,17 @@ def main():
     ap.add_argument("--impl", default="vc", choices=["vc", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging"])
     args = ap.parse_args()
     rank, ws = dist_init()
     if args.impl == "reference":
         reference_main(args, rank, ws)
+        return
+    if args.workload != WORKLOAD:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        {"mixed_32req_3bit": mixed_main, "toy_e2e": toy_main, "staging": staging_main}[args.workload](args)
         return
     import torch
     import synth
@@ -448,6 +455,167 @@ def e2e_measure(w, st, rnd, args, ws, device):
             "d2h_bytes_per_step": d2h,
             "note": "KV_full (%.2f GB) staged from pinned host memory on a side stream each round, "
                     "overlapping the drafting" % (2 * nbytes / 1e9)}
+
+
+# ---------------------------------------------------------------------------
+# other workloads (not the headline line): staggered mixed batch, toy loop,
+# host -> device staging bandwidth
+# ---------------------------------------------------------------------------
+
+def staging_main(args):
+    """Pinned host -> device copy bandwidth, one stream and four streams."""
+    import torch
+    import lossless_compressed_kv_gb300 as vc
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    res = {}
+    for ns in (1, 2, 4):
+        streams = [torch.cuda.Stream() for _ in range(ns)]
+        part = n // ns
+        for it in range(args.warmup + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i, st in enumerate(streams):
+                vc.stage_async(d[i * part:], h[i * part:], part, st)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+        res["streams_%d_GBps" % ns] = n / dt / 1e9
+    print(json.dumps({"metric": "pinned host -> device staging GB/s", "bytes": n, **res}), flush=True)
+
+
+def mixed_main(args):
+    """Staggered mixed batch: 32 requests, contexts U[8192, 65536], 32q/8kv,
+    D 128, 3-bit KV_comp; even requests draft, odd ones verify x = 25 in one
+    launch, while the NEXT round's verifying requests' KV_full (odd requests
+    of the other parity set) is staged from pinned host memory on a side
+    stream.  Reports tokens/s of both halves, the staging bandwidth and the
+    overlap efficiency (t_mixed + t_stage) / t_wall."""
+    import torch
+    import synth
+    import lossless_compressed_kv_gb300 as vc
+    w = dict(synth.WORKLOADS["mixed_32req_3bit"])
+    B, hq, hkv, d, x, bits = w["batch"], w["hq"], w["hkv"], w["d"], w["x"], w["bits"]
+    rng = np.random.default_rng(w["seed"])
+    lens = rng.integers(w["ctx_lo"], w["ctx_hi"] + 1, size=B).astype(np.int64)
+    role = np.array([b % 2 for b in range(B)], np.int32)
+    full_lens = lens + x                            # verifying requests hold the block too
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(w["seed"])
+    npg = [(int(n) + 15) // 16 for n in full_lens]
+    maxb = max(npg)
+    table = torch.full((B, maxb), -1, dtype=torch.int32)
+    o = 0
+    for b in range(B):
+        table[b, :npg[b]] = torch.arange(o, o + npg[b], dtype=torch.int32)
+        o += npg[b]
+    P = o
+    pb = vc.page_bytes(hkv, d, 16)
+    kp = torch.empty((P, pb // 2), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    for s0 in range(0, P, 4096):
+        e = min(P, s0 + 4096)
+        kp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=dev).to(torch.bfloat16)
+        vp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=dev).to(torch.bfloat16)
+    tdev = table.to(dev)
+    full = vc.PagedKV(kp.view(torch.uint8), vp.view(torch.uint8), tdev,
+                      torch.tensor(full_lens, dtype=torch.int32, device=dev), hkv, d, 16)
+    comp = vc.PagedKV.allocate(P, hkv, d, bits, tdev, torch.tensor(lens, dtype=torch.int32, device=dev))
+    kept = [np.arange(n, dtype=np.int32) for n in lens]
+    offs, idx = synth.csr(kept)
+    vc.compress(full, torch.from_numpy(offs).to(dev), torch.from_numpy(idx).to(dev), comp, int(lens.max()))
+    qd = torch.randn((B, hq, d), generator=g, device=dev).to(torch.bfloat16)
+    qv = torch.randn((B, x, hq, d), generator=g, device=dev).to(torch.bfloat16)
+    od = torch.empty((B, hq, d), dtype=torch.float32, device=dev)
+    ov = torch.empty((B, x, hq, d), dtype=torch.float32, device=dev)
+    msl = int(full_lens.max())
+    wsb = torch.empty(vc.mixed_workspace_bytes(comp, full, x, hq, msl), dtype=torch.uint8, device=dev)
+    roled = torch.from_numpy(role).to(dev)
+    # staging: the verifying requests' KV_full for the next round, pinned host -> device
+    ver_pages = sum(npg[b] for b in range(B) if role[b] == 1)
+    stage_bytes = ver_pages * pb
+    hk = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
+    hv = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
+    hk.fill_(0)
+    hv.fill_(0)
+    sk = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+    sv = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def mixed():
+        vc.mixed_attn(roled, qd, comp, od, qv, full, ov, 1.0 / math.sqrt(d), msl, wsb, status=status)
+
+    def stage():
+        vc.stage_async(sk, hk, stage_bytes, side)
+        vc.stage_async(sv, hv, stage_bytes, side)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn, n):
+        torch.cuda.synchronize()
+        ev[0].record()
+        for _ in range(n):
+            fn()
+        ev[1].record()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / n
+
+    for _ in range(max(3, args.warmup)):
+        mixed()
+    t_mixed = timed(mixed, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        stage()
+    torch.cuda.synchronize()
+    t_stage = (time.perf_counter() - t0) * 1e3 / args.steps
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        stage()
+        mixed()
+    torch.cuda.synchronize()
+    t_wall = (time.perf_counter() - t0) * 1e3 / args.steps
+    assert status.item() == 0
+    nd = int((role == 0).sum())
+    nv = int((role == 1).sum())
+    comp_bytes = sum(int(lens[b]) for b in range(B) if role[b] == 0) * hkv * 2 * (d * bits // 8 + 4 * d // 32)
+    full_bytes = sum(int(full_lens[b]) for b in range(B) if role[b] == 1) * hkv * 2 * d * 2
+    flops = sum(2 * 2 * x * hq * int(full_lens[b]) * d for b in range(B) if role[b] == 1)
+    line = {"metric": "staggered mixed batch: draft + verify attention in one launch", "workload": "mixed_32req_3bit",
+            "config": {"batch": B, "ctx": "U[%d,%d]" % (w["ctx_lo"], w["ctx_hi"]), "q_heads": hq, "kv_heads": hkv,
+                       "head_dim": d, "bits": bits, "x": x, "drafting": nd, "verifying": nv},
+            "ms_mixed_launch": t_mixed, "ms_stage": t_stage, "ms_wall_stage_and_mixed": t_wall,
+            "overlap_efficiency": (t_mixed + t_stage) / t_wall,
+            "draft_tokens_per_s": nd / (t_mixed * 1e-3), "verify_tokens_per_s": nv * x / (t_mixed * 1e-3),
+            "algorithmic_GBps": (comp_bytes + full_bytes) / (t_mixed * 1e-3) / 1e9,
+            "verify_tflops": flops / (t_mixed * 1e-3) / 1e12, "stage_GBps": 2 * stage_bytes / (t_stage * 1e-3) / 1e9,
+            "stage_bytes": 2 * stage_bytes}
+    print(json.dumps(line), flush=True)
+
+
+def toy_main(args):
+    """End-to-end toy loop (batch 4, 16384-token prompt, 512 tokens, x = 32,
+    4-bit KV_comp): wall time of the VeriCache rounds and of full-KV greedy
+    decoding from the same prefilled state, identical outputs checked."""
+    import torch
+    import synth
+    from lossless_compressed_kv_gb300 import toy
+    w = dict(synth.WORKLOADS["toy_e2e"])
+    t0 = time.perf_counter()
+    r = toy.run(w, timed=True)
+    line = {"metric": "toy decoder greedy tokens/s: VeriCache rounds vs full-KV decoding", "workload": "toy_e2e",
+            "config": {k: w[k] for k in ("batch", "layers", "d_model", "hq", "hkv", "d", "ffn", "vocab", "prompt",
+                                         "bits", "x", "gen")},
+            "identical_outputs": bool(np.array_equal(r["vericache"].numpy(), r["full"].numpy())),
+            "rounds": r["stats"]["rounds"], "mean_accepted_per_round": r["stats"]["mean_accepted"],
+            "vericache_tokens_per_s": w["batch"] * w["gen"] / r["stats"]["t_vericache"],
+            "full_kv_tokens_per_s": w["batch"] * w["gen"] / r["stats"]["t_full"],
+            "note": "host loop in Python driving the C ABI; KV_full resident in HBM; wall %.1f s" %
+                    (time.perf_counter() - t0)}
+    print(json.dumps(line), flush=True)
 
 
 def source_hash():

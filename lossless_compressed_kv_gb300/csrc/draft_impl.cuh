@@ -33,7 +33,9 @@ struct Cfg {
     static constexpr int STAGE = 2 * HB;
     static constexpr int RING = NW * NSTAGE * STAGE;
     static constexpr int COMBINE = NW * 8 * (D + 2) * 4;
-    static constexpr int SMEM = (RING > COMBINE ? RING : COMBINE) + NW * NSTAGE * 8;
+    static constexpr int BARS = NW * NSTAGE * 8;
+    static constexpr int QS = 8 * D * 2 + 8 * NG * 4;  // q of the group (bf16) + its group sums
+    static constexpr int SMEM = (RING > COMBINE ? RING : COMBINE) + BARS + QS;
 };
 
 // Load one token row of packed codes (CB bytes) as 32-bit words.
@@ -216,9 +218,25 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     if (lane == 0)
         for (int k = 0; k < min(nw, C::NSTAGE); ++k) issue(k);
 
-    // ---- query fragments (B operand of S^T = K Q^T), row n = head g ----
-    const bool head_ok = g < a.grp;
-    const uint16_t *qrow = a.q + ((int64_t)b * a.hq + kvh * a.grp + (head_ok ? g : 0)) * D;
+    // ---- the group's queries, staged once per CTA in shared memory ----
+    uint16_t *qs = reinterpret_cast<uint16_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE) + C::BARS);
+    float *qsum = reinterpret_cast<float *>(qs + 8 * D);  // [8 heads][NG] group sums, pre-scaled
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.hq + kvh * a.grp) * D);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(qs);
+        for (int e = threadIdx.x; e < 8 * D / 2; e += NW * 32) dst[e] = e < a.grp * D / 2 ? src[e] : 0u;
+        __syncthreads();
+        if constexpr (BITS != 16) {
+            for (int e = threadIdx.x; e < 8 * C::NG; e += NW * 32) {
+                const int n = e / C::NG, gr = e % C::NG;
+                float sum = 0.0f;
+                for (int i = 0; i < kGroup; ++i) sum += bf16_bits_to_f32(qs[n * D + gr * kGroup + i]);
+                qsum[e] = sum * a.scale_log2;
+            }
+            __syncthreads();
+        }
+    }
+    // ---- query fragments (B operand of S^T = K Q^T), column n = head g ----
     const KPos<BITS> kpos(t);
     uint32_t bq[C::NT][2];
 #pragma unroll
@@ -227,7 +245,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int slot = (j & 1) + 2 * t + 8 * (j >> 1);
-            v[j] = head_ok ? bf16_bits_to_f32(qrow[q_channel<BITS>(ks, slot)]) : 0.0f;
+            v[j] = bf16_bits_to_f32(qs[g * D + q_channel<BITS>(ks, slot)]);
         }
         if constexpr (BITS == 16) {
             bq[ks][0] = pack_bf16(v[0], v[1]);
@@ -243,16 +261,9 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     float qg[C::NG][2];
     if constexpr (BITS != 16) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int h = 2 * t + j;
-            const uint16_t *qr = a.q + ((int64_t)b * a.hq + kvh * a.grp + (h < a.grp ? h : 0)) * D;
-#pragma unroll
-            for (int gr = 0; gr < C::NG; ++gr) {
-                float s = 0.0f;
-                if (h < a.grp)
-                    for (int i = 0; i < kGroup; ++i) s += bf16_bits_to_f32(qr[gr * kGroup + i]);
-                qg[gr][j] = s * a.scale_log2;
-            }
+        for (int gr = 0; gr < C::NG; ++gr) {
+            qg[gr][0] = qsum[(2 * t) * C::NG + gr];
+            qg[gr][1] = qsum[(2 * t + 1) * C::NG + gr];
         }
     }
 

@@ -28,7 +28,7 @@ using verify::kSplitPages;
 namespace {
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) verify_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(verify::kMaxWarps * 32) verify_kernel(VerifyArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     verify::verify_block<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }
@@ -45,8 +45,13 @@ cudaError_t launch(const VerifyArgs &a, int batch, cudaStream_t st) {
         cudaFuncSetAttribute(verify_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, VCfg<D>::SMEM);
         attr = true;
     }
-    dim3 grid(a.n_splits, ceil_div(a.n_q * a.grp, kRows), batch * a.hkv);
-    verify_kernel<D><<<grid, kWarps * 32, VCfg<D>::SMEM, st>>>(a);
+    // one warp per 16-row tile; as few CTAs per (request, kv head, split) as
+    // the 16-warp limit allows, rows spread evenly over them
+    const int tiles = ceil_div(a.n_q * a.grp, 16);
+    const int rb = ceil_div(tiles, verify::kMaxWarps);
+    const int warps = ceil_div(tiles, rb);
+    dim3 grid(a.n_splits, rb, batch * a.hkv);
+    verify_kernel<D><<<grid, warps * 32, VCfg<D>::SMEM, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return cudaSuccess;

@@ -8,8 +8,9 @@ namespace vc {
 namespace verify {
 
 
-constexpr int kWarps = 8;
-constexpr int kRows = kWarps * 16;      // rows per CTA
+constexpr int kWarps = 8;               // warps per CTA in the mixed launch
+constexpr int kRows = kWarps * 16;      // rows per CTA in the mixed launch
+constexpr int kMaxWarps = 16;           // standalone launch: one warp per m16 row tile
 constexpr int kSplitPages = 256;        // 4096 keys per split (fixed)
 constexpr int kStages = 4;
 
@@ -51,7 +52,8 @@ __device__ __forceinline__ void verify_block(const VerifyArgs &a, int split, int
     const int b = bk / a.hkv, kvh = bk % a.hkv;
     const int len = a.lens[b];
     const int nrows = a.n_q * a.grp;
-    const int row0 = rb * kRows + warp * 16;
+    const int nthreads = blockDim.x;
+    const int row0 = rb * (nthreads / 32) * 16 + warp * 16;
     const bool len_ok = len >= a.n_q;
     if (!len_ok && threadIdx.x == 0 && split == 0 && rb == 0 && kvh == 0) report(a.status, VC_ERR_BAD_INDEX);
     const int npages = len_ok ? ceil_div(len, kPage) : 0;
@@ -94,7 +96,7 @@ __device__ __forceinline__ void verify_block(const VerifyArgs &a, int split, int
         const bool ok = id >= 0 && id < a.n_pages;
         if (!ok && threadIdx.x == 0) report(a.status, VC_ERR_BAD_INDEX);
         const int64_t off = ((int64_t)(ok ? id : 0) * a.hkv + kvh) * C::TILE;
-        for (int c = threadIdx.x; c < 2 * kPage * C::CHUNKS; c += kWarps * 32) {
+        for (int c = threadIdx.x; c < 2 * kPage * C::CHUNKS; c += nthreads) {
             const int kv = c / (kPage * C::CHUNKS);
             const int rem = c % (kPage * C::CHUNKS);
             const int row = rem / C::CHUNKS, ch = rem % C::CHUNKS;

@@ -267,7 +267,7 @@ class ToyDecoder:
         return torch.tensor([g[:n_tokens] for g in gen], dtype=torch.int32)
 
 
-def run(w: dict, device="cuda", prompt=None, n_gen=None, batch=None, seed=None):
+def run(w: dict, device="cuda", prompt=None, n_gen=None, batch=None, seed=None, timed=False):
     """Prefill, then decode n_gen tokens per request twice from the same
     state: with VeriCache rounds and with plain full-KV greedy decoding.
     Returns dict(vericache ids, full-KV ids, stats, first tokens)."""
@@ -292,8 +292,14 @@ def run(w: dict, device="cuda", prompt=None, n_gen=None, batch=None, seed=None):
     for li in range(s.layers):
         vc.compress(model.view(full_a[li], lensP), offs, idx, comp[li], P, status=model.status)
     stats = {}
+    import time
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     ids_vc = model.vericache(first, full_a, comp, P, G, stats)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
     ids_ref = model.greedy_full(first, full_b, P, G).cpu()
     torch.cuda.synchronize()
+    stats["t_vericache"], stats["t_full"] = t1 - t0, time.perf_counter() - t1
     stats["status"] = int(model.status.item())
     return dict(vericache=ids_vc, full=ids_ref, stats=stats, prompt=ids, weights=weights, first=first.cpu())
