@@ -7,24 +7,26 @@
 // Drafting is HBM-bandwidth bound, verification brings dense tensor work, so
 // one grid holding both keeps both busy.  Blocks [0, Nv) run the
 // verification body for requests with role 1, blocks [Nv, Nv + Nd) the
-// draft body (8 warps) for requests with role 0; a block whose request has
+// draft body (6 warps) for requests with role 0; a block whose request has
 // the other role exits at once.  One combine launch finishes both.
 #include "draft_impl.cuh"
-#include "verify_impl.cuh"
+#include "verify_tc.cuh"
 
 namespace vc {
 int verify_splits(int max_seq_len);
-void verify_args(verify::VerifyArgs &a, const void *q, int n_q, int hq, const vc_paged_kv &f, float scale,
+bool verify_args(vtc::Args &a, const void *q, int n_q, int hq, const vc_paged_kv &f, float scale,
                  int max_seq_len, void *ws, int32_t *status);
 
 namespace {
 
-constexpr int kThreads = 256;
+// the verification body of one 128-row tile needs 4 softmax warps, a
+// producer warp and an MMA warp; draft blocks use the same 6 warps
+constexpr int kThreads = vtc::Cfg<128, 1>::THREADS;
 constexpr int kDraftWarps = kThreads / 32;
 
 struct MixedArgs {
     draft::DraftArgs d;
-    verify::VerifyArgs v;
+    vtc::Args v;
     const int32_t *role;
     int n_verify_blocks, rb;
 };
@@ -32,20 +34,20 @@ struct MixedArgs {
 template <int BITS, int D>
 struct MCfg {
     static constexpr int DS = draft::Cfg<BITS, D, kDraftWarps>::SMEM;
-    static constexpr int VS = verify::VCfg<D>::SMEM;
+    static constexpr int VS = vtc::Cfg<D, 1>::SMEM;
     static constexpr int SMEM = DS > VS ? DS : VS;
 };
 
 template <int BITS, int D>
-__global__ void __launch_bounds__(kThreads) mixed_kernel(MixedArgs m) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ MixedArgs m) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     int bid = blockIdx.x;
     if (bid < m.n_verify_blocks) {
         const int split = bid % m.v.n_splits;
         const int rest = bid / m.v.n_splits;
         const int rb = rest % m.rb, bk = rest / m.rb;
         if (m.role[bk / m.v.hkv] != 1) return;
-        verify::verify_block<D>(m.v, split, rb, bk, smem);
+        vtc::verify_tc_block<D, 1>(m.v, split, rb, bk, smem);
     } else {
         bid -= m.n_verify_blocks;
         const int split = bid % m.d.n_splits;
@@ -65,7 +67,7 @@ __global__ void mixed_reduce_kernel(MixedArgs m, float *out_draft, float *out_ve
     } else {  // ((b * n_q + i) * Hq + h)
         const int r = row - draft_rows;
         if (m.role[r / (m.v.n_q * m.v.hq)] != 1) return;
-        verify::reduce_row<D>(m.v.ws_o, m.v.ws_ml, m.v.n_splits, r, out_verify, threadIdx.x, blockDim.x);
+        vtc::reduce_row<D>(m.v.ws_o, m.v.ws_ml, m.v.n_splits, r, out_verify, threadIdx.x, blockDim.x);
     }
 }
 
@@ -148,9 +150,9 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
     m.d.ws_ml = m.d.ws_o + (size_t)batch * hq * splits * d;
     m.d.status = status;
     void *vws = (uint8_t *)ws + draft_part(comp, hq, max_seq_len);
-    verify_args(m.v, q_verify, n_q, hq, full, scale, max_seq_len, vws, status);
+    if (!verify_args(m.v, q_verify, n_q, hq, full, scale, max_seq_len, vws, status)) return cudaErrorInvalidValue;
     m.role = role;
-    m.rb = ceil_div(n_q * m.v.grp, verify::kRows);
+    m.rb = ceil_div(n_q * m.v.grp, vtc::kTileRows);
     m.n_verify_blocks = m.v.n_splits * m.rb * batch * m.v.hkv;
 #define VC_L(B_, D_) launch<B_, D_>(m, batch, out_draft, out_verify, st)
     if (d == 64)

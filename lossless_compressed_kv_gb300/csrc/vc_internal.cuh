@@ -54,9 +54,11 @@ __device__ inline void mbar_arrive(uint64_t *bar) {
 
 __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
+    // suspend-time hint 20 us: a poll returns within that time even if the
+    // phase is still open, so the caller's wall-clock bound holds
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -64,14 +66,26 @@ __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls (each poll may itself block for
-// a short hardware-defined time), reports VC_ERR_TIMEOUT and returns false.
-constexpr uint32_t kWaitLimit = 1u << 22;
+__device__ inline uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: gives up after about 2 seconds of wall-clock time, reports
+// VC_ERR_TIMEOUT and returns false (the caller then drains and exits).
+constexpr uint64_t kWaitNs = 2000000000ull;
 __device__ inline bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *st) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    report(st, VC_ERR_TIMEOUT);
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) {
+            report(st, VC_ERR_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 // One bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).

@@ -1,65 +1,77 @@
-// vc_verify_attn: the verification pass over the full (bf16) cache.
+// vc_verify_attn: the verification pass over the full (bf16) cache on
+// tcgen05 / TMEM (see verify_tc.cuh for the design).
 //
 // "VeriCache: Making Lossy KV Compression Exact", section "The Core Idea"
 // items 3-5: one pass over KV_full checks all drafted positions in
 // parallel; query i of the block attends causally to every earlier position
 // and to itself ("KV Cache and Speculative Decoding": causal attention).
-//
-// Rows of the contraction are (query, head) pairs of one kv head's GQA
-// group: n_q * G rows share every K/V byte, which makes QK^T / PV a dense
-// contraction (128 rows for x = 32, G = 4).  Design:
-//  - CTA = 8 warps x 16 rows (one m16 tile each) of one (request, kv head),
-//    one split of 4096 keys (256 pages).  Splits are fixed by key position,
-//    the pages of a split are visited in order and the split partials are
-//    combined in split order, so a row's result never depends on n_q, on the
-//    row's place in the block or on the batch.
-//  - K/V pages staged in shared memory with cp.async (16-byte chunks, XOR
-//    swizzle so ldmatrix is conflict-free), 4-stage ring, one barrier/page.
-//  - S = Q K^T and O += P V on mma.sync m16n8k16 bf16, fp32 accumulate,
-//    online softmax in fp32 (log2 domain).
-#include "verify_impl.cuh"
+// Launch: one CTA per (split of 4096 keys, row block, request x kv head);
+// a row block holds up to two 128-row MMA tiles of (query, head) rows.
+#include "verify_tc.cuh"
 
 namespace vc {
-using verify::VerifyArgs;
-using verify::VCfg;
-using verify::kWarps;
-using verify::kRows;
-using verify::kSplitPages;
+using vtc::Args;
 namespace {
 
-template <int D>
-__global__ void __launch_bounds__(verify::kMaxWarps * 32) verify_kernel(VerifyArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    verify::verify_block<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
+template <int D, int QT>
+__global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS) verify_kernel(const __grid_constant__ Args a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    vtc::verify_tc_block<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }
 
 template <int D>
 __global__ void verify_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, float *out) {
-    verify::reduce_row<D>(ws_o, ws_ml, n_splits, blockIdx.x, out, threadIdx.x, blockDim.x);
+    vtc::reduce_row<D>(ws_o, ws_ml, n_splits, blockIdx.x, out, threadIdx.x, blockDim.x);
 }
 
-template <int D>
-cudaError_t launch(const VerifyArgs &a, int batch, cudaStream_t st) {
+template <int D, int QT>
+cudaError_t launch(Args &a, int batch, cudaStream_t st) {
+    using C = vtc::Cfg<D, QT>;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(verify_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, VCfg<D>::SMEM);
+        cudaFuncSetAttribute(verify_kernel<D, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         attr = true;
     }
-    // one warp per 16-row tile; as few CTAs per (request, kv head, split) as
-    // the 16-warp limit allows, rows spread evenly over them
-    const int tiles = ceil_div(a.n_q * a.grp, 16);
-    const int rb = ceil_div(tiles, verify::kMaxWarps);
-    const int warps = ceil_div(tiles, rb);
-    dim3 grid(a.n_splits, rb, batch * a.hkv);
-    verify_kernel<D><<<grid, warps * 32, VCfg<D>::SMEM, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return cudaSuccess;
+    a.rows_per_cta = QT * vtc::kTileRows;
+    dim3 grid(a.n_splits, ceil_div(a.n_q * a.grp, a.rows_per_cta), batch * a.hkv);
+    verify_kernel<D, QT><<<grid, C::THREADS, C::SMEM, st>>>(a);
+    return cudaGetLastError();
+}
+
+typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// A page pool seen by the TMA unit: rows = pages * kv heads * 16 tokens,
+// D bf16 channels each; boxes of 16 rows x 64 channels, 128-byte swizzle.
+bool encode_pool(CUtensorMap *m, const void *pool, int64_t n_pages, int hkv, int d) {
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)n_pages * hkv * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
-int verify_splits(int max_seq_len) { return max(1, ceil_div(ceil_div(max_seq_len, kPage), kSplitPages)); }
+int verify_splits(int max_seq_len) { return max(1, ceil_div(ceil_div(max_seq_len, kPage), vtc::kSplitPages)); }
 
 bool verify_supported(const vc_kv_format &f, int hq, int n_q) {
     const int d = f.head_dim, hkv = f.num_kv_heads;
@@ -72,9 +84,10 @@ size_t verify_workspace(const vc_paged_kv &f, int n_q, int hq, int max_seq_len) 
     return (size_t)f.batch * n_q * hq * verify_splits(max_seq_len) * (f.fmt.head_dim + 2) * sizeof(float);
 }
 
-// Fill the kernel arguments (shared with the mixed launch).
-void verify_args(VerifyArgs &a, const void *q, int n_q, int hq, const vc_paged_kv &f, float scale,
-                 int max_seq_len, void *ws, int32_t *status) {
+// Fill the kernel arguments (shared with the mixed launch); false when the
+// tensor maps of the pools cannot be encoded.
+bool verify_args(Args &a, const void *q, int n_q, int hq, const vc_paged_kv &f, float scale, int max_seq_len,
+                 void *ws, int32_t *status) {
     a.q = (const uint16_t *)q;
     a.kp = (const uint8_t *)f.k_pages;
     a.vp = (const uint8_t *)f.v_pages;
@@ -88,17 +101,22 @@ void verify_args(VerifyArgs &a, const void *q, int n_q, int hq, const vc_paged_k
     a.grp = hq / a.hkv;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.n_splits = verify_splits(max_seq_len);
+    a.rows_per_cta = vtc::kTileRows;
     a.ws_o = (float *)ws;
     a.ws_ml = a.ws_o + (size_t)f.batch * n_q * hq * a.n_splits * f.fmt.head_dim;
     a.status = status;
+    return encode_pool(&a.kmap, f.k_pages, f.num_pages, a.hkv, f.fmt.head_dim) &&
+           encode_pool(&a.vmap, f.v_pages, f.num_pages, a.hkv, f.fmt.head_dim);
 }
 
 cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, float scale, float *out,
                           int max_seq_len, void *ws, int32_t *status, cudaStream_t st) {
-    VerifyArgs a;
-    verify_args(a, q, n_q, hq, f, scale, max(max_seq_len, 1), ws, status);
+    Args a;
+    if (!verify_args(a, q, n_q, hq, f, scale, max(max_seq_len, 1), ws, status)) return cudaErrorInvalidValue;
     const int d = f.fmt.head_dim;
-    cudaError_t e = d == 64 ? launch<64>(a, f.batch, st) : launch<128>(a, f.batch, st);
+    const bool two = n_q * a.grp > vtc::kTileRows;
+    cudaError_t e = d == 64 ? (two ? launch<64, 2>(a, f.batch, st) : launch<64, 1>(a, f.batch, st))
+                            : (two ? launch<128, 2>(a, f.batch, st) : launch<128, 1>(a, f.batch, st));
     if (e != cudaSuccess) return e;
     const int rows = f.batch * n_q * hq;
     if (d == 64)

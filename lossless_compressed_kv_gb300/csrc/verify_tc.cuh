@@ -1,0 +1,432 @@
+// Verification attention on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// "VeriCache: Making Lossy KV Compression Exact", "The Core Idea" items 3-5:
+// one pass over KV_full checks every drafted position; query i of the block
+// attends causally to the prefix and the block up to itself.  The rows of a
+// CTA are (query, head) pairs of one kv head's GQA group (up to 256 rows =
+// two 128-row MMA tiles), so every K/V byte feeds n_q * G rows.
+//
+// Roles (one CTA = one (request, kv head, 4096-key split, row block)):
+//  - producer warp: one thread streams 64-key blocks (4 pages) of K and V
+//    into a 3-stage shared-memory ring with TMA tensor copies (one 16-row x
+//    64-channel box per page and 128-byte column chunk); the TMA unit writes
+//    the 128-byte-swizzled layout the tensor core reads.  Full / empty
+//    mbarriers per stage (transaction bytes / MMA completion).
+//  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 64,
+//    K 16 steps) into TMEM, then O += P V (M 128, N = D, V read MN-major).
+//  - 4 softmax warps per 128-row tile: each thread owns one row = one TMEM
+//    lane; it loads the row's 64 scores from TMEM, masks, keeps a running max
+//    (rescaling O in TMEM only when the max grows by more than 2^8), writes
+//    P (bf16) as the next MMA's A operand, and finally reads O from TMEM.
+// Splits are fixed by key position and each row's arithmetic depends on that
+// row alone, so results do not depend on n_q, the row block or the batch.
+// Every mbarrier wait is bounded; a timeout is reported and the CTA drains.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; maps are encoded by the host code)
+
+#include "vc_internal.cuh"
+
+namespace vc {
+namespace vtc {
+
+constexpr int kBlockKeys = 64;   // keys per MMA block (4 pages)
+constexpr int kSplitPages = 256; // 4096 keys per split, fixed by position
+constexpr int kTileRows = 128;
+
+struct Args {
+    CUtensorMap kmap, vmap;  // K / V pools as [pages * hkv * 16 rows][D] bf16, box 16 x 64, 128B swizzle
+    const uint16_t *q;  // [B][n_q][Hq][D]
+    const uint8_t *kp, *vp;
+    int64_t n_pages;
+    const int32_t *table, *lens;
+    int maxb;
+    int n_q, hq, hkv, grp;
+    float scale_log2;
+    int n_splits;
+    int rows_per_cta;   // QT * 128
+    float *ws_o;        // [B][n_q][Hq][n_splits][D]
+    float *ws_ml;       // [..][2]
+    int32_t *status;
+};
+
+template <int D, int QT>
+struct Cfg {
+    static constexpr int NC = D / 64;                      // swizzle atoms along D
+    static constexpr int STAGES = 3;
+    static constexpr int QTILE = kTileRows * D * 2;        // one Q tile
+    static constexpr int KTILE = kBlockKeys * D * 2;       // one K (or V) block
+    static constexpr int PTILE = kTileRows * kBlockKeys * 2;
+    static constexpr int OFF_KV = QT * QTILE;
+    static constexpr int OFF_P = OFF_KV + STAGES * 2 * KTILE;
+    static constexpr int OFF_BAR = OFF_P + QT * 2 * PTILE;
+    static constexpr int NBAR = QT * 2 + QT * 2 + 2 + 2 * STAGES;  // s_ready, p_ready, pv_done, full, empty
+    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+    static constexpr int TMEM_COLS = (QT * 128 + QT * D) <= 256 ? 256 : 512;
+    static constexpr int THREADS = QT * 128 + 64;  // softmax warps + producer warp + MMA warp
+    __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) { return (uint32_t)(qt * 2 + buf) * 64; }
+    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * 128 + qt * D); }
+};
+
+// --- tcgen05 / descriptor helpers ------------------------------------------
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.
+__device__ inline uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+__device__ inline void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ inline void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// One TMA tensor copy: box at (x = channel, y = row) of `map` -> dst.
+__device__ inline void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ inline void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ inline void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ inline void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ inline void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])));
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// offset of (row, 16-byte chunk c) in a 128-byte-swizzled K-major tile whose
+// rows are `rows` long per 64-element atom column
+__device__ inline int sw128(int row, int c, int rows) {
+    return (c >> 3) * rows * 128 + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+}
+
+// --- the CTA body ------------------------------------------------------------
+template <int D, int QT>
+__device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb, int bk, uint8_t *smem_raw) {
+    using C = Cfg<D, QT>;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned
+    uint8_t *sq = smem;
+    uint8_t *skv = smem + C::OFF_KV;
+    uint8_t *sp = smem + C::OFF_P;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *s_ready = bars;             // [QT][2]
+    uint64_t *p_ready = bars + QT * 2;    // [QT][2]
+    uint64_t *pv_done = bars + QT * 4;    // [2]
+    uint64_t *full = bars + QT * 4 + 2;   // [STAGES]
+    uint64_t *empty = full + C::STAGES;   // [STAGES]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + C::NBAR);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp == QT * 4;
+    const bool mma_warp = warp == QT * 4 + 1;
+    const int b = bk / a.hkv, kvh = bk % a.hkv;
+    const int len = a.lens[b];
+    const bool len_ok = len >= a.n_q;
+    if (!len_ok && tid == 0 && split == 0 && rb == 0 && kvh == 0) report(a.status, VC_ERR_BAD_INDEX);
+    const int npages = len_ok ? ceil_div(len, kPage) : 0;
+    const int p0 = split * kSplitPages;
+    const int p1 = min(p0 + kSplitPages, npages);
+    const int nkeys = max(0, min(p1 * kPage, len) - p0 * kPage);
+    const int nb = ceil_div(nkeys, kBlockKeys);
+    const int nrows = a.n_q * a.grp;
+    const int32_t *trow = a.table + (int64_t)b * a.maxb;
+
+    // ---- set-up: barriers, TMEM, Q tiles ----
+    if (tid == 0) {
+        for (int i = 0; i < QT * 2; ++i) {
+            mbar_init(&s_ready[i], 1);
+            mbar_init(&p_ready[i], kTileRows);
+        }
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(C::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < QT * kTileRows * (D / 8); e += C::THREADS) {
+        const int r = e / (D / 8), c = e % (D / 8);     // r: row within the CTA, c: 16-byte chunk
+        const int rg = rb * a.rows_per_cta + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (rg < nrows) {
+            const int i = rg / a.grp, n = rg % a.grp;
+            v = *reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D +
+                                                 c * 8);
+        }
+        *reinterpret_cast<uint4 *>(sq + (r >> 7) * C::QTILE + sw128(r & 127, c, kTileRows)) = v;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool alive = true;
+
+    constexpr uint32_t IQK = idesc_bf16(128, kBlockKeys, false);
+    constexpr uint32_t IPV = idesc_bf16(128, D, true);
+    if (producer) {
+        // ================= producer: TMA tensor copies into the stage ring =================
+        if (lane == 0) {
+            for (int j = 0; j < nb && alive; ++j) {
+                const int st = j % C::STAGES;
+                if (j >= C::STAGES) alive = mbar_wait(&empty[st], ((j / C::STAGES) - 1) & 1, a.status);
+                if (!alive) break;
+                uint8_t *kt = skv + st * 2 * C::KTILE;
+                mbar_arrive_expect_tx(&full[st], 2 * C::KTILE);
+                for (int pg = 0; pg < kBlockKeys / kPage; ++pg) {
+                    const int pidx = p0 + j * (kBlockKeys / kPage) + pg;
+                    int id = 0;
+                    if (pidx < npages) {  // pages past the request's end: any valid page (masked / zeroed)
+                        id = pidx < a.maxb ? trow[pidx] : -1;
+                        if (id < 0 || id >= a.n_pages) {
+                            report(a.status, VC_ERR_BAD_INDEX);
+                            id = 0;
+                        }
+                    }
+                    const int y = (id * a.hkv + kvh) * kPage;
+#pragma unroll
+                    for (int c = 0; c < C::NC; ++c) {
+                        tma2d(kt + c * (kBlockKeys * 128) + pg * (kPage * 128), &a.kmap, c * 64, y, &full[st]);
+                        tma2d(kt + C::KTILE + c * (kBlockKeys * 128) + pg * (kPage * 128), &a.vmap, c * 64, y,
+                              &full[st]);
+                    }
+                }
+            }
+        }
+    } else if (mma_warp) {
+        // ================= MMA issue (one thread) =================
+        if (lane == 0) {
+            auto issue_pv = [&](int j) {
+                const uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
+                for (int qt = 0; qt < QT; ++qt) {
+                    const uint8_t *pt = sp + (qt * 2 + (j & 1)) * C::PTILE;
+#pragma unroll
+                    for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+                        umma(tmem + C::O_COL(qt), sdesc(smem_u32(pt) + kk * 32, 16, 1024),
+                             sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
+                }
+                umma_commit(&pv_done[j & 1]);
+                umma_commit(&empty[j % C::STAGES]);
+            };
+            auto wait_p = [&](int j) {
+                for (int qt = 0; qt < QT && alive; ++qt)
+                    alive = mbar_wait(&p_ready[qt * 2 + (j & 1)], (j >> 1) & 1, a.status);
+                tc_fence_after();
+            };
+            for (int j = 0; j < nb && alive; ++j) {
+                const int st = j % C::STAGES;
+                alive = mbar_wait(&full[st], (j / C::STAGES) & 1, a.status);
+                if (!alive) break;
+                tc_fence_after();
+                const uint8_t *kt = skv + st * 2 * C::KTILE;
+                for (int qt = 0; qt < QT; ++qt) {
+                    const uint8_t *qtile = sq + qt * C::QTILE;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma(tmem + C::S_COL(qt, j & 1),
+                             sdesc(smem_u32(qtile) + (ks >> 2) * (kTileRows * 128) + (ks & 3) * 32, 16, 1024),
+                             sdesc(smem_u32(kt) + (ks >> 2) * (kBlockKeys * 128) + (ks & 3) * 32, 16, 1024), IQK,
+                             ks > 0);
+                    umma_commit(&s_ready[qt * 2 + (j & 1)]);
+                }
+                if (j >= 1) {
+                    wait_p(j - 1);
+                    if (alive) issue_pv(j - 1);
+                }
+            }
+            if (nb > 0 && alive) {
+                wait_p(nb - 1);
+                if (alive) issue_pv(nb - 1);
+            }
+        }
+    } else {
+        // ================= softmax / epilogue: one thread per row =================
+        const int qt = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;                 // row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int rg = rb * a.rows_per_cta + qt * kTileRows + r;
+        const bool rvalid = rg < nrows;
+        const int qpos = len - a.n_q + (rvalid ? rg / a.grp : 0);
+        float m_used = -INFINITY, l = 0.0f;
+        bool o_touched = false;
+        // tcgen05.ld / st are warp-collective: every lane of a softmax warp runs
+        // them together (row validity and rescale decisions only pick values)
+        for (int j = 0; j < nb && alive; ++j) {
+            alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + (j & 1)], (j >> 1) & 1, a.status));
+            if (!alive) break;
+            tc_fence_after();
+            float s[kBlockKeys];
+#pragma unroll
+            for (int c0 = 0; c0 < kBlockKeys; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + C::S_COL(qt, j & 1) + c0, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) s[c0 + i] = v[i];
+            }
+            const int key0 = p0 * kPage + j * kBlockKeys;
+            float mb = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kBlockKeys; ++c) {
+                const int key = key0 + c;
+                const float v = (rvalid && key <= qpos && key < len) ? s[c] * a.scale_log2 : -INFINITY;
+                s[c] = v;
+                mb = fmaxf(mb, v);
+            }
+            // grow the reference max only when it rises by more than 2^8
+            // (rare after the first block); O is rescaled in TMEM
+            const bool grow = mb > m_used + 8.0f;
+            const float f = grow ? (m_used == -INFINITY ? 0.0f : ex2(m_used - mb)) : 1.0f;
+            if (__any_sync(0xffffffffu, grow) && o_touched) {
+                // the previous block's P V must have landed before O is rescaled
+                alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status));
+                if (!alive) break;
+                tc_fence_after();
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + C::O_COL(qt) + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] *= f;
+                    tmem_st16(tmem + lane_base + C::O_COL(qt) + c0, v);
+                }
+            }
+            if (grow) {
+                l *= f;
+                m_used = mb;
+            }
+            const float ms = m_used == -INFINITY ? 0.0f : m_used;
+            // slots past the request's end (or of pages past it) may hold any
+            // bytes: zero their V rows so that 0 * NaN never reaches P V
+            const int nvalid = len - key0;
+            if (nvalid < kBlockKeys && qt == 0) {
+                uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
+                for (int e = r; e < (kBlockKeys - nvalid) * (D / 8); e += kTileRows) {
+                    const int kr = nvalid + e / (D / 8), c = e % (D / 8);
+                    *reinterpret_cast<uint4 *>(vt + sw128(kr, c, kBlockKeys)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            // this P buffer was last read by block j - 2's P V
+            if (j >= 2) {
+                alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, a.status));
+                if (!alive) break;
+            }
+            uint8_t *prow = sp + (qt * 2 + (j & 1)) * C::PTILE;
+#pragma unroll
+            for (int c = 0; c < kBlockKeys / 8; ++c) {
+                float p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p[i] = ex2(s[c * 8 + i] - ms);
+                    l += p[i];
+                }
+                uint4 u = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
+                                     pack_bf16(p[6], p[7]));
+                *reinterpret_cast<uint4 *>(prow + sw128(r, c, kTileRows)) = u;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            mbar_arrive(&p_ready[qt * 2 + (j & 1)]);
+            o_touched = true;
+        }
+        // epilogue: the whole warp waits for the last P V and reads O
+        float *dst = nullptr;
+        int64_t row = 0;
+        if (rvalid) {
+            const int i = rg / a.grp, n = rg % a.grp;
+            row = (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * a.n_splits + split;
+            dst = a.ws_o + row * D;
+        }
+        bool have_o = nb > 0 && alive;
+        if (have_o) {
+            have_o = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, a.status));
+            alive = have_o;
+        }
+        if (have_o) {
+            tc_fence_after();
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + C::O_COL(qt) + c0, v);
+                if (rvalid) {
+#pragma unroll
+                    for (int i2 = 0; i2 < 16; i2 += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + i2) =
+                            make_float4(v[i2], v[i2 + 1], v[i2 + 2], v[i2 + 3]);
+                }
+            }
+        } else if (rvalid) {
+            for (int c0 = 0; c0 < D; ++c0) dst[c0] = 0.0f;
+            m_used = -INFINITY;
+            l = 0.0f;
+        }
+        if (rvalid) {
+            a.ws_ml[row * 2] = m_used;
+            a.ws_ml[row * 2 + 1] = l;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// Combine the splits of one row in split order (fixed, so a row's result does
+// not depend on how many empty splits follow it).
+template <int D>
+__device__ __forceinline__ void reduce_row(const float *ws_o, const float *ws_ml, int n_splits, int64_t row,
+                                           float *out, int tid, int nthreads) {
+    const float *ml = ws_ml + row * n_splits * 2;
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ml[2 * s]);
+    for (int c = tid; c < D; c += nthreads) {
+        float acc = 0.0f, L = 0.0f;
+        if (M != -INFINITY) {
+            for (int s = 0; s < n_splits; ++s) {
+                const float f = ex2(ml[2 * s] - M);
+                acc += f * ws_o[(row * n_splits + s) * D + c];
+                L += f * ml[2 * s + 1];
+            }
+        }
+        out[row * D + c] = L > 0.0f ? acc / L : 0.0f;
+    }
+}
+
+}  // namespace vtc
+}  // namespace vc
