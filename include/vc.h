@@ -226,7 +226,7 @@ VC_API vc_status vc_verify_attn(const void *q, int32_t n_q, int32_t num_q_heads,
  *                when a < n_pred; remaining slots -1.
  * n_pred is x + 1 (bonus available) or x (no bonus); 1 <= n_pred.
  */
-VC_API size_t vc_accept_workspace_bytes(int32_t batch, int32_t n_pred, int32_t vocab);
+VC_API size_t vc_accept_workspace_bytes(int32_t batch, int32_t n_pred, int32_t vocab, int32_t d);
 VC_API vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t hidden_group,
                     const float *lm_head, int32_t d, int32_t vocab, const int32_t *drafts,
                     int32_t x, int32_t *verified, int32_t *accept_len, int32_t *emitted,

@@ -52,7 +52,7 @@ _SIG = {
     "vc_verify_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32, C.c_int32]),
     "vc_verify_attn": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32,
                                  _P, C.c_size_t, _P, _P]),
-    "vc_accept_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32]),
+    "vc_accept_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "vc_accept": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
                             _P, _P, C.c_size_t, _P]),
     "vc_stage_async": (C.c_int, [_P, _P, C.c_size_t, _P, _P]),
@@ -198,8 +198,8 @@ def verify_attn(q, full: PagedKV, softmax_scale: float, out, max_seq_len: int, w
            "vc_verify_attn")
 
 
-def accept_workspace_bytes(batch: int, n_pred: int, vocab: int) -> int:
-    return int(_lib.vc_accept_workspace_bytes(batch, n_pred, vocab))
+def accept_workspace_bytes(batch: int, n_pred: int, vocab: int, d: int) -> int:
+    return int(_lib.vc_accept_workspace_bytes(batch, n_pred, vocab, d))
 
 
 def accept(hidden, lm_head, drafts, verified, accept_len, emitted, workspace, hidden_group: int = 1,

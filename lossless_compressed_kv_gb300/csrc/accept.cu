@@ -30,9 +30,19 @@ __device__ inline Best better(Best a, Best b) {  // larger value, lower id on ti
     return a;
 }
 
-__global__ void __launch_bounds__(kCols) logits_argmax_kernel(const float *hidden, int rows, int hg,
-                                                             const float *w, int d, int vocab,
-                                                             float *part_v, int *part_i, int ntiles) {
+// h[r][k] = (sum_j hidden[r][j][k], in increasing j) / hg, once per row.
+__global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, float *h) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)rows * d) return;
+    const int64_t r = i / d, k = i % d;
+    const float *hp = hidden + (r * hg) * d + k;
+    float s = 0.0f;
+    for (int j = 0; j < hg; ++j) s = __fadd_rn(s, hp[(int64_t)j * d]);
+    h[i] = __fdiv_rn(s, (float)hg);
+}
+
+__global__ void __launch_bounds__(kCols) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
+                                                             int vocab, float *part_v, int *part_i, int ntiles) {
     __shared__ float hs[kRowsT][kKT];
     __shared__ Best red[kRowsT][kCols / 32];
     const int vt = blockIdx.x, r0 = blockIdx.y * kRowsT;
@@ -41,19 +51,11 @@ __global__ void __launch_bounds__(kCols) logits_argmax_kernel(const float *hidde
     float acc[kRowsT];
 #pragma unroll
     for (int r = 0; r < kRowsT; ++r) acc[r] = 0.0f;
-    const float inv_hg = (float)hg;
     for (int k0 = 0; k0 < d; k0 += kKT) {
         __syncthreads();
         for (int e = threadIdx.x; e < kRowsT * kKT; e += kCols) {
             const int r = e / kKT, k = k0 + e % kKT;
-            float val = 0.0f;
-            if (r0 + r < rows && k < d) {
-                const float *hp = hidden + ((int64_t)(r0 + r) * hg) * d + k;
-                float s = 0.0f;
-                for (int j = 0; j < hg; ++j) s = __fadd_rn(s, hp[(int64_t)j * d]);
-                val = __fdiv_rn(s, inv_hg);
-            }
-            hs[r][e % kKT] = val;
+            hs[r][e % kKT] = (r0 + r < rows && k < d) ? h[(int64_t)(r0 + r) * d + k] : 0.0f;
         }
         __syncthreads();
         if (vok) {
@@ -116,9 +118,9 @@ __global__ void accept_finalize_kernel(const float *part_v, const int *part_i, i
 
 }  // namespace
 
-size_t accept_workspace(int batch, int n_pred, int vocab) {
+size_t accept_workspace(int batch, int n_pred, int vocab, int d) {
     const int ntiles = ceil_div(vocab, kCols);
-    return (size_t)batch * n_pred * ntiles * (sizeof(float) + sizeof(int));
+    return (size_t)batch * n_pred * ntiles * (sizeof(float) + sizeof(int)) + (size_t)batch * n_pred * d * sizeof(float);
 }
 
 cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, const float *w, int d,
@@ -128,8 +130,11 @@ cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, co
     const int rows = batch * n_pred;
     float *pv = (float *)ws;
     int *pi = (int *)(pv + (size_t)rows * ntiles);
+    float *h = reinterpret_cast<float *>(pi + (size_t)rows * ntiles);
+    const int64_t nh = (int64_t)rows * d;
+    group_mean_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hidden, rows, hg, d, h);
     dim3 grid(ntiles, ceil_div(rows, kRowsT));
-    logits_argmax_kernel<<<grid, kCols, 0, st>>>(hidden, rows, hg, w, d, vocab, pv, pi, ntiles);
+    logits_argmax_kernel<<<grid, kCols, 0, st>>>(h, rows, w, d, vocab, pv, pi, ntiles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     accept_finalize_kernel<<<batch, 128, n_pred * sizeof(int32_t), st>>>(pv, pi, ntiles, n_pred, drafts, x,

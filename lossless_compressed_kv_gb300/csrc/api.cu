@@ -17,7 +17,7 @@ bool verify_supported(const vc_kv_format &f, int hq, int n_q);
 size_t verify_workspace(const vc_paged_kv &f, int n_q, int hq, int max_seq_len);
 cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, float scale, float *out,
                           int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
-size_t accept_workspace(int batch, int n_pred, int vocab);
+size_t accept_workspace(int batch, int n_pred, int vocab, int d);
 cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, const float *w, int d,
                           int vocab, const int32_t *drafts, int x, int32_t *verified, int32_t *accept_len,
                           int32_t *emitted, void *ws, cudaStream_t st);
@@ -96,9 +96,9 @@ vc_status vc_verify_attn(const void *q, int32_t n_q, int32_t num_q_heads, const 
                                    (cudaStream_t)stream));
 }
 
-size_t vc_accept_workspace_bytes(int32_t batch, int32_t n_pred, int32_t vocab) {
-    if (batch < 0 || n_pred < 1 || vocab < 1) return 0;
-    return accept_workspace(batch, n_pred, vocab);
+size_t vc_accept_workspace_bytes(int32_t batch, int32_t n_pred, int32_t vocab, int32_t d) {
+    if (batch < 0 || n_pred < 1 || vocab < 1 || d < 1) return 0;
+    return accept_workspace(batch, n_pred, vocab, d);
 }
 
 vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t hidden_group,
@@ -110,7 +110,7 @@ vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t 
         return VC_ERR_INVALID_ARG;
     if (n_pred != x && n_pred != x + 1) return VC_ERR_INVALID_ARG;
     if (batch == 0) return VC_OK;
-    if (!workspace || workspace_bytes < accept_workspace(batch, n_pred, vocab)) return VC_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < accept_workspace(batch, n_pred, vocab, d)) return VC_ERR_WORKSPACE;
     return from_cuda(accept_launch(hidden, batch, n_pred, hidden_group, lm_head, d, vocab, drafts, x, verified,
                                    accept_len, emitted, workspace, (cudaStream_t)stream));
 }

@@ -130,7 +130,7 @@ class ToyDecoder:
         ver = self._buf("ver", (batch, n_pred), torch.int32)
         al = self._buf("al", (batch,), torch.int32)
         em = self._buf("em", (batch, x + 1), torch.int32)
-        ws = self._buf("aws", (vc.accept_workspace_bytes(batch, n_pred, self.s.vocab),), torch.uint8)
+        ws = self._buf("aws", (vc.accept_workspace_bytes(batch, n_pred, self.s.vocab, self.s.d_model),), torch.uint8)
         dr = drafts if drafts is not None else self._buf("nodraft", (batch, 0), torch.int32)
         vc.accept(hidden.view(batch, n_pred, 1, -1), self.lm_head, dr, ver, al, em, ws)
         return ver, al, em

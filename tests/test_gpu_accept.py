@@ -25,7 +25,7 @@ def gpu_accept(hidden, w, drafts, hg=1):
     ver = torch.full((b, n_pred), -7, dtype=torch.int32, device="cuda")
     al = torch.full((b,), -7, dtype=torch.int32, device="cuda")
     em = torch.full((b, x + 1), -7, dtype=torch.int32, device="cuda")
-    ws = torch.empty(vc.accept_workspace_bytes(b, n_pred, w.shape[1]), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(vc.accept_workspace_bytes(b, n_pred, w.shape[1], w.shape[0]), dtype=torch.uint8, device="cuda")
     vc.accept(hd, wd, dd, ver, al, em, ws, hidden_group=hg)
     torch.cuda.synchronize()
     return ver.cpu().numpy(), al.cpu().numpy(), em.cpu().numpy()
