@@ -43,6 +43,7 @@ extern "C" {
 
 size_t vc_head_block_bytes(const vc_kv_format *f) {
     if (!f || !bits_ok(f->bits) || f->head_dim < 32 || f->head_dim % 32) return 0;
+    if (f->bits != 16 && f->head_dim % 64) return 0;  // quantised formats: head_dim a multiple of 64
     return (size_t)head_block_bytes(f->bits, f->head_dim);
 }
 

@@ -6,10 +6,14 @@
 // heads).  The bit format (asymmetric 32-channel groups, fp16 scale and
 // zero, little-endian packing) is the library's reading; see vc.h.
 //
-// One warp per (kept entry, kv head): 32 lanes each own D/32 consecutive
-// channels (a lane's channels never straddle a group), min/max of a group is
-// a shuffle reduction over the lanes of that group, codes are staged in
-// shared memory and packed into 32-bit words by the first D*bits/32 lanes.
+// Quantised formats: one CTA per (KV_comp page, kv head) touched by a
+// request's slot range.  It loads the page's K and V head blocks into shared
+// memory, quantises the covered token slots (one warp per slot: 32 lanes own
+// D/32 consecutive channels each, so a group's min/max is a shuffle over the
+// lanes of that group), places the codes with comp_layout.cuh's map and
+// writes both blocks back whole.  Slots outside the range keep their bytes.
+// bf16 token drop: one warp per (kept entry, kv head) copies the row.
+#include "comp_layout.cuh"
 #include "vc_internal.cuh"
 
 namespace vc {
@@ -36,10 +40,10 @@ __device__ inline uint16_t f16_store(float f) {  // saturate to +-65504, round t
     return __half_as_ushort(__float2half_rn(f));
 }
 
-// Quantise one row (D channels) held CPL per lane; write codes, scales, zeros.
+// Quantise one row (D channels, CPL = D/32 consecutive ones per lane):
+// codes of the lane's channels, and the fp16 scale / zero of its group.
 template <int BITS, int D>
-__device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t *codes_smem, uint8_t *dst_codes,
-                             uint16_t *dst_scales, uint16_t *dst_zeros, int lane) {
+__device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t (&code)[D / 32], uint16_t &sh, uint16_t &zh) {
     constexpr int CPL = D / 32;             // channels per lane
     constexpr int LPG = kGroup / CPL;       // lanes per group
     constexpr int QMAX = (1 << BITS) - 1;
@@ -62,8 +66,8 @@ __device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t *codes_smem, u
     mn = __fadd_rn(mn, 0.0f);  // -0 -> +0
     const float range = __fsub_rn(mx, mn);
     const float sdot = __fdiv_rn(range, (float)QMAX);
-    const uint16_t sh = f16_store(sdot);
-    const uint16_t zh = f16_store(mn);
+    sh = f16_store(sdot);
+    zh = f16_store(mn);
     const float s = __half2float(__ushort_as_half(sh));
     const float z = __half2float(__ushort_as_half(zh));
 #pragma unroll
@@ -75,33 +79,115 @@ __device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t *codes_smem, u
             r = fminf(fmaxf(r, 0.0f), (float)QMAX);
             c = (int)r;
         }
-        codes_smem[lane * CPL + i] = (uint8_t)c;
+        code[i] = (uint8_t)c;
     }
-    if (lane % LPG == 0) {
-        const int grp = lane / LPG;
-        dst_scales[grp] = sh;
-        dst_zeros[grp] = zh;
-    }
-    __syncwarp();
-    constexpr int WORDS = D * BITS / 32;
-    if (lane < WORDS) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const int bit = lane * 32 + k;
-            const int ch = bit / BITS;
-            const int off = bit % BITS;
-            w |= (uint32_t)((codes_smem[ch] >> off) & 1) << k;
-        }
-        reinterpret_cast<uint32_t *>(dst_codes)[lane] = w;
-    }
-    __syncwarp();
 }
 
-template <int BITS, int D>
-__global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
+// Load the bf16 row a lane quantises: D/32 consecutive channels per lane.
+template <int D>
+__device__ inline void load_lane_row(const uint8_t *src, int lane, uint16_t (&x)[D / 32]) {
     constexpr int CPL = D / 32;
-    __shared__ __align__(16) uint8_t codes[kWarps][D];
+    if constexpr (CPL == 4) {
+        uint2 u = reinterpret_cast<const uint2 *>(src)[lane];
+        x[0] = u.x & 0xffff; x[1] = u.x >> 16; x[2] = u.y & 0xffff; x[3] = u.y >> 16;
+    } else if constexpr (CPL == 2) {
+        uint32_t u = reinterpret_cast<const uint32_t *>(src)[lane];
+        x[0] = u & 0xffff; x[1] = u >> 16;
+    } else {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) x[i] = reinterpret_cast<const uint16_t *>(src)[lane * CPL + i];
+    }
+}
+
+// Replace the `width` bits at bit offset `off` of a shared-memory block.
+__device__ inline void put_bits(uint32_t *blk, int off, int width, uint32_t v) {
+    const uint32_t m = ((1u << width) - 1u) << (off & 31);
+    atomicAnd(&blk[off >> 5], ~m);
+    atomicOr(&blk[off >> 5], (v << (off & 31)) & m);
+}
+
+constexpr int kPageWarps = 8;
+
+template <int BITS, int D>
+__global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(CompressArgs a) {
+    constexpr int HB = 2 * D * (BITS + 1);    // head block bytes
+    constexpr int CR = kPage * D * BITS / 8;  // code region bytes
+    constexpr int G = D / kGroup, CPL = D / 32, LPG = kGroup / CPL;
+    __shared__ __align__(16) uint32_t blk[2][HB / 4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int o0 = a.offs[b], n = a.offs[b + 1] - o0;
+    if (n <= 0) return;
+    const int start = a.start ? a.start[b] : 0;
+    if (start < 0) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    const int pg = start / kPage + blockIdx.x;
+    const int s_lo = max(start, pg * kPage), s_hi = min(start + n, (pg + 1) * kPage);
+    if (s_lo >= s_hi) return;
+    const int cp = pg < a.c_maxb ? a.c_table[(int64_t)b * a.c_maxb + pg] : -1;
+    if (cp < 0 || cp >= a.c_pages) {
+        if (threadIdx.x == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    uint8_t *gk = a.ck + ((int64_t)cp * a.hkv + h) * HB;
+    uint8_t *gv = a.cv + ((int64_t)cp * a.hkv + h) * HB;
+    for (int i = threadIdx.x; i < HB / 16; i += blockDim.x) {
+        reinterpret_cast<uint4 *>(blk[0])[i] = reinterpret_cast<const uint4 *>(gk)[i];
+        reinterpret_cast<uint4 *>(blk[1])[i] = reinterpret_cast<const uint4 *>(gv)[i];
+    }
+    __syncthreads();
+    const int fhb = head_block_bytes(16, D);
+    for (int s = s_lo + warp; s < s_hi; s += kPageWarps) {
+        const int t = a.idx[o0 + (s - start)];
+        const int fp = (t >= 0 && t < a.f_lens[b] && t / kPage < a.f_maxb)
+                           ? a.f_table[(int64_t)b * a.f_maxb + t / kPage] : -1;
+        if (fp < 0 || fp >= a.f_pages) {  // bad kept index: the slot keeps its bytes
+            if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
+            continue;
+        }
+        const int slot = s % kPage;
+        const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            uint16_t x[CPL];
+            load_lane_row<D>((kv ? a.fv : a.fk) + fbase, lane, x);
+            uint8_t code[CPL];
+            uint16_t sh, zh;
+            quantize_row<BITS, D>(x, code, sh, zh);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const int ch = lane * CPL + i;
+                const int o = kv ? layout::v_bit(BITS, D, slot, ch, 0) : layout::k_bit(BITS, D, slot, ch, 0);
+                if constexpr (BITS == 3) {
+                    put_bits(blk[kv], o, 2, code[i] & 3u);
+                    const int o1 = kv ? layout::v_bit(3, D, slot, ch, 1) : layout::k_bit(3, D, slot, ch, 1);
+                    put_bits(blk[kv], o1, 1, code[i] >> 2);
+                } else {
+                    put_bits(blk[kv], o, BITS, code[i]);
+                }
+            }
+            if (lane % LPG == 0) {
+                const int gr = lane / LPG;
+                const int e = kv ? layout::v_param(G, slot, gr) : slot * G + gr;
+                uint16_t *par = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(blk[kv]) + CR);
+                par[e] = sh;
+                par[kPage * G + e] = zh;
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < HB / 16; i += blockDim.x) {
+        reinterpret_cast<uint4 *>(gk)[i] = reinterpret_cast<const uint4 *>(blk[0])[i];
+        reinterpret_cast<uint4 *>(gv)[i] = reinterpret_cast<const uint4 *>(blk[1])[i];
+    }
+}
+
+// bf16 token drop: one warp per (kept entry, kv head) copies the row.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) compress_bf16_kernel(CompressArgs a) {
+    constexpr int CPL = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     const int item = blockIdx.x * kWarps + warp;  // (entry, head) pair
@@ -121,51 +207,36 @@ __global__ void __launch_bounds__(kWarps * 32) compress_kernel(CompressArgs a) {
         if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
         return;
     }
-    const int fhb = head_block_bytes(16, D), chb = head_block_bytes(BITS, D);
-    const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
-    const int64_t cbase = ((int64_t)cp * a.hkv + h) * chb;
-    const int s = slot % kPage;
+    const int hb = head_block_bytes(16, D);
+    const int64_t fbase = ((int64_t)fp * a.hkv + h) * hb + (int64_t)(t % kPage) * D * 2;
+    const int64_t cbase = ((int64_t)cp * a.hkv + h) * hb + (int64_t)(slot % kPage) * D * 2;
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
-        const uint8_t *src = (kv ? a.fv : a.fk) + fbase;
-        uint8_t *dst = (kv ? a.cv : a.ck) + cbase;
         uint16_t x[CPL];
-        // CPL bf16 = 2*CPL bytes per lane, contiguous across the warp
-        if constexpr (CPL == 4) {
-            uint2 u = reinterpret_cast<const uint2 *>(src)[lane];
-            x[0] = u.x & 0xffff; x[1] = u.x >> 16; x[2] = u.y & 0xffff; x[3] = u.y >> 16;
-        } else if constexpr (CPL == 2) {
-            uint32_t u = reinterpret_cast<const uint32_t *>(src)[lane];
-            x[0] = u & 0xffff; x[1] = u >> 16;
-        } else {
+        load_lane_row<D>((kv ? a.fv : a.fk) + fbase, lane, x);
+        uint16_t *d16 = reinterpret_cast<uint16_t *>((kv ? a.cv : a.ck) + cbase);
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) x[i] = reinterpret_cast<const uint16_t *>(src)[lane * CPL + i];
-        }
-        if constexpr (BITS == 16) {
-            uint16_t *d16 = reinterpret_cast<uint16_t *>(dst + (int64_t)s * D * 2);
-#pragma unroll
-            for (int i = 0; i < CPL; ++i) d16[lane * CPL + i] = x[i];
-        } else {
-            constexpr int CB = D * BITS / 8, NG = D / kGroup;
-            uint8_t *dc = dst + s * CB;
-            uint16_t *dsc = reinterpret_cast<uint16_t *>(dst + kPage * CB) + s * NG;
-            uint16_t *dz = reinterpret_cast<uint16_t *>(dst + kPage * CB + kPage * NG * 2) + s * NG;
-            quantize_row<BITS, D>(x, codes[warp], dc, dsc, dz, lane);
-        }
+        for (int i = 0; i < CPL; ++i) d16[lane * CPL + i] = x[i];
     }
 }
 
 template <int BITS, int D>
 cudaError_t launch_bd(const CompressArgs &a, int batch, int max_kept, cudaStream_t st) {
-    dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
-    compress_kernel<BITS, D><<<grid, kWarps * 32, 0, st>>>(a);
+    if constexpr (BITS == 16) {
+        dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
+        compress_bf16_kernel<D><<<grid, kWarps * 32, 0, st>>>(a);
+    } else {
+        // a range of max_kept slots starting anywhere touches at most this many pages
+        dim3 grid(ceil_div(max_kept, kPage) + 1, a.hkv, batch);
+        compress_page_kernel<BITS, D><<<grid, kPageWarps * 32, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t launch_b(int d, const CompressArgs &a, int batch, int max_kept, cudaStream_t st) {
     switch (d) {
-        case 32: return launch_bd<BITS, 32>(a, batch, max_kept, st);
+        case 32: if constexpr (BITS == 16) return launch_bd<BITS, 32>(a, batch, max_kept, st); break;
         case 64: return launch_bd<BITS, 64>(a, batch, max_kept, st);
         case 128: return launch_bd<BITS, 128>(a, batch, max_kept, st);
         case 256: return launch_bd<BITS, 256>(a, batch, max_kept, st);
@@ -185,6 +256,7 @@ vc_status compress(const vc_paged_kv *full, const int32_t *kept_offsets, const i
         return VC_ERR_INVALID_ARG;
     if (!(d == 32 || d == 64 || d == 128 || d == 256) || hkv < 1) return VC_ERR_UNSUPPORTED;
     if (!(bits == 2 || bits == 3 || bits == 4 || bits == 16)) return VC_ERR_UNSUPPORTED;
+    if (bits != 16 && d % 64) return VC_ERR_UNSUPPORTED;  // quantised formats: head_dim 64, 128, 256
     if (!full->k_pages || !full->v_pages || !full->block_table || !full->seq_lens || !comp->k_pages ||
         !comp->v_pages || !comp->block_table || full->batch < 0 || full->max_blocks < 1 ||
         comp->max_blocks < 1)

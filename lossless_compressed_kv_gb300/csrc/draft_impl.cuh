@@ -1,12 +1,12 @@
 // Device body of the draft attention (shared by the draft launch and the
-// mixed draft/verify launch).  See draft_attn.cu for the design notes.
+// mixed draft/verify launch).  See draft_attn.cu for the design notes and
+// comp_layout.cuh for the code placement this body reads.
 #pragma once
 
 #include "vc_internal.cuh"
 
 namespace vc {
 namespace draft {
-
 
 struct DraftArgs {
     const uint16_t *q;  // [B][Hq][D] bf16
@@ -24,11 +24,10 @@ struct DraftArgs {
 
 template <int BITS, int D, int NW>
 struct Cfg {
-    static constexpr int NT = D / 16;
-    static constexpr int NG = D / 32;
+    static constexpr int NT = D / 16;  // k-steps of QK^T, m-tiles of PV
+    static constexpr int NG = D / 32;  // quantisation groups
     static constexpr int HB = BITS == 16 ? kPage * D * 2 : 2 * D * (BITS + 1);
-    static constexpr int CB = BITS == 16 ? D * 2 : D * BITS / 8;  // bytes per token row
-    static constexpr int WPR = CB / 4;                            // 32-bit words per row
+    static constexpr int CR = kPage * D * (BITS == 16 ? 16 : BITS) / 8;  // code region bytes
     static constexpr int NSTAGE = BITS == 16 ? 3 : 4;
     static constexpr int STAGE = 2 * HB;
     static constexpr int RING = NW * NSTAGE * STAGE;
@@ -38,125 +37,167 @@ struct Cfg {
     static constexpr int SMEM = (RING > COMBINE ? RING : COMBINE) + BARS + QS;
 };
 
-// Load one token row of packed codes (CB bytes) as 32-bit words.
-template <int CB>
-__device__ inline void load_row(uint32_t (&w)[CB / 4], const uint8_t *p) {
-    if constexpr (CB % 16 == 0) {
+// ---------------------------------------------------------------------------
+// packed f32x2 arithmetic (one instruction for two lanes of fp32)
+// ---------------------------------------------------------------------------
+struct f2 {
+    float x, y;
+};
+__device__ inline f2 fma2(f2 a, f2 b, f2 c) {
+    unsigned long long ua, ub, uc, ud;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
+    f2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+    return d;
+}
+__device__ inline f2 mul2(f2 a, f2 b) {
+    unsigned long long ua, ub, ud;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
+    f2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+    return d;
+}
+__device__ inline uint32_t hmul2(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// ---------------------------------------------------------------------------
+// Quantised K operand.  Thread t of a fragment reads its region of a token
+// row and turns it into R = D/8 registers; register r = 2 ks + h holds the
+// codes of channels 16 ks + 4 t + 2 h + {0, 1} in its two halves at bit
+// position kpos(r), i.e. the f16 subnormals code * 2^(kpos - 24).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__host__ __device__ constexpr int kpos(int r) {
+    return BITS == 2 ? ((r & 7) < 5 ? 2 * (r & 7) : 2 * ((r & 7) - 5))
+         : BITS == 4 ? 4 * (r & 1)
+                     : 2 * (r & 3);
+}
+
+template <int BITS, int D>
+struct KRow {
+    static constexpr int NLO = BITS == 4 ? D / 32 : D / 64;  // main-plane words of a thread region
+    static constexpr int NHI = BITS == 3 ? (D >= 128 ? D / 128 : 1) : 0;
+    uint32_t w[NLO];
+    uint32_t hw[NHI > 0 ? NHI : 1];
+
+    __device__ inline void load(const uint8_t *row, int t) {
+        if constexpr (BITS == 2 || BITS == 3) {
+            const uint8_t *p = row + t * (D / 16);
+            if constexpr (NLO == 1) {
+                w[0] = *reinterpret_cast<const uint32_t *>(p);
+            } else if constexpr (NLO == 2) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(p);
+                w[0] = u.x; w[1] = u.y;
+            } else {
 #pragma unroll
-        for (int i = 0; i < CB / 16; ++i) {
-            uint4 u = reinterpret_cast<const uint4 *>(p)[i];
-            w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
-        }
-    } else {
+                for (int i = 0; i < NLO / 4; ++i) {
+                    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+                    w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+                }
+            }
+            if constexpr (BITS == 3) {
+                const uint8_t *h = row + D / 4;  // high-bit plane after the four low regions
+                if constexpr (D == 64) {
+                    const uint32_t u = *reinterpret_cast<const uint16_t *>(h + 2 * t);
+                    hw[0] = __byte_perm(u, 0u, 0x4140);  // half-0 byte -> bits 0-7, half-1 byte -> 16-23
+                } else {
 #pragma unroll
-        for (int i = 0; i < CB / 8; ++i) {
-            uint2 u = reinterpret_cast<const uint2 *>(p)[i];
-            w[2 * i] = u.x; w[2 * i + 1] = u.y;
+                    for (int i = 0; i < NHI; ++i) hw[i] = reinterpret_cast<const uint32_t *>(h + t * (D / 32))[i];
+                }
+            }
+        } else {  // 4 bits
+            const uint8_t *p = row + t * (D / 8);
+            if constexpr (NLO == 2) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(p);
+                w[0] = u.x; w[1] = u.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < NLO / 4; ++i) {
+                    const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+                    w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+                }
+            }
         }
     }
-}
 
-// 3-bit: the 48 bits of channels [16 j, 16 j + 16) of a row, right-aligned.
-template <int WPR>
-__device__ inline uint64_t win3(const uint32_t (&w)[WPR], int j) {
-    const int wi = (3 * j) >> 1;
-    uint64_t x = ((uint64_t)w[wi + 1] << 32) | w[wi];
-    return (j & 1) ? (x >> 16) : x;
-}
-
-// Codes enter the MMA as f16 subnormals: a code c masked in place at bit p
-// of a 16-bit half is the f16 value c * 2^(p - 24), exact (the tensor cores
-// do not flush subnormal operands).  The query operand of those k-slots is
-// pre-scaled by 2^-p, so every product is c * q * 2^-24 and the group scale
-// carries the 2^24.  Per-thread shift s and in-half positions (pl for
-// k-slots 2t, 2t+1; ph for 2t+8, 2t+9) keep every masked code below 2^10.
-template <int BITS>
-struct KPos {
-    int s, pl, ph;
-    __device__ explicit KPos(int t) {
+    // operand register r (compile-time after unrolling)
+    __device__ inline uint32_t reg(int r) const {
         if constexpr (BITS == 2) {
-            s = t < 2 ? 0 : (t == 2 ? 2 : 6);
-            pl = 4 * t - s;
-            ph = pl + 2;
+            const int u = r >> 3, j = r & 7;
+            return j < 5 ? (w[u] & (0x00030003u << (2 * j))) : ((w[u] >> 10) & (0x00030003u << (2 * (j - 5))));
         } else if constexpr (BITS == 4) {
-            s = t < 2 ? 0 : 4 * t - 4;
-            pl = ph = 4 * t - s;
+            const int u = r >> 2, j = r & 3;
+            const uint32_t y = j < 2 ? w[u] : (w[u] >> 8);
+            return y & (0x000F000Fu << (4 * (j & 1)));
         } else {
-            s = 0;
-            pl = ph = 0;
+            const int u = r >> 3, j = r & 7, p = 2 * (j & 3);
+            const uint32_t lo = j < 4 ? w[u] : (w[u] >> 8);
+            const int set = 2 * (u & 1) + (j >> 2);
+            const uint32_t h = hw[u >> 1];
+            const uint32_t y = set == 0 ? (h << 2) : set == 1 ? (h << 1) : set == 2 ? (h >> 6) : (h >> 7);
+            return (lo & (0x00030003u << p)) | (y & (0x00040004u << p));
         }
     }
 };
 
-// K operand (A, rows = tokens) for k-step ks from one token row's words; the
-// k-slot -> channel map of each bit width is mirrored by q_channel().
-template <int BITS, int WPR>
-__device__ inline void k_pair(const uint32_t (&w)[WPR], int ks, int t, const KPos<BITS> &kp, uint32_t &lo,
-                              uint32_t &hi) {
-    if constexpr (BITS == 2) {
-        const uint32_t y = w[ks] >> kp.s;  // channels (2t, 2t+8) at pl, (2t+1, 2t+9) at ph
-        lo = y & (0x00030003u << kp.pl);
-        hi = y & (0x00030003u << kp.ph);
-    } else if constexpr (BITS == 4) {
-        lo = (w[2 * ks] >> kp.s) & (0x000F000Fu << kp.pl);      // channels (t, t+4)
-        hi = (w[2 * ks + 1] >> kp.s) & (0x000F000Fu << kp.pl);  // channels (8+t, 12+t)
-    } else {  // 3
-        const uint64_t x = win3<WPR>(w, ks);
-        lo = (uint32_t)((x >> (6 * t)) & 7u) | ((uint32_t)((x >> (6 * t + 24)) & 7u) << 16);
-        hi = (uint32_t)((x >> (6 * t + 3)) & 7u) | ((uint32_t)((x >> (6 * t + 27)) & 7u) << 16);
-    }
-}
+// ---------------------------------------------------------------------------
+// Quantised V operand.  Row-thread g reads its D/8 channel strings (string
+// i = 2 mt + hi8 is channel 16 mt + 8 hi8 + g); column-thread t takes the
+// codes of tokens (2t, 2t+1) as its low register (position 0) and of tokens
+// (2t+8, 2t+9) as its high register (position VHI).
+// ---------------------------------------------------------------------------
+template <int BITS, int D>
+struct VStr {
+    static constexpr int NS = D / 8;
+    static constexpr int VHI = BITS == 4 ? 4 : 2;
+    uint32_t w[NS];
+    uint32_t hw[BITS == 3 ? NS / 2 : 1];
 
-// Channel read by k-slot `slot` (0..15) of k-step ks.
-template <int BITS>
-__device__ inline int q_channel(int ks, int slot) {
-    const int t = (slot & 7) >> 1, odd = slot & 1, upper = slot >> 3;
-    if constexpr (BITS == 4) {
-        // slots (2t, 2t+1) -> (t, t+4); (2t+8, 2t+9) -> (8+t, 12+t)
-        return 16 * ks + (upper ? 8 : 0) + t + (odd ? 4 : 0);
-    } else if constexpr (BITS == 16) {
-        // per pair of k-steps, thread t holds channels 8t..8t+7 of a 32-block
-        const int kk = ks >> 1, second = ks & 1;
-        return 32 * kk + 8 * t + 4 * second + 2 * upper + odd;
-    } else {
-        // 2 and 3 bits: (2t, 2t+1) -> (2t, 2t+8); (2t+8, 2t+9) -> (2t+1, 2t+9)
-        return 16 * ks + 2 * t + upper + (odd ? 8 : 0);
+    __device__ inline void load(const uint8_t *vb, int g, int t) {
+        const uint8_t *p = BITS == 4 ? vb + 4 * (D * (t >> 1) + g * NS) : vb + 4 * g * NS;
+#pragma unroll
+        for (int i = 0; i < NS / 4; ++i) {
+            const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+            w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+        }
+        if constexpr (BITS == 3) {
+            const uint8_t *h = vb + 4 * D + 2 * g * NS;
+#pragma unroll
+            for (int i = 0; i < NS / 8; ++i) {
+                const uint4 u = reinterpret_cast<const uint4 *>(h)[i];
+                hw[4 * i] = u.x; hw[4 * i + 1] = u.y; hw[4 * i + 2] = u.z; hw[4 * i + 3] = u.w;
+            }
+        }
     }
-}
 
-// V operand (A, rows = channels of m-tile mt, k-slot pair = tokens (a, b)):
-// row_lo -> channel 16 mt + g, row_hi -> channel 16 mt + 8 + g.  A byte
-// permute brings the byte holding channel g of both tokens into the two
-// halves, a mask keeps the code in place (f16 subnormal c * 2^(vp - 24),
-// vp = v_pos(g)); the thread's output rows are rescaled by 2^(24 - vp).
-template <int BITS>
-__device__ inline int v_pos(int g) {
-    return BITS == 2 ? 2 * (g & 3) : BITS == 4 ? 4 * (g & 1) : 0;
-}
-template <int BITS, int WPR>
-__device__ inline void v_pair(const uint32_t (&wa)[WPR], const uint32_t (&wb)[WPR], int mt, int g,
-                              uint32_t &row_lo, uint32_t &row_hi) {
-    if constexpr (BITS == 2) {
-        const uint32_t bi = g >> 2, bh = bi + 2;
-        const uint32_t sl = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
-        const uint32_t sh = bh | (bh << 4) | ((4 + bh) << 8) | ((4 + bh) << 12);
-        const uint32_t m = 0x00030003u << (2 * (g & 3));
-        row_lo = __byte_perm(wa[mt], wb[mt], sl) & m;
-        row_hi = __byte_perm(wa[mt], wb[mt], sh) & m;
-    } else if constexpr (BITS == 4) {
-        const uint32_t bi = g >> 1;
-        const uint32_t sl = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
-        const uint32_t m = 0x000F000Fu << (4 * (g & 1));
-        row_lo = __byte_perm(wa[2 * mt], wb[2 * mt], sl) & m;
-        row_hi = __byte_perm(wa[2 * mt + 1], wb[2 * mt + 1], sl) & m;
-    } else {
-        const uint64_t xa = win3<WPR>(wa, mt), xb = win3<WPR>(wb, mt);
-        row_lo = (uint32_t)((xa >> (3 * g)) & 7u) | ((uint32_t)((xb >> (3 * g)) & 7u) << 16);
-        row_hi = (uint32_t)((xa >> (24 + 3 * g)) & 7u) | ((uint32_t)((xb >> (24 + 3 * g)) & 7u) << 16);
+    __device__ inline void regs(int i, int t, uint32_t &lo, uint32_t &hi) const {
+        if constexpr (BITS == 2) {
+            const uint32_t y = w[i] >> (4 * t);
+            lo = y & 0x00030003u;
+            hi = y & 0x000C000Cu;
+        } else if constexpr (BITS == 4) {
+            const uint32_t y = w[i] >> (8 * (t & 1));
+            lo = y & 0x000F000Fu;
+            hi = y & 0x00F000F0u;
+        } else {
+            const uint32_t y = w[i] >> (4 * t);
+            const uint32_t x = __byte_perm(hw[i >> 1], 0u, (i & 1) ? 0x3424 : 0x1404);
+            const int sp = t == 0 ? 0 : t == 1 ? 1 : t == 2 ? 4 : 5;
+            const uint32_t z = x >> (6 + sp);
+            lo = (y & 0x00030003u) | (z & 0x00040004u);
+            hi = (y & 0x000C000Cu) | (z & 0x00100010u);
+        }
     }
-}
+};
 
-// NG fp16 values (one token's scales or zeros) as floats.
+// NG fp16 values (one token's K scales) as floats.
 template <int NG>
 __device__ inline void load_halves(const __half *p, float (&f)[NG]) {
     if constexpr (NG == 4) {
@@ -186,7 +227,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     uint8_t *ring = smem + warp * C::NSTAGE * C::STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE)) +
                      warp * C::NSTAGE;
-    // pages of this warp: p0 + warp + 4 k
+    // pages of this warp: p0 + warp + NW k
     const int nw = p1 > p0 + warp ? ceil_div(p1 - (p0 + warp), NW) : 0;
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
@@ -236,63 +277,38 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             __syncthreads();
         }
     }
-    // ---- query fragments (B operand of S^T = K Q^T), column n = head g ----
-    const KPos<BITS> kpos(t);
-    uint32_t bq[C::NT][2];
-#pragma unroll
-    for (int ks = 0; ks < C::NT; ++ks) {
-        float v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int slot = (j & 1) + 2 * t + 8 * (j >> 1);
-            v[j] = bf16_bits_to_f32(qs[g * D + q_channel<BITS>(ks, slot)]);
-        }
-        if constexpr (BITS == 16) {
-            bq[ks][0] = pack_bf16(v[0], v[1]);
-            bq[ks][1] = pack_bf16(v[2], v[3]);
-        } else {
-            const float fl = __uint_as_float((uint32_t)(127 - kpos.pl) << 23);  // 2^-pl
-            const float fh = __uint_as_float((uint32_t)(127 - kpos.ph) << 23);
-            bq[ks][0] = pack_f16(v[0] * fl, v[1] * fl);
-            bq[ks][1] = pack_f16(v[2] * fh, v[3] * fh);
-        }
-    }
-    // per-group query sums of the two head columns this thread accumulates
-    float qg[C::NG][2];
-    if constexpr (BITS != 16) {
-#pragma unroll
-        for (int gr = 0; gr < C::NG; ++gr) {
-            qg[gr][0] = qsum[(2 * t) * C::NG + gr];
-            qg[gr][1] = qsum[(2 * t + 1) * C::NG + gr];
-        }
-    }
 
     float o[C::NT][4];
 #pragma unroll
     for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float zacc[C::NG][2];
-#pragma unroll
-    for (int i = 0; i < C::NG; ++i) zacc[i][0] = zacc[i][1] = 0.0f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
     const int src0 = t * 4 + (g >> 1), src1 = (t + 4) * 4 + (g >> 1);
     const bool odd_head = g & 1;
 
-    for (int k = 0; k < nw; ++k) {
-        const int st = k % C::NSTAGE;
-        if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status)) break;
-        const uint8_t *kb = ring + st * C::STAGE;
-        uint8_t *vb = ring + st * C::STAGE + C::HB;
-        const int pg = p0 + warp + NW * k;
-        if (page_id(k) < 0) {  // reported at issue time; nothing landed in this stage
-            __syncwarp();
-            if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
-            continue;
+    if constexpr (BITS == 16) {
+        // ---- bf16 token-drop cache: query fragments (B of S^T = K Q^T) ----
+        uint32_t bq[C::NT][2];
+#pragma unroll
+        for (int ks = 0; ks < C::NT; ++ks) {
+            // per pair of k-steps, thread t holds channels 8t..8t+7 of a 32-block
+            const int kk = ks >> 1, second = ks & 1;
+            const int c0 = 32 * kk + 8 * t + 4 * second;
+            bq[ks][0] = pack_bf16(bf16_bits_to_f32(qs[g * D + c0]), bf16_bits_to_f32(qs[g * D + c0 + 1]));
+            bq[ks][1] = pack_bf16(bf16_bits_to_f32(qs[g * D + c0 + 2]), bf16_bits_to_f32(qs[g * D + c0 + 3]));
         }
-        const int slot0 = 2 * g, slot1 = 2 * g + 1;
-        const int pos0 = pg * kPage + slot0;
-        const bool valid0 = pos0 < len, valid1 = pos0 + 1 < len;
-        float s[4];  // (slot0, head 2t), (slot0, 2t+1), (slot1, 2t), (slot1, 2t+1)
-        if constexpr (BITS == 16) {
+        for (int k = 0; k < nw; ++k) {
+            const int st = k % C::NSTAGE;
+            if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status)) break;
+            const uint8_t *kb = ring + st * C::STAGE;
+            uint8_t *vb = ring + st * C::STAGE + C::HB;
+            const int pg = p0 + warp + NW * k;
+            if (page_id(k) < 0) {  // reported at issue time; nothing landed in this stage
+                __syncwarp();
+                if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+                continue;
+            }
+            const int slot0 = 2 * g, slot1 = 2 * g + 1;
+            const int pos0 = pg * kPage + slot0;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < C::NT / 2; ++kk) {
@@ -303,73 +319,37 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 mma_bf16(acc, a0, bq[2 * kk][0], bq[2 * kk][1]);
                 mma_bf16(acc, a1, bq[2 * kk + 1][0], bq[2 * kk + 1][1]);
             }
+            float s[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) s[j] = acc[j] * a.scale_log2;
-        } else {
-            uint32_t w0[C::WPR], w1[C::WPR];
-            load_row<C::CB>(w0, kb + slot0 * C::CB);
-            load_row<C::CB>(w1, kb + slot1 * C::CB);
-            const __half *scl = reinterpret_cast<const __half *>(kb + kPage * C::CB);
-            const __half *zer = scl + kPage * C::NG;
-            float sc0[C::NG], sc1[C::NG], zr0[C::NG], zr1[C::NG];
-            load_halves<C::NG>(scl + slot0 * C::NG, sc0);
-            load_halves<C::NG>(scl + slot1 * C::NG, sc1);
-            load_halves<C::NG>(zer + slot0 * C::NG, zr0);
-            load_halves<C::NG>(zer + slot1 * C::NG, zr1);
-            const float kscale = a.scale_log2 * 16777216.0f;  // products carry 2^-24
-            s[0] = s[1] = s[2] = s[3] = 0.0f;
+            if (pos0 >= len) s[0] = s[1] = -INFINITY;
+            if (pos0 + 1 >= len) s[2] = s[3] = -INFINITY;
+
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
-            for (int gr = 0; gr < C::NG; ++gr) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            if (__any_sync(0xffffffffu, mn0 > m[0] || mn1 > m[1])) {
+                const float al0 = mn0 == -INFINITY ? 1.0f : ex2(m[0] - mn0);
+                const float al1 = mn1 == -INFINITY ? 1.0f : ex2(m[1] - mn1);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int ks = 2 * gr + h2;
-                    uint32_t af[4];
-                    k_pair<BITS, C::WPR>(w0, ks, t, kpos, af[0], af[2]);
-                    k_pair<BITS, C::WPR>(w1, ks, t, kpos, af[1], af[3]);
-                    mma_f16(acc, af, bq[ks][0], bq[ks][1]);
+                for (int i = 0; i < C::NT; ++i) {
+                    o[i][0] *= al0; o[i][2] *= al0;
+                    o[i][1] *= al1; o[i][3] *= al1;
                 }
-                const float f0 = sc0[gr] * kscale, f1 = sc1[gr] * kscale;
-                s[0] = fmaf(f0, acc[0], fmaf(zr0[gr], qg[gr][0], s[0]));
-                s[1] = fmaf(f0, acc[1], fmaf(zr0[gr], qg[gr][1], s[1]));
-                s[2] = fmaf(f1, acc[2], fmaf(zr1[gr], qg[gr][0], s[2]));
-                s[3] = fmaf(f1, acc[3], fmaf(zr1[gr], qg[gr][1], s[3]));
+                l[0] *= al0;
+                l[1] *= al1;
+                m[0] = mn0;
+                m[1] = mn1;
             }
-        }
-        // mask positions past the request length (their slots may hold garbage)
-        if (!valid0) s[0] = s[1] = -INFINITY;
-        if (!valid1) s[2] = s[3] = -INFINITY;
+            const float ms0 = m[0] == -INFINITY ? 0.0f : m[0], ms1 = m[1] == -INFINITY ? 0.0f : m[1];
+            const float p[4] = {ex2(s[0] - ms0), ex2(s[1] - ms1), ex2(s[2] - ms0), ex2(s[3] - ms1)};
+            l[0] += p[0] + p[2];
+            l[1] += p[1] + p[3];
 
-        // ---- online softmax over the page (per head column) ----
-        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        if (__any_sync(0xffffffffu, mn0 > m[0] || mn1 > m[1])) {
-            const float al0 = mn0 == -INFINITY ? 1.0f : ex2(m[0] - mn0);
-            const float al1 = mn1 == -INFINITY ? 1.0f : ex2(m[1] - mn1);
-#pragma unroll
-            for (int i = 0; i < C::NT; ++i) {
-                o[i][0] *= al0; o[i][2] *= al0;
-                o[i][1] *= al1; o[i][3] *= al1;
-            }
-#pragma unroll
-            for (int i = 0; i < C::NG; ++i) { zacc[i][0] *= al0; zacc[i][1] *= al1; }
-            l[0] *= al0;
-            l[1] *= al1;
-            m[0] = mn0;
-            m[1] = mn1;
-        }
-        const float ms0 = m[0] == -INFINITY ? 0.0f : m[0], ms1 = m[1] == -INFINITY ? 0.0f : m[1];
-        const float p[4] = {ex2(s[0] - ms0), ex2(s[1] - ms1), ex2(s[2] - ms0), ex2(s[3] - ms1)};
-        l[0] += p[0] + p[2];
-        l[1] += p[1] + p[3];
-
-        // ---- O^T += V^T P^T ----
-        if constexpr (BITS == 16) {
             const int nvalid = len - pg * kPage;  // slots >= nvalid are past the end
             if (nvalid < kPage) {
                 for (int c = lane; c < (kPage - nvalid) * D / 8; c += 32)
@@ -388,71 +368,202 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 ldsm_x4_t(af, vrow + 16 * mt * 2);
                 mma_bf16(o[mt], af, b0, b1);
             }
-        } else {
-            uint32_t wa[C::WPR], wb[C::WPR], wc[C::WPR], wd[C::WPR];
-            load_row<C::CB>(wa, vb + (2 * t) * C::CB);
-            load_row<C::CB>(wb, vb + (2 * t + 1) * C::CB);
-            load_row<C::CB>(wc, vb + (2 * t + 8) * C::CB);
-            load_row<C::CB>(wd, vb + (2 * t + 9) * C::CB);
-            const __half *vscl = reinterpret_cast<const __half *>(vb + kPage * C::CB);
-            const __half *vzer = vscl + kPage * C::NG;
-            // V scale / zero of this thread's tokens (slot0, slot1); slots past
-            // the end contribute exactly nothing, whatever their bytes hold
-            float vsc0[C::NG], vsc1[C::NG], vze0[C::NG], vze1[C::NG];
-            load_halves<C::NG>(vscl + slot0 * C::NG, vsc0);
-            load_halves<C::NG>(vscl + slot1 * C::NG, vsc1);
-            load_halves<C::NG>(vzer + slot0 * C::NG, vze0);
-            load_halves<C::NG>(vzer + slot1 * C::NG, vze1);
+            __syncwarp();
+            if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+        }
+    } else {
+        // ---- quantised cache ----
+        // Q fragments: B of S^T = K Q^T, column n = head g, k-slot pair of
+        // register r pre-scaled by 2^-kpos(r) so every product is c q 2^-24.
+        uint32_t bq[C::NT][2];
+#pragma unroll
+        for (int ks = 0; ks < C::NT; ++ks) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c0 = 16 * ks + 4 * t + 2 * h;
+                const float f = __uint_as_float((uint32_t)(127 - kpos<BITS>(2 * ks + h)) << 23);
+                bq[ks][h] = pack_f16(bf16_bits_to_f32(qs[g * D + c0]) * f, bf16_bits_to_f32(qs[g * D + c0 + 1]) * f);
+            }
+        }
+        // Zero-point term of the scores as one more MMA: k-slots (2t, 2t+1)
+        // carry groups (2P, 2P+1), P = t & 1, as the hi (t < 2) or lo (t >= 2)
+        // f16 part of the pre-scaled query group sums.
+        const int zp = t & 1;
+        const bool zuse = 2 * zp + 1 < C::NG;
+        uint32_t bz = 0u;
+        if (zuse) {
+            const float s0 = qsum[g * C::NG + 2 * zp], s1 = qsum[g * C::NG + 2 * zp + 1];
+            const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+            if (t < 2) {
+                bz = pack_f16(__half2float(h0), __half2float(h1));
+            } else {
+                bz = pack_f16(s0 - __half2float(h0), s1 - __half2float(h1));
+            }
+        }
+        float oz[4] = {0.f, 0.f, 0.f, 0.f};  // V zero-point term, rows = groups, columns = heads
+        const float kscale = a.scale_log2 * 16777216.0f;  // products carry 2^-24
+        constexpr float kVhi = VStr<BITS, D>::VHI == 4 ? 0.0625f : 0.25f;
+        const uint32_t vhi_scale = pack_f16(kVhi, kVhi);
+
+        for (int k = 0; k < nw; ++k) {
+            const int st = k % C::NSTAGE;
+            if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status)) break;
+            const uint8_t *kb = ring + st * C::STAGE;
+            uint8_t *vb = ring + st * C::STAGE + C::HB;
+            const int pg = p0 + warp + NW * k;
+            if (page_id(k) < 0) {
+                __syncwarp();
+                if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+                continue;
+            }
+            const int nvalid = len - pg * kPage;  // slots >= nvalid are past the end
+
+            // ---- S^T = K Q^T per group, scaled and summed ----
+            KRow<BITS, D> r0, r1;  // tokens 2g (rows g) and 2g+1 (rows g+8)
+            r0.load(kb + (2 * g) * (D * BITS / 8), t);
+            r1.load(kb + (2 * g + 1) * (D * BITS / 8), t);
+            const __half *ksc = reinterpret_cast<const __half *>(kb + C::CR);
+            const __half *kzr = ksc + kPage * C::NG;
+            float sc0[C::NG], sc1[C::NG];
+            load_halves<C::NG>(ksc + (2 * g) * C::NG, sc0);
+            load_halves<C::NG>(ksc + (2 * g + 1) * C::NG, sc1);
+            f2 s01 = {0.f, 0.f}, s23 = {0.f, 0.f};
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
-                const float vs0 = valid0 ? vsc0[gr] : 0.0f, vs1 = valid1 ? vsc1[gr] : 0.0f;
-                const float vz0 = valid0 ? vze0[gr] : 0.0f, vz1 = valid1 ? vze1[gr] : 0.0f;
-                zacc[gr][0] = fmaf(p[0], vz0, fmaf(p[2], vz1, zacc[gr][0]));
-                zacc[gr][1] = fmaf(p[1], vz0, fmaf(p[3], vz1, zacc[gr][1]));
-                const uint32_t e = pack_f16(p[0] * vs0, p[2] * vs1), od = pack_f16(p[1] * vs0, p[3] * vs1);
-                const uint32_t e0 = __shfl_sync(0xffffffffu, e, src0), o0 = __shfl_sync(0xffffffffu, od, src0);
-                const uint32_t e1 = __shfl_sync(0xffffffffu, e, src1), o1 = __shfl_sync(0xffffffffu, od, src1);
-                const uint32_t b0 = odd_head ? o0 : e0, b1 = odd_head ? o1 : e1;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int ks = 2 * gr + h2;
+                    const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
+                    mma_f16(acc, af, bq[ks][0], bq[ks][1]);
+                }
+                s01 = fma2(f2{sc0[gr], sc0[gr]}, f2{acc[0], acc[1]}, s01);
+                s23 = fma2(f2{sc1[gr], sc1[gr]}, f2{acc[2], acc[3]}, s23);
+            }
+            float z[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                uint32_t za[4] = {0u, 0u, 0u, 0u};
+                if (zuse) {
+                    za[0] = *reinterpret_cast<const uint32_t *>(kzr + (2 * g) * C::NG + 2 * zp);
+                    za[1] = *reinterpret_cast<const uint32_t *>(kzr + (2 * g + 1) * C::NG + 2 * zp);
+                }
+                mma_f16(z, za, bz, 0u);
+            }
+            const float ms0 = m[0] == -INFINITY ? 0.0f : m[0], ms1 = m[1] == -INFINITY ? 0.0f : m[1];
+            const f2 zm01 = {z[0] - ms0, z[1] - ms1}, zm23 = {z[2] - ms0, z[3] - ms1};
+            const f2 x01 = fma2(s01, f2{kscale, kscale}, zm01), x23 = fma2(s23, f2{kscale, kscale}, zm23);
+            float x[4] = {x01.x, x01.y, x23.x, x23.y};  // log2 score - running max
+            if (nvalid < kPage) {  // ragged last page: mask, and clear V parameters of empty slots
+                if (2 * g >= nvalid) x[0] = x[1] = -INFINITY;
+                if (2 * g + 1 >= nvalid) x[2] = x[3] = -INFINITY;
+                uint16_t *vpar = reinterpret_cast<uint16_t *>(vb + C::CR);
+                for (int e = lane; e < (kPage - nvalid) * C::NG; e += 32) {
+                    const int tau = nvalid + e / C::NG, gr = e % C::NG;
+                    const int t2 = (tau >> 1) & 3, i2 = 2 * (tau >> 3) + (tau & 1);
+                    vpar[(t2 * C::NG + gr) * 4 + i2] = 0;
+                    vpar[kPage * C::NG + (t2 * C::NG + gr) * 4 + i2] = 0;
+                }
+                __syncwarp();
+            }
+
+            // ---- online softmax: rescale only when a score beats the running max ----
+            const float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            if (__any_sync(0xffffffffu, mx > 0.0f || m[0] == -INFINITY || m[1] == -INFINITY)) {
+                float sv[4] = {x[0] + ms0, x[1] + ms1, x[2] + ms0, x[3] + ms1};
+                float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+                const float al0 = (mn0 == -INFINITY || m[0] == mn0) ? 1.0f : ex2(m[0] - mn0);
+                const float al1 = (mn1 == -INFINITY || m[1] == mn1) ? 1.0f : ex2(m[1] - mn1);
+#pragma unroll
+                for (int i = 0; i < C::NT; ++i) {
+                    o[i][0] *= al0; o[i][2] *= al0;
+                    o[i][1] *= al1; o[i][3] *= al1;
+                }
+                oz[0] *= al0; oz[2] *= al0;
+                oz[1] *= al1; oz[3] *= al1;
+                l[0] *= al0;
+                l[1] *= al1;
+                m[0] = mn0;
+                m[1] = mn1;
+                const float n0 = mn0 == -INFINITY ? 0.0f : mn0, n1 = mn1 == -INFINITY ? 0.0f : mn1;
+                x[0] = sv[0] - n0; x[1] = sv[1] - n1; x[2] = sv[2] - n0; x[3] = sv[3] - n1;
+            }
+            const float p[4] = {ex2(x[0]), ex2(x[1]), ex2(x[2]), ex2(x[3])};
+            l[0] += p[0] + p[2];
+            l[1] += p[1] + p[3];
+
+            // ---- P^T as the B operand: k-slot = token, column = head ----
+            const uint32_t e = pack_f16(p[0], p[2]), od = pack_f16(p[1], p[3]);
+            const uint32_t e0 = __shfl_sync(0xffffffffu, e, src0), o0 = __shfl_sync(0xffffffffu, od, src0);
+            const uint32_t e1 = __shfl_sync(0xffffffffu, e, src1), o1 = __shfl_sync(0xffffffffu, od, src1);
+            const uint32_t blo = odd_head ? o0 : e0, bhi = odd_head ? o1 : e1;
+            const uint32_t bhi_s = hmul2(bhi, vhi_scale);
+
+            // ---- O^T += V^T (P s)^T, zero points as one more MMA ----
+            VStr<BITS, D> vs;
+            vs.load(vb, g, t);
+            const uint8_t *vpar = vb + C::CR;
+            uint32_t vsc[2 * C::NG];
+            {
+                const uint32_t *pp = reinterpret_cast<const uint32_t *>(vpar + t * 8 * C::NG);
+#pragma unroll
+                for (int i = 0; i < 2 * C::NG; i += 4) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(pp + i);
+                    vsc[i] = u.x; vsc[i + 1] = u.y; vsc[i + 2] = u.z; vsc[i + 3] = u.w;
+                }
+            }
+#pragma unroll
+            for (int gr = 0; gr < C::NG; ++gr) {
+                const uint32_t b0 = hmul2(blo, vsc[2 * gr]), b1 = hmul2(bhi_s, vsc[2 * gr + 1]);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int mt = 2 * gr + h2;
                     uint32_t af[4];
-                    v_pair<BITS, C::WPR>(wa, wb, mt, g, af[0], af[1]);
-                    v_pair<BITS, C::WPR>(wc, wd, mt, g, af[2], af[3]);
+                    vs.regs(2 * mt, t, af[0], af[2]);
+                    vs.regs(2 * mt + 1, t, af[1], af[3]);
                     mma_f16(o[mt], af, b0, b1);
                 }
             }
+            {
+                uint32_t za[4] = {0u, 0u, 0u, 0u};
+                if (g < C::NG) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
+                    za[0] = u.x;
+                    za[2] = u.y;
+                }
+                mma_f16(oz, za, blo, bhi);
+            }
+            __syncwarp();
+            if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
         }
-        __syncwarp();
-        if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+        // ---- finish O^T: 2^24 * codes part + zero-point part of the channel's group ----
+#pragma unroll
+        for (int gr = 0; gr < C::NG; ++gr) {
+            const float z0 = __shfl_sync(0xffffffffu, oz[0], gr * 4 + t);
+            const float z1 = __shfl_sync(0xffffffffu, oz[1], gr * 4 + t);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int mt = 2 * gr + h2;
+                o[mt][0] = fmaf(o[mt][0], 16777216.0f, z0);
+                o[mt][2] = fmaf(o[mt][2], 16777216.0f, z0);
+                o[mt][1] = fmaf(o[mt][1], 16777216.0f, z1);
+                o[mt][3] = fmaf(o[mt][3], 16777216.0f, z1);
+            }
+        }
     }
 
-    // ---- warp epilogue: finish l and the zero terms ----
+    // ---- warp epilogue: finish l ----
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
         l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
     }
-    if constexpr (BITS != 16) {
-#pragma unroll
-        for (int gr = 0; gr < C::NG; ++gr) {
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                zacc[gr][0] += __shfl_xor_sync(0xffffffffu, zacc[gr][0], off);
-                zacc[gr][1] += __shfl_xor_sync(0xffffffffu, zacc[gr][1], off);
-            }
-        }
-        const float osc = __uint_as_float((uint32_t)(127 + 24 - v_pos<BITS>(g)) << 23);  // 2^(24 - vp)
-#pragma unroll
-        for (int mt = 0; mt < C::NT; ++mt) {
-            const int gr = mt / 2;
-            o[mt][0] = fmaf(o[mt][0], osc, zacc[gr][0]);
-            o[mt][2] = fmaf(o[mt][2], osc, zacc[gr][0]);
-            o[mt][1] = fmaf(o[mt][1], osc, zacc[gr][1]);
-            o[mt][3] = fmaf(o[mt][3], osc, zacc[gr][1]);
-        }
-    }
-    // ---- combine the 4 warps of the CTA in shared memory ----
+    // ---- combine the warps of the CTA in shared memory ----
     __syncthreads();  // every warp is done with its ring
     float *cm = reinterpret_cast<float *>(smem);   // [warp][8] m
     float *cl = cm + NW * 8;                    // [warp][8] l

@@ -53,6 +53,8 @@ def test_page_sizes_follow_the_layout(vc):
     assert vc.head_block_bytes(64, 4) == 640
     assert vc.page_bytes(8, 128, 2) == 8 * 768
     assert vc.head_block_bytes(128, 5) == 0          # unsupported width
+    assert vc.head_block_bytes(32, 16) == 1024
+    assert vc.head_block_bytes(32, 2) == 0           # quantised formats need head_dim % 64 == 0
 
 
 def test_struct_layout_matches_c(vc):

@@ -36,8 +36,10 @@ def check(comp, ctable, hfull, kept_lists, bits, start=None):
                 assert np.array_equal(got[key], ref[key]), (b, key)
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 16])
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+SHAPES = [(bits, d) for bits in (2, 3, 4, 16) for d in (32, 64, 128, 256) if bits == 16 or d % 64 == 0]
+
+
+@pytest.mark.parametrize("bits,d", SHAPES)
 def test_compress_random_shapes(bits, d):
     rng = np.random.default_rng(100 + bits * 7 + d)
     lens = [37, 500, 16, 1]
@@ -62,7 +64,7 @@ def test_compress_append_offsets(bits):
     start = [23, 50]
     assert run_compress(full, comp, kept, comp_start=start) == 0
     check(comp, ctable, hf, kept, bits, start=start)
-    before = H.read_comp(comp.k_pages, ctable[0], 23, hkv, d, bits)
+    before = H.read_comp(comp.k_pages, ctable[0], 23, hkv, d, bits, "k")
     assert not before["packed"].any() and not before["scales"].any()
 
 

@@ -55,28 +55,100 @@ def comp_cache(rng, batch, capacity, hkv, d, bits, zero=False):
     return comp, table
 
 
-def read_comp(pool: torch.Tensor, table_row: np.ndarray, n: int, hkv: int, d: int, bits: int) -> dict:
-    """GPU comp pool -> oracle.compress-style logical dict for one request."""
+# Code placement inside a quantised head block (the page format in
+# include/vc.h): bit offset of each (token, channel) code, per plane.
+def k_bit(bits: int, d: int, s, c, plane: int = 0):
+    s, c = np.asarray(s), np.asarray(c)
+    ks, t, e = c >> 4, (c >> 2) & 3, c & 3
+    r, half = 2 * ks + (e >> 1), e & 1
+    if bits == 2:
+        return s * 2 * d + t * (d // 2) + 32 * (r >> 3) + 16 * half + 2 * (r & 7)
+    if bits == 4:
+        return s * 4 * d + t * d + 32 * (r >> 2) + 16 * half + 4 * (r & 3)
+    if plane == 0:
+        return s * 3 * d + t * (d // 2) + 32 * (r >> 3) + 16 * half + 2 * (r & 7)
+    u, j = r >> 3, r & 7
+    beta = 2 * (j & 3) + np.array([0, 1, 8, 9])[2 * (u & 1) + (j >> 2)]
+    if d == 64:
+        return s * 3 * d + 2 * d + t * 16 + 8 * half + beta
+    return s * 3 * d + 2 * d + t * (d // 4) + 32 * (u >> 1) + 16 * half + beta
+
+
+def v_bit(bits: int, d: int, tau, c, plane: int = 0):
+    tau, c = np.asarray(tau), np.asarray(c)
+    lam = (c & 7) * (d // 8) + 2 * (c >> 4) + ((c >> 3) & 1)
+    t, h, half = (tau >> 1) & 3, tau >> 3, tau & 1
+    if bits == 2 or (bits == 3 and plane == 0):
+        return 32 * lam + 16 * half + 4 * t + 2 * h
+    if bits == 4:
+        return 32 * (d * (t >> 1) + lam) + 16 * half + 8 * (t & 1) + 4 * h
+    return 32 * d + 16 * lam + 8 * half + np.array([0, 1, 4, 5])[t] + 2 * h
+
+
+def v_param(g: int, tau, gr):
+    tau, gr = np.asarray(tau), np.asarray(gr)
+    return (((tau >> 1) & 3) * g + gr) * 4 + 2 * (tau >> 3) + (tau & 1)
+
+
+def _bits_at(region: np.ndarray, off: np.ndarray, width: int) -> np.ndarray:
+    """region: [..., nbytes] uint8; off: bit offsets (broadcast over the
+    leading axes) -> unsigned fields of `width` bits (never straddling a byte
+    pair boundary within a 32-bit word)."""
+    w = region.view("<u4")
+    word = w[..., off >> 5]
+    return ((word >> (off & 31).astype(np.uint32)) & np.uint32((1 << width) - 1)).astype(np.uint8)
+
+
+def _pack_le(codes: np.ndarray, bits: int) -> np.ndarray:
+    """codes [..., D] -> little-endian packing (channel i at bits [bits*i,
+    bits*i + bits) of the row's byte string), the oracle's logical layout."""
+    d = codes.shape[-1]
+    bitv = ((codes[..., :, None] >> np.arange(bits, dtype=np.uint8)) & 1).reshape(*codes.shape[:-1], d * bits)
+    return np.packbits(bitv, axis=-1, bitorder="little")
+
+
+def decode_codes(blk: np.ndarray, d: int, bits: int, kind: str) -> np.ndarray:
+    """Code regions of quantised K ("k") or V ("v") head blocks [n, HB] ->
+    codes [n][16 tokens][d] uint8."""
+    s = np.arange(PAGE)[:, None]
+    c = np.arange(d)[None, :]
+    reg = np.ascontiguousarray(blk[:, :PAGE * d * bits // 8])
+    f = k_bit if kind == "k" else v_bit
+    if bits == 3:
+        return _bits_at(reg, f(3, d, s, c, 0), 2) | (_bits_at(reg, f(3, d, s, c, 1), 1) << 2)
+    return _bits_at(reg, f(bits, d, s, c), bits)
+
+
+def read_comp(pool: torch.Tensor, table_row: np.ndarray, n: int, hkv: int, d: int, bits: int,
+              kind: str = "k") -> dict:
+    """GPU comp pool -> oracle.compress-style logical dict for one request
+    (`kind` "k" or "v": the two pools place codes and parameters
+    differently)."""
     p = pool.cpu().numpy()
     B = hb(d, bits)
     npg = (n + PAGE - 1) // PAGE
-    blk = p.reshape(p.shape[0], hkv, B)[table_row[:npg]]          # [npg][hkv][B]
+    blk = p.reshape(p.shape[0], hkv, B)[table_row[:npg]].reshape(npg * hkv, B)   # [npg*hkv][B]
     if bits == 16:
         x = blk.view(np.uint16).reshape(npg, hkv, PAGE, d).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, d)
         return dict(bits=16, x16=x[:n])
     cb, ng = d * bits // 8, d // GROUP
-    codes = blk[:, :, :PAGE * cb].reshape(npg, hkv, PAGE, cb).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, cb)
-    sc = blk[:, :, PAGE * cb:PAGE * cb + PAGE * ng * 2].copy().view(np.uint16).reshape(npg, hkv, PAGE, ng)
-    ze = blk[:, :, PAGE * cb + PAGE * ng * 2:].copy().view(np.uint16).reshape(npg, hkv, PAGE, ng)
-    sc = sc.transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
-    ze = ze.transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
-    return dict(bits=bits, packed=codes[:n], scales=sc[:n], zeros=ze[:n])
+    codes = decode_codes(blk, d, bits, kind)
+    codes = codes.reshape(npg, hkv, PAGE, d).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, d)
+    par = blk[:, PAGE * cb:].copy().view(np.uint16).reshape(npg * hkv, 2, PAGE * ng)
+    if kind == "k":
+        sc, ze = par[:, 0].reshape(npg * hkv, PAGE, ng), par[:, 1].reshape(npg * hkv, PAGE, ng)
+    else:
+        idx = v_param(ng, np.arange(PAGE)[:, None], np.arange(ng)[None, :])
+        sc, ze = par[:, 0][:, idx], par[:, 1][:, idx]
+    sc = sc.reshape(npg, hkv, PAGE, ng).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
+    ze = ze.reshape(npg, hkv, PAGE, ng).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
+    return dict(bits=bits, packed=_pack_le(codes[:n], bits), scales=sc[:n], zeros=ze[:n])
 
 
 def read_comp_kv(comp, table: np.ndarray, b: int, n: int) -> dict:
     """Both K and V of request b in the layout of oracle.compress."""
-    kk = read_comp(comp.k_pages, table[b], n, comp.num_kv_heads, comp.head_dim, comp.bits)
-    vv = read_comp(comp.v_pages, table[b], n, comp.num_kv_heads, comp.head_dim, comp.bits)
+    kk = read_comp(comp.k_pages, table[b], n, comp.num_kv_heads, comp.head_dim, comp.bits, "k")
+    vv = read_comp(comp.v_pages, table[b], n, comp.num_kv_heads, comp.head_dim, comp.bits, "v")
     if comp.bits == 16:
         return dict(bits=16, k16=kk["x16"], v16=vv["x16"])
     return dict(bits=comp.bits, k_packed=kk["packed"], k_scales=kk["scales"], k_zeros=kk["zeros"],
