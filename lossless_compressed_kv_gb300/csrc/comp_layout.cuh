@@ -11,10 +11,13 @@
 //    is operand register r = 2 ks + (e >> 1), half e & 1: the two codes of a
 //    register sit at the same bit position of the two 16-bit halves of one
 //    word, so a mask leaves two f16 subnormals that are exactly code * 2^(p-24).
-//  * V codes, one string of 16 token codes per channel (channel-major), the
-//    D/8 strings that one fragment row-thread g needs stored contiguously.
-//    Token tau is operand k-slot tau; the string puts tokens (2t, 2t+1) and
-//    (2t+8, 2t+9) of thread t at the same position of the two halves.
+//  * V codes, regions per fragment thread (g, t) of the V^T P^T product:
+//    thread (g, t) owns the codes of channels {16 mt + g, 16 mt + 8 + g}
+//    (all m-tiles mt) for tokens {2t, 2t+1, 2t+8, 2t+9}.  An operand
+//    register holds one channel of tokens (2t, 2t+1) or (2t+8, 2t+9); the
+//    four registers of an m-tile sit at positions p, p+VHI (second token
+//    pair) and, for the row g+8 channel, 4 higher (2- and 3-bit) or one
+//    byte higher (4-bit).
 //  * 3 bits: the low two bits of each code use the 2-bit placement, the high
 //    bit a separate plane placed so that one shift and mask put it right
 //    above the low bits of its register.
@@ -43,21 +46,21 @@ __host__ __device__ inline int k_bit(int bits, int D, int s, int c, int plane) {
     return s * 3 * D + 2 * D + t * (D / 4) + 32 * (u >> 1) + 16 * half + beta;
 }
 
-// Index of channel c's string among the D V strings.
-__host__ __device__ inline int v_string(int D, int c) {
-    const int g = c & 7, hi8 = (c >> 3) & 1, mt = c >> 4;
-    return g * (D / 8) + 2 * mt + hi8;
-}
-
 // V code of token tau of channel c; plane 1 = high bit of a 3-bit code.
 __host__ __device__ inline int v_bit(int bits, int D, int tau, int c, int plane) {
-    const int lam = v_string(D, c);
-    const int t = (tau >> 1) & 3, h = tau >> 3, half = tau & 1;
-    if (bits == 2) return 32 * lam + 16 * half + 4 * t + 2 * h;
-    if (bits == 4) return 32 * (D * (t >> 1) + lam) + 16 * half + 8 * (t & 1) + 4 * h;
-    if (plane == 0) return 32 * lam + 16 * half + 4 * t + 2 * h;
-    const int sp = t == 0 ? 0 : t == 1 ? 1 : t == 2 ? 4 : 5;
-    return 32 * D + 16 * lam + 8 * half + sp + 2 * h;
+    const int g = c & 7, row8 = (c >> 3) & 1, mt = c >> 4;
+    const int t = (tau >> 1) & 3, hi = tau >> 3, half = tau & 1;
+    const int region = g * 4 + t;
+    if (bits == 4) return 32 * (region * (D / 16) + mt) + 16 * half + 8 * row8 + 4 * hi;
+    const int u = mt >> 1, m = mt & 1;  // word of the region: one 32-channel group
+    if (plane == 0) return 32 * (region * (D / 32) + u) + 16 * half + 8 * m + 4 * row8 + 2 * hi;
+    // 3 bits, high bit of the register at low-plane position p = 2 j (j < 4)
+    // of word u, shift 8 m: placed in a high-plane word so that one of four
+    // shifts lines it up at p + 2
+    const int j = 2 * row8 + hi;
+    const int set = 2 * (u & 1) + m;
+    const int beta = 2 * j + (set == 0 ? 0 : set == 1 ? 1 : set == 2 ? 8 : 9);
+    return 32 * D + 32 * (region * (D / 64) + (u >> 1)) + 16 * half + beta;
 }
 
 // Element index (in fp16 units from the start of the V scale array) of the

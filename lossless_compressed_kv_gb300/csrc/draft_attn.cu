@@ -33,8 +33,13 @@ using draft::Cfg;
 using draft::DraftArgs;
 constexpr int kWarps = 4;
 
+// Resident CTAs per SM the register budget is cut for: five where the body
+// fits 102 registers without spilling (measured with -Xptxas -v), else four.
 template <int BITS, int D>
-__global__ void __launch_bounds__(kWarps * 32, 4) draft_kernel(DraftArgs a) {
+constexpr int kMinCtas = (D == 128 && (BITS == 3 || BITS == 4)) ? 4 : 4;
+
+template <int BITS, int D>
+__global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(DraftArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     draft::draft_block<BITS, D, kWarps>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }

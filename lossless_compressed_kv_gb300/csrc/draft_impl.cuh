@@ -32,8 +32,10 @@ struct Cfg {
     static constexpr int STAGE = 2 * HB;
     static constexpr int RING = NW * NSTAGE * STAGE;
     static constexpr int COMBINE = NW * 8 * (D + 2) * 4;
-    static constexpr int BARS = NW * NSTAGE * 8;
-    static constexpr int QS = 8 * D * 2 + 8 * NG * 4;  // q of the group (bf16) + its group sums
+    static constexpr int BARS = NW * NSTAGE * 8 + NW * NSTAGE * 4;  // mbarriers + per-stage page-valid flags
+    // q of the group (bf16) + its group sums + the quantised path's packed
+    // query fragments ([NT/2][32 lanes][4 words])
+    static constexpr int QS = 8 * D * 2 + 8 * NG * 4 + (BITS == 16 ? 0 : NT / 2 * 32 * 16);
     static constexpr int SMEM = (RING > COMBINE ? RING : COMBINE) + BARS + QS;
 };
 
@@ -148,51 +150,65 @@ struct KRow {
 };
 
 // ---------------------------------------------------------------------------
-// Quantised V operand.  Row-thread g reads its D/8 channel strings (string
-// i = 2 mt + hi8 is channel 16 mt + 8 hi8 + g); column-thread t takes the
-// codes of tokens (2t, 2t+1) as its low register (position 0) and of tokens
-// (2t+8, 2t+9) as its high register (position VHI).
+// Quantised V operand.  Thread (g, t) reads its region (channels 16 mt + g
+// and 16 mt + 8 + g, tokens 2t, 2t+1, 2t+8, 2t+9) and forms the four A
+// registers of m-tile mt: a0 / a2 = channel 16 mt + g with tokens (2t, 2t+1)
+// / (2t+8, 2t+9), a1 / a3 the same for channel 16 mt + 8 + g.  a2 and a3 sit
+// VHI above a0 and a1 (the B operand of the second token pair carries
+// 2^-VHI); a1 and a3 sit ROW8 above a0 and a2 (compensated on the output
+// rows g+8).
 // ---------------------------------------------------------------------------
 template <int BITS, int D>
-struct VStr {
-    static constexpr int NS = D / 8;
+struct VReg {
+    static constexpr int NW = BITS == 4 ? D / 16 : D / 32;  // main-plane words of the region
+    static constexpr int NH = BITS == 3 ? D / 64 : 0;       // high-plane words (3 bits)
     static constexpr int VHI = BITS == 4 ? 4 : 2;
-    uint32_t w[NS];
-    uint32_t hw[BITS == 3 ? NS / 2 : 1];
+    static constexpr int ROW8 = BITS == 4 ? 0 : 4;
+    uint32_t w[NW];
+    uint32_t hw[NH > 0 ? NH : 1];
 
-    __device__ inline void load(const uint8_t *vb, int g, int t) {
-        const uint8_t *p = BITS == 4 ? vb + 4 * (D * (t >> 1) + g * NS) : vb + 4 * g * NS;
+    template <int N>
+    __device__ static inline void ld(uint32_t (&dst)[N], const uint8_t *p) {
+        if constexpr (N == 1) {
+            dst[0] = *reinterpret_cast<const uint32_t *>(p);
+        } else if constexpr (N == 2) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p);
+            dst[0] = u.x; dst[1] = u.y;
+        } else {
 #pragma unroll
-        for (int i = 0; i < NS / 4; ++i) {
-            const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
-            w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
-        }
-        if constexpr (BITS == 3) {
-            const uint8_t *h = vb + 4 * D + 2 * g * NS;
-#pragma unroll
-            for (int i = 0; i < NS / 8; ++i) {
-                const uint4 u = reinterpret_cast<const uint4 *>(h)[i];
-                hw[4 * i] = u.x; hw[4 * i + 1] = u.y; hw[4 * i + 2] = u.z; hw[4 * i + 3] = u.w;
+            for (int i = 0; i < N / 4; ++i) {
+                const uint4 u = reinterpret_cast<const uint4 *>(p)[i];
+                dst[4 * i] = u.x; dst[4 * i + 1] = u.y; dst[4 * i + 2] = u.z; dst[4 * i + 3] = u.w;
             }
         }
     }
 
-    __device__ inline void regs(int i, int t, uint32_t &lo, uint32_t &hi) const {
-        if constexpr (BITS == 2) {
-            const uint32_t y = w[i] >> (4 * t);
-            lo = y & 0x00030003u;
-            hi = y & 0x000C000Cu;
-        } else if constexpr (BITS == 4) {
-            const uint32_t y = w[i] >> (8 * (t & 1));
-            lo = y & 0x000F000Fu;
-            hi = y & 0x00F000F0u;
+    __device__ inline void load(const uint8_t *vb, int g, int t) {
+        const int region = g * 4 + t;
+        ld<NW>(w, vb + 4 * region * NW);
+        if constexpr (BITS == 3) ld<NH>(hw, vb + 4 * D + 4 * region * NH);
+    }
+
+    __device__ inline void regs(int mt, uint32_t (&a)[4]) const {
+        if constexpr (BITS == 4) {
+            const uint32_t x = w[mt], y = x >> 8;
+            a[0] = x & 0x000F000Fu; a[2] = x & 0x00F000F0u;
+            a[1] = y & 0x000F000Fu; a[3] = y & 0x00F000F0u;
         } else {
-            const uint32_t y = w[i] >> (4 * t);
-            const uint32_t x = __byte_perm(hw[i >> 1], 0u, (i & 1) ? 0x3424 : 0x1404);
-            const int sp = t == 0 ? 0 : t == 1 ? 1 : t == 2 ? 4 : 5;
-            const uint32_t z = x >> (6 + sp);
-            lo = (y & 0x00030003u) | (z & 0x00040004u);
-            hi = (y & 0x000C000Cu) | (z & 0x00100010u);
+            const int u = mt >> 1, m = mt & 1;
+            const uint32_t y = m ? (w[u] >> 8) : w[u];
+            if constexpr (BITS == 2) {
+                a[0] = y & 0x00030003u; a[2] = y & 0x000C000Cu;
+                a[1] = y & 0x00300030u; a[3] = y & 0x00C000C0u;
+            } else {
+                const int set = 2 * (u & 1) + m;
+                const uint32_t h = hw[u >> 1];
+                const uint32_t z = set == 0 ? (h << 2) : set == 1 ? (h << 1) : set == 2 ? (h >> 6) : (h >> 7);
+                a[0] = (y & 0x00030003u) | (z & 0x00040004u);
+                a[2] = (y & 0x000C000Cu) | (z & 0x00100010u);
+                a[1] = (y & 0x00300030u) | (z & 0x00400040u);
+                a[3] = (y & 0x00C000C0u) | (z & 0x01000100u);
+            }
         }
     }
 };
@@ -231,24 +247,43 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     const int nw = p1 > p0 + warp ? ceil_div(p1 - (p0 + warp), NW) : 0;
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
-    auto page_id = [&](int k) -> int {
-        const int pg = p0 + warp + NW * k;
+    int *sflag = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + (C::RING > C::COMBINE ? C::RING
+                                                                                                : C::COMBINE)) +
+                                         NW * C::NSTAGE) +
+                 warp * C::NSTAGE;
+
+    // Page ids of this warp's pages, 32 at a time: lane i holds page 32 blk + i
+    // (-1: past the warp's pages or not a valid page id).  Two blocks are kept
+    // so the table reads run a block ahead of the copies.
+    auto load_ids = [&](int blk) -> int {
+        const int kk = 32 * blk + lane;
+        if (kk >= nw) return -1;
+        const int pg = p0 + warp + NW * kk;
         const int id = pg < a.maxb ? trow[pg] : -1;
         return (id >= 0 && id < a.n_pages) ? id : -1;
     };
-    auto issue = [&](int k) {  // lane 0 only
-        const int st = k % C::NSTAGE;
-        const int id = page_id(k);
-        if (id < 0) {
-            report(a.status, VC_ERR_BAD_INDEX);
-            mbar_arrive(&bars[st]);
-            return;
+    int ids_cur = load_ids(0), ids_nxt = load_ids(1), cur_blk = 0;
+    auto issue = [&](int k) {  // every lane (k is warp-uniform); lane 0 issues the copies
+        if ((k >> 5) != cur_blk) {
+            ids_cur = ids_nxt;
+            ids_nxt = load_ids((k >> 5) + 1);
+            cur_blk = k >> 5;
         }
-        const int64_t off = ((int64_t)id * a.hkv + kvh) * C::HB;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&bars[st], 2 * C::HB);
-        bulk_g2s(ring + st * C::STAGE, a.kp + off, C::HB, &bars[st]);
-        bulk_g2s(ring + st * C::STAGE + C::HB, a.vp + off, C::HB, &bars[st]);
+        const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
+        if (lane == 0) {
+            const int st = k % C::NSTAGE;
+            sflag[st] = id >= 0;
+            if (id < 0) {
+                report(a.status, VC_ERR_BAD_INDEX);
+                mbar_arrive(&bars[st]);
+            } else {
+                const int64_t off = ((int64_t)id * a.hkv + kvh) * C::HB;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(&bars[st], 2 * C::HB);
+                bulk_g2s(ring + st * C::STAGE, a.kp + off, C::HB, &bars[st]);
+                bulk_g2s(ring + st * C::STAGE + C::HB, a.vp + off, C::HB, &bars[st]);
+            }
+        }
     };
 
     if (lane == 0) {
@@ -256,8 +291,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         fence_mbar_init();
     }
     __syncwarp();
-    if (lane == 0)
-        for (int k = 0; k < min(nw, C::NSTAGE); ++k) issue(k);
+    for (int k = 0; k < min(nw, C::NSTAGE); ++k) issue(k);
 
     // ---- the group's queries, staged once per CTA in shared memory ----
     uint16_t *qs = reinterpret_cast<uint16_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE) + C::BARS);
@@ -282,6 +316,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
 #pragma unroll
     for (int i = 0; i < C::NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+    static_assert(BITS == 16 || C::NG < 8, "the V zero-point MMA keeps one spare row for the P sums");
     const int src0 = t * 4 + (g >> 1), src1 = (t + 4) * 4 + (g >> 1);
     const bool odd_head = g & 1;
 
@@ -302,9 +337,9 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             const uint8_t *kb = ring + st * C::STAGE;
             uint8_t *vb = ring + st * C::STAGE + C::HB;
             const int pg = p0 + warp + NW * k;
-            if (page_id(k) < 0) {  // reported at issue time; nothing landed in this stage
+            if (!sflag[st]) {  // reported at issue time; nothing landed in this stage
                 __syncwarp();
-                if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+                if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
                 continue;
             }
             const int slot0 = 2 * g, slot1 = 2 * g + 1;
@@ -369,22 +404,33 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 mma_bf16(o[mt], af, b0, b1);
             }
             __syncwarp();
-            if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+            if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
         }
     } else {
         // ---- quantised cache ----
         // Q fragments: B of S^T = K Q^T, column n = head g, k-slot pair of
         // register r pre-scaled by 2^-kpos(r) so every product is c q 2^-24.
-        uint32_t bq[C::NT][2];
+        // The same for every warp: warp 0 packs them once into shared memory
+        // as [group][lane][k-step 2gr lo, hi, k-step 2gr+1 lo, hi].
+        uint32_t *qfrag = reinterpret_cast<uint32_t *>(qsum + 8 * C::NG);
+        if (warp == 0) {
 #pragma unroll
-        for (int ks = 0; ks < C::NT; ++ks) {
+            for (int ks = 0; ks < C::NT; ++ks) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c0 = 16 * ks + 4 * t + 2 * h;
-                const float f = __uint_as_float((uint32_t)(127 - kpos<BITS>(2 * ks + h)) << 23);
-                bq[ks][h] = pack_f16(bf16_bits_to_f32(qs[g * D + c0]) * f, bf16_bits_to_f32(qs[g * D + c0 + 1]) * f);
+                for (int h = 0; h < 2; ++h) {
+                    const int c0 = 16 * ks + 4 * t + 2 * h;
+                    const float f = __uint_as_float((uint32_t)(127 - kpos<BITS>(2 * ks + h)) << 23);
+                    qfrag[((ks >> 1) * 32 + lane) * 4 + 2 * (ks & 1) + h] =
+                        pack_f16(bf16_bits_to_f32(qs[g * D + c0]) * f, bf16_bits_to_f32(qs[g * D + c0 + 1]) * f);
+                }
             }
         }
+        __syncthreads();
         // Zero-point term of the scores as one more MMA: k-slots (2t, 2t+1)
         // carry groups (2P, 2P+1), P = t & 1, as the hi (t < 2) or lo (t >= 2)
         // f16 part of the pre-scaled query group sums.
@@ -401,8 +447,10 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             }
         }
         float oz[4] = {0.f, 0.f, 0.f, 0.f};  // V zero-point term, rows = groups, columns = heads
+        float ms0 = 0.0f, ms1 = 0.0f;         // running max as subtracted (0 while it is -inf)
+        bool fresh = true;                    // a head column has seen no score yet
         const float kscale = a.scale_log2 * 16777216.0f;  // products carry 2^-24
-        constexpr float kVhi = VStr<BITS, D>::VHI == 4 ? 0.0625f : 0.25f;
+        constexpr float kVhi = VReg<BITS, D>::VHI == 4 ? 0.0625f : 0.25f;
         const uint32_t vhi_scale = pack_f16(kVhi, kVhi);
 
         for (int k = 0; k < nw; ++k) {
@@ -411,14 +459,11 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             const uint8_t *kb = ring + st * C::STAGE;
             uint8_t *vb = ring + st * C::STAGE + C::HB;
             const int pg = p0 + warp + NW * k;
-            if (page_id(k) < 0) {
-                __syncwarp();
-                if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
-                continue;
-            }
-            const int nvalid = len - pg * kPage;  // slots >= nvalid are past the end
+            // slots >= nvalid are past the end; a bad page id (reported at
+            // issue time, nothing copied) masks the whole stage
+            const int nvalid = sflag[st] ? len - pg * kPage : 0;
 
-            // ---- S^T = K Q^T per group, scaled and summed ----
+            // ---- shared-memory reads of the page (K rows, V strings, parameters) ----
             KRow<BITS, D> r0, r1;  // tokens 2g (rows g) and 2g+1 (rows g+8)
             r0.load(kb + (2 * g) * (D * BITS / 8), t);
             r1.load(kb + (2 * g + 1) * (D * BITS / 8), t);
@@ -427,48 +472,45 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             float sc0[C::NG], sc1[C::NG];
             load_halves<C::NG>(ksc + (2 * g) * C::NG, sc0);
             load_halves<C::NG>(ksc + (2 * g + 1) * C::NG, sc1);
+            uint32_t kza0 = 0u, kza1 = 0u;
+            if (zuse) {
+                kza0 = *reinterpret_cast<const uint32_t *>(kzr + (2 * g) * C::NG + 2 * zp);
+                kza1 = *reinterpret_cast<const uint32_t *>(kzr + (2 * g + 1) * C::NG + 2 * zp);
+            }
+            // ---- S^T = K Q^T per group, scaled and summed ----
             f2 s01 = {0.f, 0.f}, s23 = {0.f, 0.f};
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint4 qb = *reinterpret_cast<const uint4 *>(qfrag + (gr * 32 + lane) * 4);
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int ks = 2 * gr + h2;
                     const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
-                    mma_f16(acc, af, bq[ks][0], bq[ks][1]);
+                    mma_f16(acc, af, h2 ? qb.z : qb.x, h2 ? qb.w : qb.y);
                 }
-                s01 = fma2(f2{sc0[gr], sc0[gr]}, f2{acc[0], acc[1]}, s01);
-                s23 = fma2(f2{sc1[gr], sc1[gr]}, f2{acc[2], acc[3]}, s23);
+                s01.x = fmaf(sc0[gr], acc[0], s01.x);
+                s01.y = fmaf(sc0[gr], acc[1], s01.y);
+                s23.x = fmaf(sc1[gr], acc[2], s23.x);
+                s23.y = fmaf(sc1[gr], acc[3], s23.y);
             }
-            float z[4] = {0.f, 0.f, 0.f, 0.f};
+            // zero-point term, accumulated onto minus the running max
+            float z[4] = {-ms0, -ms1, -ms0, -ms1};
             {
-                uint32_t za[4] = {0u, 0u, 0u, 0u};
-                if (zuse) {
-                    za[0] = *reinterpret_cast<const uint32_t *>(kzr + (2 * g) * C::NG + 2 * zp);
-                    za[1] = *reinterpret_cast<const uint32_t *>(kzr + (2 * g + 1) * C::NG + 2 * zp);
-                }
+                const uint32_t za[4] = {kza0, kza1, 0u, 0u};
                 mma_f16(z, za, bz, 0u);
             }
-            const float ms0 = m[0] == -INFINITY ? 0.0f : m[0], ms1 = m[1] == -INFINITY ? 0.0f : m[1];
-            const f2 zm01 = {z[0] - ms0, z[1] - ms1}, zm23 = {z[2] - ms0, z[3] - ms1};
-            const f2 x01 = fma2(s01, f2{kscale, kscale}, zm01), x23 = fma2(s23, f2{kscale, kscale}, zm23);
+            const f2 x01 = fma2(s01, f2{kscale, kscale}, f2{z[0], z[1]});
+            const f2 x23 = fma2(s23, f2{kscale, kscale}, f2{z[2], z[3]});
             float x[4] = {x01.x, x01.y, x23.x, x23.y};  // log2 score - running max
-            if (nvalid < kPage) {  // ragged last page: mask, and clear V parameters of empty slots
+            if (nvalid < kPage) {  // ragged last page: mask the scores of empty slots
                 if (2 * g >= nvalid) x[0] = x[1] = -INFINITY;
                 if (2 * g + 1 >= nvalid) x[2] = x[3] = -INFINITY;
-                uint16_t *vpar = reinterpret_cast<uint16_t *>(vb + C::CR);
-                for (int e = lane; e < (kPage - nvalid) * C::NG; e += 32) {
-                    const int tau = nvalid + e / C::NG, gr = e % C::NG;
-                    const int t2 = (tau >> 1) & 3, i2 = 2 * (tau >> 3) + (tau & 1);
-                    vpar[(t2 * C::NG + gr) * 4 + i2] = 0;
-                    vpar[kPage * C::NG + (t2 * C::NG + gr) * 4 + i2] = 0;
-                }
-                __syncwarp();
             }
 
             // ---- online softmax: rescale only when a score beats the running max ----
             const float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            if (__any_sync(0xffffffffu, mx > 0.0f || m[0] == -INFINITY || m[1] == -INFINITY)) {
+            if (__any_sync(0xffffffffu, mx > 0.0f || fresh)) {
                 float sv[4] = {x[0] + ms0, x[1] + ms1, x[2] + ms0, x[3] + ms1};
                 float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
 #pragma unroll
@@ -486,16 +528,49 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 }
                 oz[0] *= al0; oz[2] *= al0;
                 oz[1] *= al1; oz[3] *= al1;
-                l[0] *= al0;
-                l[1] *= al1;
                 m[0] = mn0;
                 m[1] = mn1;
-                const float n0 = mn0 == -INFINITY ? 0.0f : mn0, n1 = mn1 == -INFINITY ? 0.0f : mn1;
-                x[0] = sv[0] - n0; x[1] = sv[1] - n1; x[2] = sv[2] - n0; x[3] = sv[3] - n1;
+                fresh = mn0 == -INFINITY || mn1 == -INFINITY;
+                ms0 = mn0 == -INFINITY ? 0.0f : mn0;
+                ms1 = mn1 == -INFINITY ? 0.0f : mn1;
+                x[0] = sv[0] - ms0; x[1] = sv[1] - ms1; x[2] = sv[2] - ms0; x[3] = sv[3] - ms1;
             }
+            const uint8_t *vpar = vb + C::CR;
+            uint32_t vsc[2 * C::NG];  // per group: scales of tokens (2t, 2t+1), then (2t+8, 2t+9)
+            {
+                const uint32_t *pp = reinterpret_cast<const uint32_t *>(vpar + t * 8 * C::NG);
+#pragma unroll
+                for (int i = 0; i < 2 * C::NG; i += 4) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(pp + i);
+                    vsc[i] = u.x; vsc[i + 1] = u.y; vsc[i + 2] = u.z; vsc[i + 3] = u.w;
+                }
+            }
+            // A of the V zero-point MMA: rows 0..G-1 the group's zero points of
+            // tokens (2t, 2t+1) / (2t+8, 2t+9); row G ones, so the MMA also sums
+            // P over the page (the softmax denominator)
+            uint32_t vza0 = 0u, vza2 = 0u;
+            if (g < C::NG) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
+                vza0 = u.x;
+                vza2 = u.y;
+            } else if (g == C::NG) {
+                vza0 = vza2 = 0x3C003C00u;
+            }
+
+            if (nvalid < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
+                const uint32_t mlo = (2 * t < nvalid ? 0x0000FFFFu : 0u) | (2 * t + 1 < nvalid ? 0xFFFF0000u : 0u);
+                const uint32_t mhi = (2 * t + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t + 9 < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+                for (int gr = 0; gr < C::NG; ++gr) {
+                    vsc[2 * gr] &= mlo;
+                    vsc[2 * gr + 1] &= mhi;
+                }
+                vza0 &= mlo;
+                vza2 &= mhi;
+            }
+            VReg<BITS, D> vs;
+            vs.load(vb, g, t);
             const float p[4] = {ex2(x[0]), ex2(x[1]), ex2(x[2]), ex2(x[3])};
-            l[0] += p[0] + p[2];
-            l[1] += p[1] + p[3];
 
             // ---- P^T as the B operand: k-slot = token, column = head ----
             const uint32_t e = pack_f16(p[0], p[2]), od = pack_f16(p[1], p[3]);
@@ -505,18 +580,6 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             const uint32_t bhi_s = hmul2(bhi, vhi_scale);
 
             // ---- O^T += V^T (P s)^T, zero points as one more MMA ----
-            VStr<BITS, D> vs;
-            vs.load(vb, g, t);
-            const uint8_t *vpar = vb + C::CR;
-            uint32_t vsc[2 * C::NG];
-            {
-                const uint32_t *pp = reinterpret_cast<const uint32_t *>(vpar + t * 8 * C::NG);
-#pragma unroll
-                for (int i = 0; i < 2 * C::NG; i += 4) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(pp + i);
-                    vsc[i] = u.x; vsc[i + 1] = u.y; vsc[i + 2] = u.z; vsc[i + 3] = u.w;
-                }
-            }
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
                 const uint32_t b0 = hmul2(blo, vsc[2 * gr]), b1 = hmul2(bhi_s, vsc[2 * gr + 1]);
@@ -524,24 +587,21 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int mt = 2 * gr + h2;
                     uint32_t af[4];
-                    vs.regs(2 * mt, t, af[0], af[2]);
-                    vs.regs(2 * mt + 1, t, af[1], af[3]);
+                    vs.regs(mt, af);
                     mma_f16(o[mt], af, b0, b1);
                 }
             }
             {
-                uint32_t za[4] = {0u, 0u, 0u, 0u};
-                if (g < C::NG) {
-                    const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
-                    za[0] = u.x;
-                    za[2] = u.y;
-                }
+                const uint32_t za[4] = {vza0, 0u, vza2, 0u};
                 mma_f16(oz, za, blo, bhi);
             }
             __syncwarp();
-            if (lane == 0 && k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+            if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
         }
-        // ---- finish O^T: 2^24 * codes part + zero-point part of the channel's group ----
+        l[0] = __shfl_sync(0xffffffffu, oz[0], C::NG * 4 + t);
+        l[1] = __shfl_sync(0xffffffffu, oz[1], C::NG * 4 + t);
+        // ---- finish O^T: codes part (2^24, rows g+8 2^(24 - ROW8)) + zero-point part of the group ----
+        constexpr float kRow8 = VReg<BITS, D>::ROW8 == 4 ? 1048576.0f : 16777216.0f;
 #pragma unroll
         for (int gr = 0; gr < C::NG; ++gr) {
             const float z0 = __shfl_sync(0xffffffffu, oz[0], gr * 4 + t);
@@ -550,19 +610,13 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int mt = 2 * gr + h2;
                 o[mt][0] = fmaf(o[mt][0], 16777216.0f, z0);
-                o[mt][2] = fmaf(o[mt][2], 16777216.0f, z0);
                 o[mt][1] = fmaf(o[mt][1], 16777216.0f, z1);
-                o[mt][3] = fmaf(o[mt][3], 16777216.0f, z1);
+                o[mt][2] = fmaf(o[mt][2], kRow8, z0);
+                o[mt][3] = fmaf(o[mt][3], kRow8, z1);
             }
         }
     }
 
-    // ---- warp epilogue: finish l ----
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-    }
     // ---- combine the warps of the CTA in shared memory ----
     __syncthreads();  // every warp is done with its ring
     float *cm = reinterpret_cast<float *>(smem);   // [warp][8] m

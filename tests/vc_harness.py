@@ -76,13 +76,17 @@ def k_bit(bits: int, d: int, s, c, plane: int = 0):
 
 def v_bit(bits: int, d: int, tau, c, plane: int = 0):
     tau, c = np.asarray(tau), np.asarray(c)
-    lam = (c & 7) * (d // 8) + 2 * (c >> 4) + ((c >> 3) & 1)
-    t, h, half = (tau >> 1) & 3, tau >> 3, tau & 1
-    if bits == 2 or (bits == 3 and plane == 0):
-        return 32 * lam + 16 * half + 4 * t + 2 * h
+    g, row8, mt = c & 7, (c >> 3) & 1, c >> 4
+    t, hi, half = (tau >> 1) & 3, tau >> 3, tau & 1
+    region = g * 4 + t
     if bits == 4:
-        return 32 * (d * (t >> 1) + lam) + 16 * half + 8 * (t & 1) + 4 * h
-    return 32 * d + 16 * lam + 8 * half + np.array([0, 1, 4, 5])[t] + 2 * h
+        return 32 * (region * (d // 16) + mt) + 16 * half + 8 * row8 + 4 * hi
+    u, m = mt >> 1, mt & 1
+    if bits == 2 or plane == 0:
+        return 32 * (region * (d // 32) + u) + 16 * half + 8 * m + 4 * row8 + 2 * hi
+    j = 2 * row8 + hi
+    beta = 2 * j + np.array([0, 1, 8, 9])[2 * (u & 1) + m]
+    return 32 * d + 32 * (region * (d // 64) + (u >> 1)) + 16 * half + beta
 
 
 def v_param(g: int, tau, gr):
