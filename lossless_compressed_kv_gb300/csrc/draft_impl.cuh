@@ -448,14 +448,16 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         }
         float oz[4] = {0.f, 0.f, 0.f, 0.f};  // V zero-point term, rows = groups, columns = heads
         float ms0 = 0.0f, ms1 = 0.0f;         // running max as subtracted (0 while it is -inf)
+        float nm[4] = {0.f, 0.f, 0.f, 0.f};   // minus the running max, per accumulator column
         bool fresh = true;                    // a head column has seen no score yet
         const float kscale = a.scale_log2 * 16777216.0f;  // products carry 2^-24
         constexpr float kVhi = VReg<BITS, D>::VHI == 4 ? 0.0625f : 0.25f;
         const uint32_t vhi_scale = pack_f16(kVhi, kVhi);
 
-        for (int k = 0; k < nw; ++k) {
-            const int st = k % C::NSTAGE;
-            if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status)) break;
+        // One page: k = page index of the warp, st = its ring stage (a
+        // compile-time constant in the unrolled driver below).
+        auto page = [&](int k, int st, uint32_t parity) -> bool {
+            if (!mbar_wait(&bars[st], parity, a.status)) return false;
             const uint8_t *kb = ring + st * C::STAGE;
             uint8_t *vb = ring + st * C::STAGE + C::HB;
             const int pg = p0 + warp + NW * k;
@@ -464,30 +466,34 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             const int nvalid = sflag[st] ? len - pg * kPage : 0;
 
             // ---- shared-memory reads of the page (K rows, V strings, parameters) ----
-            KRow<BITS, D> r0, r1;  // tokens 2g (rows g) and 2g+1 (rows g+8)
-            r0.load(kb + (2 * g) * (D * BITS / 8), t);
-            r1.load(kb + (2 * g + 1) * (D * BITS / 8), t);
+            KRow<BITS, D> r0, r1;  // tokens g (rows g) and g+8 (rows g+8)
+            r0.load(kb + g * (D * BITS / 8), t);
+            r1.load(kb + (g + 8) * (D * BITS / 8), t);
             const __half *ksc = reinterpret_cast<const __half *>(kb + C::CR);
             const __half *kzr = ksc + kPage * C::NG;
             float sc0[C::NG], sc1[C::NG];
-            load_halves<C::NG>(ksc + (2 * g) * C::NG, sc0);
-            load_halves<C::NG>(ksc + (2 * g + 1) * C::NG, sc1);
+            load_halves<C::NG>(ksc + g * C::NG, sc0);
+            load_halves<C::NG>(ksc + (g + 8) * C::NG, sc1);
             uint32_t kza0 = 0u, kza1 = 0u;
             if (zuse) {
-                kza0 = *reinterpret_cast<const uint32_t *>(kzr + (2 * g) * C::NG + 2 * zp);
-                kza1 = *reinterpret_cast<const uint32_t *>(kzr + (2 * g + 1) * C::NG + 2 * zp);
+                kza0 = *reinterpret_cast<const uint32_t *>(kzr + g * C::NG + 2 * zp);
+                kza1 = *reinterpret_cast<const uint32_t *>(kzr + (g + 8) * C::NG + 2 * zp);
             }
             // ---- S^T = K Q^T per group, scaled and summed ----
             f2 s01 = {0.f, 0.f}, s23 = {0.f, 0.f};
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[4];
                 const uint4 qb = *reinterpret_cast<const uint4 *>(qfrag + (gr * 32 + lane) * 4);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int ks = 2 * gr + h2;
+                {
+                    const int ks = 2 * gr;
                     const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
-                    mma_f16(acc, af, h2 ? qb.z : qb.x, h2 ? qb.w : qb.y);
+                    mma_f16_z(acc, af, qb.x, qb.y);
+                }
+                {
+                    const int ks = 2 * gr + 1;
+                    const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
+                    mma_f16(acc, af, qb.z, qb.w);
                 }
                 s01.x = fmaf(sc0[gr], acc[0], s01.x);
                 s01.y = fmaf(sc0[gr], acc[1], s01.y);
@@ -495,17 +501,17 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 s23.y = fmaf(sc1[gr], acc[3], s23.y);
             }
             // zero-point term, accumulated onto minus the running max
-            float z[4] = {-ms0, -ms1, -ms0, -ms1};
+            float z[4];
             {
                 const uint32_t za[4] = {kza0, kza1, 0u, 0u};
-                mma_f16(z, za, bz, 0u);
+                mma_f16_c(z, za, bz, 0u, nm);
             }
             const f2 x01 = fma2(s01, f2{kscale, kscale}, f2{z[0], z[1]});
             const f2 x23 = fma2(s23, f2{kscale, kscale}, f2{z[2], z[3]});
             float x[4] = {x01.x, x01.y, x23.x, x23.y};  // log2 score - running max
             if (nvalid < kPage) {  // ragged last page: mask the scores of empty slots
-                if (2 * g >= nvalid) x[0] = x[1] = -INFINITY;
-                if (2 * g + 1 >= nvalid) x[2] = x[3] = -INFINITY;
+                if (g >= nvalid) x[0] = x[1] = -INFINITY;
+                if (g + 8 >= nvalid) x[2] = x[3] = -INFINITY;
             }
 
             // ---- online softmax: rescale only when a score beats the running max ----
@@ -533,6 +539,8 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 fresh = mn0 == -INFINITY || mn1 == -INFINITY;
                 ms0 = mn0 == -INFINITY ? 0.0f : mn0;
                 ms1 = mn1 == -INFINITY ? 0.0f : mn1;
+                nm[0] = nm[2] = -ms0;
+                nm[1] = nm[3] = -ms1;
                 x[0] = sv[0] - ms0; x[1] = sv[1] - ms1; x[2] = sv[2] - ms0; x[3] = sv[3] - ms1;
             }
             const uint8_t *vpar = vb + C::CR;
@@ -572,11 +580,10 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             vs.load(vb, g, t);
             const float p[4] = {ex2(x[0]), ex2(x[1]), ex2(x[2]), ex2(x[3])};
 
-            // ---- P^T as the B operand: k-slot = token, column = head ----
-            const uint32_t e = pack_f16(p[0], p[2]), od = pack_f16(p[1], p[3]);
-            const uint32_t e0 = __shfl_sync(0xffffffffu, e, src0), o0 = __shfl_sync(0xffffffffu, od, src0);
-            const uint32_t e1 = __shfl_sync(0xffffffffu, e, src1), o1 = __shfl_sync(0xffffffffu, od, src1);
-            const uint32_t blo = odd_head ? o0 : e0, bhi = odd_head ? o1 : e1;
+            // ---- P^T as the B operand (k-slot = token, column = head): the
+            // score fragment rows 0-7 / 8-15 (tokens 0-7 / 8-15) transposed ----
+            const uint32_t blo = movmatrix_t(pack_f16(p[0], p[1]));
+            const uint32_t bhi = movmatrix_t(pack_f16(p[2], p[3]));
             const uint32_t bhi_s = hmul2(bhi, vhi_scale);
 
             // ---- O^T += V^T (P s)^T, zero points as one more MMA ----
@@ -597,6 +604,17 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             }
             __syncwarp();
             if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+            return true;
+        };
+        // driver: stages in order, the ring index known at compile time
+        for (int k0 = 0; k0 < nw; k0 += C::NSTAGE) {
+            const uint32_t parity = (uint32_t)(k0 / C::NSTAGE) & 1u;
+            bool ok = true;
+#pragma unroll
+            for (int j = 0; j < C::NSTAGE; ++j) {
+                if (k0 + j < nw && ok) ok = page(k0 + j, j, parity);
+            }
+            if (!ok) break;
         }
         l[0] = __shfl_sync(0xffffffffu, oz[0], C::NG * 4 + t);
         l[1] = __shfl_sync(0xffffffffu, oz[1], C::NG * 4 + t);
