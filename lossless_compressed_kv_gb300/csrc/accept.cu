@@ -6,33 +6,39 @@
 // emitted (the rest of the draft is discarded); when every draft matches
 // the draft is emitted together with the verifier's extra (bonus) token.
 //
-// Kernel 1: logits of a tile of prediction rows x a tile of the vocabulary,
-// one column per thread, fp32 with one fused multiply-add per term in
-// increasing k (so a row's logits are the same bits whatever the batch or
-// the number of rows), then the tile's argmax (ties -> lowest id).
-// Kernel 2: per request, argmax over the vocabulary tiles and the prefix
-// rule.
+// Kernel 1 (prepass): the mean of each row's hidden group, and the row's
+// argmax key reset.  Kernel 2: logits of 16 prediction rows x 512
+// vocabulary columns per CTA (a 16 x 4 register tile per thread, the row
+// values of one hidden dimension read as four 16-byte shared loads), each
+// logit fp32 with one fused multiply-add per term in increasing k (so a
+// row's logits are the same bits whatever the batch or the number of rows);
+// the tile's best column per row goes into the row's 64-bit key with
+// atomicMax (larger value wins, lower id on ties).  Kernel 3: per request,
+// the prefix rule.
 #include "vc_internal.cuh"
 
 namespace vc {
 namespace {
 
-constexpr int kCols = 256;  // vocabulary columns per CTA (one per thread)
-constexpr int kRowsT = 16;  // prediction rows per CTA
-constexpr int kKT = 64;     // hidden dims staged per step
+constexpr int kThreadsL = 128;        // logits CTA
+constexpr int kColsT = 4;             // vocabulary columns per thread
+constexpr int kCols = kThreadsL * kColsT;
+constexpr int kRowsT = 16;            // prediction rows per CTA
+constexpr int kKT = 128;              // hidden dims staged per step
 
-struct Best {
-    float v;
-    int i;
-};
-__device__ inline Best better(Best a, Best b) {  // larger value, lower id on ties
-    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
-    return a;
+// Order-preserving key: value bits mapped to an unsigned order in the high
+// word (-0 folded onto +0 first), the complement of the id in the low word.
+__device__ inline unsigned long long argmax_key(float v, int id) {
+    uint32_t b = __float_as_uint(v + 0.0f);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)b << 32) | (uint32_t)(~(uint32_t)id);
 }
 
 // h[r][k] = (sum_j hidden[r][j][k], in increasing j) / hg, once per row.
-__global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, float *h) {
+__global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, float *h,
+                                  unsigned long long *keys) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < rows) keys[i] = 0ull;
     if (i >= (int64_t)rows * d) return;
     const int64_t r = i / d, k = i % d;
     const float *hp = hidden + (r * hg) * d + k;
@@ -41,66 +47,83 @@ __global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, 
     h[i] = __fdiv_rn(s, (float)hg);
 }
 
-__global__ void __launch_bounds__(kCols) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
-                                                             int vocab, float *part_v, int *part_i, int ntiles) {
-    __shared__ float hs[kRowsT][kKT];
-    __shared__ Best red[kRowsT][kCols / 32];
-    const int vt = blockIdx.x, r0 = blockIdx.y * kRowsT;
-    const int v = vt * kCols + threadIdx.x;
-    const bool vok = v < vocab;
-    float acc[kRowsT];
+__global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
+                                                                 int vocab, unsigned long long *keys) {
+    __shared__ __align__(16) float hs[kKT][kRowsT];  // k-major: one k's 16 row values contiguous
+    const int r0 = blockIdx.y * kRowsT;
+    const int v0 = blockIdx.x * kCols + threadIdx.x * kColsT;
+    const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
+    float acc[kRowsT][kColsT];
 #pragma unroll
-    for (int r = 0; r < kRowsT; ++r) acc[r] = 0.0f;
+    for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+        for (int c = 0; c < kColsT; ++c) acc[r][c] = 0.0f;
     for (int k0 = 0; k0 < d; k0 += kKT) {
+        const int kn = min(kKT, d - k0);
         __syncthreads();
-        for (int e = threadIdx.x; e < kRowsT * kKT; e += kCols) {
-            const int r = e / kKT, k = k0 + e % kKT;
-            hs[r][e % kKT] = (r0 + r < rows && k < d) ? h[(int64_t)(r0 + r) * d + k] : 0.0f;
+        for (int e = threadIdx.x; e < kRowsT * kKT; e += kThreadsL) {
+            const int r = e / kKT, k = e % kKT;
+            hs[k][r] = (r0 + r < rows && k < kn) ? h[(int64_t)(r0 + r) * d + k0 + k] : 0.0f;
         }
         __syncthreads();
-        if (vok) {
-            const int kn = min(kKT, d - k0);
-            for (int kk = 0; kk < kn; ++kk) {
-                const float wv = w[(int64_t)(k0 + kk) * vocab + v];
+        // four hidden dims per step: the W loads of all four issued first
+        for (int kk = 0; kk < kn; kk += 4) {
+            float wv[4][kColsT];
 #pragma unroll
-                for (int r = 0; r < kRowsT; ++r) acc[r] = __fmaf_rn(hs[r][kk], wv, acc[r]);
+            for (int u = 0; u < 4; ++u) {
+                const float *wp = w + (int64_t)(k0 + kk + u) * vocab + v0;
+                if (kk + u < kn && vec && v0 + kColsT <= vocab) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(wp);
+                    wv[u][0] = q4.x; wv[u][1] = q4.y; wv[u][2] = q4.z; wv[u][3] = q4.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kColsT; ++c) wv[u][c] = (kk + u < kn && v0 + c < vocab) ? wp[c] : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (kk + u >= kn) break;
+                float hv[kRowsT];
+#pragma unroll
+                for (int i = 0; i < kRowsT / 4; ++i) {
+                    const float4 q4 = reinterpret_cast<const float4 *>(hs[kk + u])[i];
+                    hv[4 * i] = q4.x; hv[4 * i + 1] = q4.y; hv[4 * i + 2] = q4.z; hv[4 * i + 3] = q4.w;
+                }
+#pragma unroll
+                for (int r = 0; r < kRowsT; ++r)
+#pragma unroll
+                    for (int c = 0; c < kColsT; ++c) acc[r][c] = __fmaf_rn(hv[r], wv[u][c], acc[r][c]);
             }
         }
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int r = 0; r < kRowsT; ++r) {
-        Best bb = {vok ? acc[r] : -INFINITY, vok ? v : 0x7fffffff};
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int c = 0; c < kColsT; ++c)
+            if (v0 + c < vocab) {
+                const unsigned long long kc = argmax_key(acc[r][c], v0 + c);
+                best = kc > best ? kc : best;
+            }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            Best o;
-            o.v = __shfl_xor_sync(0xffffffffu, bb.v, off);
-            o.i = __shfl_xor_sync(0xffffffffu, bb.i, off);
-            bb = better(bb, o);
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
         }
-        if (lane == 0) red[r][warp] = bb;
-    }
-    __syncthreads();
-    if (threadIdx.x < kRowsT && r0 + threadIdx.x < rows) {
-        Best bb = red[threadIdx.x][0];
-        for (int w2 = 1; w2 < kCols / 32; ++w2) bb = better(bb, red[threadIdx.x][w2]);
-        const int64_t o = (int64_t)(r0 + threadIdx.x) * ntiles + vt;
-        part_v[o] = bb.v;
-        part_i[o] = bb.i;
+        if (lane == 0 && r0 + r < rows && best) atomicMax(&keys[r0 + r], best);
     }
 }
 
-__global__ void accept_finalize_kernel(const float *part_v, const int *part_i, int ntiles, int n_pred,
-                                       const int32_t *drafts, int x, int32_t *verified,
-                                       int32_t *accept_len, int32_t *emitted) {
+__global__ void accept_finalize_kernel(const unsigned long long *keys, int n_pred, const int32_t *drafts, int x,
+                                       int32_t *verified, int32_t *accept_len, int32_t *emitted) {
     extern __shared__ int32_t ver[];  // [n_pred]
     const int b = blockIdx.x;
     for (int i = threadIdx.x; i < n_pred; i += blockDim.x) {
         const int64_t r = (int64_t)b * n_pred + i;
-        Best bb = {part_v[r * ntiles], part_i[r * ntiles]};
-        for (int tt = 1; tt < ntiles; ++tt) bb = better(bb, Best{part_v[r * ntiles + tt], part_i[r * ntiles + tt]});
-        ver[i] = bb.i;
-        verified[r] = bb.i;
+        const int32_t id = (int32_t)~(uint32_t)(keys[r] & 0xffffffffull);
+        ver[i] = id;
+        verified[r] = id;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -119,26 +142,25 @@ __global__ void accept_finalize_kernel(const float *part_v, const int *part_i, i
 }  // namespace
 
 size_t accept_workspace(int batch, int n_pred, int vocab, int d) {
-    const int ntiles = ceil_div(vocab, kCols);
-    return (size_t)batch * n_pred * ntiles * (sizeof(float) + sizeof(int)) + (size_t)batch * n_pred * d * sizeof(float);
+    (void)vocab;
+    const size_t rows = (size_t)batch * n_pred;
+    return rows * sizeof(unsigned long long) + rows * d * sizeof(float);
 }
 
 cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, const float *w, int d,
                           int vocab, const int32_t *drafts, int x, int32_t *verified, int32_t *accept_len,
                           int32_t *emitted, void *ws, cudaStream_t st) {
-    const int ntiles = ceil_div(vocab, kCols);
     const int rows = batch * n_pred;
-    float *pv = (float *)ws;
-    int *pi = (int *)(pv + (size_t)rows * ntiles);
-    float *h = reinterpret_cast<float *>(pi + (size_t)rows * ntiles);
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(ws);
+    float *h = reinterpret_cast<float *>(keys + rows);
     const int64_t nh = (int64_t)rows * d;
-    group_mean_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hidden, rows, hg, d, h);
-    dim3 grid(ntiles, ceil_div(rows, kRowsT));
-    logits_argmax_kernel<<<grid, kCols, 0, st>>>(h, rows, w, d, vocab, pv, pi, ntiles);
+    group_mean_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hidden, rows, hg, d, h, keys);
+    dim3 grid(ceil_div(vocab, kCols), ceil_div(rows, kRowsT));
+    logits_argmax_kernel<<<grid, kThreadsL, 0, st>>>(h, rows, w, d, vocab, keys);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    accept_finalize_kernel<<<batch, 128, n_pred * sizeof(int32_t), st>>>(pv, pi, ntiles, n_pred, drafts, x,
-                                                                         verified, accept_len, emitted);
+    accept_finalize_kernel<<<batch, 128, n_pred * sizeof(int32_t), st>>>(keys, n_pred, drafts, x, verified,
+                                                                         accept_len, emitted);
     return cudaGetLastError();
 }
 

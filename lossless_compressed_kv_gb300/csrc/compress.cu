@@ -107,6 +107,8 @@ __device__ inline void put_bits(uint32_t *blk, int off, int width, uint32_t v) {
 }
 
 constexpr int kPageWarps = 8;
+// Up to this many entries per request the token-parallel path is used.
+constexpr int kTokenPathMax = 32;
 
 template <int BITS, int D>
 __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(CompressArgs a) {
@@ -133,29 +135,41 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
     }
     uint8_t *gk = a.ck + ((int64_t)cp * a.hkv + h) * HB;
     uint8_t *gv = a.cv + ((int64_t)cp * a.hkv + h) * HB;
+    const int fhb = head_block_bytes(16, D);
+    // Each warp's first slot: kept index -> page -> bf16 rows, started before
+    // the old blocks are copied so the two chains of dependent loads overlap.
+    int s = s_lo + warp;
+    uint16_t xk[CPL], xv[CPL];
+    int fp = -1;
+    auto fetch = [&](int slot_pos) {
+        const int t = a.idx[o0 + (slot_pos - start)];
+        fp = (t >= 0 && t < a.f_lens[b] && t / kPage < a.f_maxb) ? a.f_table[(int64_t)b * a.f_maxb + t / kPage] : -1;
+        if (fp >= 0 && fp < a.f_pages) {
+            const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
+            load_lane_row<D>(a.fk + fbase, lane, xk);
+            load_lane_row<D>(a.fv + fbase, lane, xv);
+        } else {
+            fp = -1;
+        }
+    };
+    if (s < s_hi) fetch(s);
     for (int i = threadIdx.x; i < HB / 16; i += blockDim.x) {
         reinterpret_cast<uint4 *>(blk[0])[i] = reinterpret_cast<const uint4 *>(gk)[i];
         reinterpret_cast<uint4 *>(blk[1])[i] = reinterpret_cast<const uint4 *>(gv)[i];
     }
     __syncthreads();
-    const int fhb = head_block_bytes(16, D);
-    for (int s = s_lo + warp; s < s_hi; s += kPageWarps) {
-        const int t = a.idx[o0 + (s - start)];
-        const int fp = (t >= 0 && t < a.f_lens[b] && t / kPage < a.f_maxb)
-                           ? a.f_table[(int64_t)b * a.f_maxb + t / kPage] : -1;
-        if (fp < 0 || fp >= a.f_pages) {  // bad kept index: the slot keeps its bytes
+    for (; s < s_hi; s += kPageWarps) {
+        if (s != s_lo + warp) fetch(s);
+        if (fp < 0) {  // bad kept index: the slot keeps its bytes
             if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
             continue;
         }
         const int slot = s % kPage;
-        const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
-            uint16_t x[CPL];
-            load_lane_row<D>((kv ? a.fv : a.fk) + fbase, lane, x);
             uint8_t code[CPL];
             uint16_t sh, zh;
-            quantize_row<BITS, D>(x, code, sh, zh);
+            quantize_row<BITS, D>(kv ? xv : xk, code, sh, zh);
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
                 const int ch = lane * CPL + i;
@@ -182,6 +196,87 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
         reinterpret_cast<uint4 *>(gk)[i] = reinterpret_cast<const uint4 *>(blk[0])[i];
         reinterpret_cast<uint4 *>(gv)[i] = reinterpret_cast<const uint4 *>(blk[1])[i];
     }
+}
+
+// Small appends (a few entries per request, e.g. one drafted token per draft
+// step): one warp per (kept entry, kv head).  The token's K row and fp16
+// parameters belong to it alone and are stored directly; its V codes share
+// 32-bit words with the other tokens of the page and are merged with global
+// AND / OR reductions (one thread per word, in program order).
+template <int BITS, int D>
+__global__ void __launch_bounds__(kWarps * 32) compress_token_kernel(CompressArgs a) {
+    constexpr int CPL = D / 32, LPG = kGroup / CPL, G = D / kGroup;
+    constexpr int HB = 2 * D * (BITS + 1), CR = kPage * D * BITS / 8, RW = D * BITS / 32;  // K row words
+    __shared__ uint32_t krow[kWarps][RW];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int item = blockIdx.x * kWarps + warp;  // (entry, head) pair
+    const int j = item / a.hkv, h = item % a.hkv;
+    const int o0 = a.offs[b], o1 = a.offs[b + 1];
+    if (o0 + j >= o1) return;
+    const int t = a.idx[o0 + j];
+    const int slot_pos = (a.start ? a.start[b] : 0) + j;
+    if (t < 0 || t >= a.f_lens[b] || t / kPage >= a.f_maxb || slot_pos < 0 || slot_pos / kPage >= a.c_maxb) {
+        if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    const int fp = a.f_table[(int64_t)b * a.f_maxb + t / kPage];
+    const int cp = a.c_table[(int64_t)b * a.c_maxb + slot_pos / kPage];
+    if (fp < 0 || fp >= a.f_pages || cp < 0 || cp >= a.c_pages) {
+        if (lane == 0) report(a.status, VC_ERR_BAD_INDEX);
+        return;
+    }
+    const int fhb = head_block_bytes(16, D);
+    const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
+    uint8_t *gk = a.ck + ((int64_t)cp * a.hkv + h) * HB;
+    uint8_t *gv = a.cv + ((int64_t)cp * a.hkv + h) * HB;
+    const int slot = slot_pos % kPage;
+    uint16_t xk[CPL], xv[CPL];
+    load_lane_row<D>(a.fk + fbase, lane, xk);
+    load_lane_row<D>(a.fv + fbase, lane, xv);
+    for (int i = lane; i < RW; i += 32) krow[warp][i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+        uint8_t code[CPL];
+        uint16_t sh, zh;
+        quantize_row<BITS, D>(kv ? xv : xk, code, sh, zh);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int ch = lane * CPL + i;
+            if (kv == 0) {  // K: the token's own row, built in shared memory
+#pragma unroll
+                for (int pl = 0; pl < (BITS == 3 ? 2 : 1); ++pl) {
+                    const int w = BITS == 3 ? (pl ? 1 : 2) : BITS;
+                    const uint32_t v = BITS == 3 ? (pl ? code[i] >> 2 : code[i] & 3u) : code[i];
+                    const int o = layout::k_bit(BITS, D, slot, ch, pl) - slot * D * BITS;
+                    atomicOr(&krow[warp][o >> 5], v << (o & 31));
+                    (void)w;
+                }
+            } else {  // V: words shared with the page's other tokens
+#pragma unroll
+                for (int pl = 0; pl < (BITS == 3 ? 2 : 1); ++pl) {
+                    const int w = BITS == 3 ? (pl ? 1 : 2) : BITS;
+                    const uint32_t v = BITS == 3 ? (pl ? code[i] >> 2 : code[i] & 3u) : code[i];
+                    const int o = layout::v_bit(BITS, D, slot, ch, pl);
+                    const uint32_t m = ((1u << w) - 1u) << (o & 31);
+                    uint32_t *word = reinterpret_cast<uint32_t *>(gv) + (o >> 5);
+                    atomicAnd(word, ~m);
+                    atomicOr(word, (v << (o & 31)) & m);
+                }
+            }
+        }
+        if (lane % LPG == 0) {
+            const int gr = lane / LPG;
+            const int e = kv ? layout::v_param(G, slot, gr) : slot * G + gr;
+            uint16_t *par = reinterpret_cast<uint16_t *>((kv ? gv : gk) + CR);
+            par[e] = sh;
+            par[kPage * G + e] = zh;
+        }
+    }
+    __syncwarp();
+    uint32_t *kd = reinterpret_cast<uint32_t *>(gk + slot * (D * BITS / 8));
+    for (int i = lane; i < RW; i += 32) kd[i] = krow[warp][i];
 }
 
 // bf16 token drop: one warp per (kept entry, kv head) copies the row.
@@ -225,6 +320,9 @@ cudaError_t launch_bd(const CompressArgs &a, int batch, int max_kept, cudaStream
     if constexpr (BITS == 16) {
         dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
         compress_bf16_kernel<D><<<grid, kWarps * 32, 0, st>>>(a);
+    } else if (max_kept <= kTokenPathMax) {
+        dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
+        compress_token_kernel<BITS, D><<<grid, kWarps * 32, 0, st>>>(a);
     } else {
         // a range of max_kept slots starting anywhere touches at most this many pages
         dim3 grid(ceil_div(max_kept, kPage) + 1, a.hkv, batch);

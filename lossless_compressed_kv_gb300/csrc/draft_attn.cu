@@ -33,10 +33,12 @@ using draft::Cfg;
 using draft::DraftArgs;
 constexpr int kWarps = 4;
 
-// Resident CTAs per SM the register budget is cut for: five where the body
-// fits 102 registers without spilling (measured with -Xptxas -v), else four.
+// Resident CTAs per SM the register budget is cut for.  Four (128
+// registers): a five-CTA cap (102 registers) fits the 2-bit body but the
+// extra register pressure costs more instructions than the extra warps hide
+// (measured: 73.4 vs 68.8 us on the 8B-shaped 32k 2-bit workload).
 template <int BITS, int D>
-constexpr int kMinCtas = (D == 128 && (BITS == 3 || BITS == 4)) ? 4 : 4;
+constexpr int kMinCtas = 4;
 
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(DraftArgs a) {

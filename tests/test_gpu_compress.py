@@ -52,12 +52,12 @@ def test_compress_random_shapes(bits, d):
     check(comp, ctable, hf, kept, bits)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
-def test_compress_append_offsets(bits):
+@pytest.mark.parametrize("bits,d", [(2, 128), (3, 128), (4, 128), (2, 64), (3, 64), (4, 64)])
+def test_compress_append_offsets(bits, d):
     """Append mode: entries go to slots comp_start[b] + j (drafted tokens
     appended to an existing KV_comp); slots before comp_start are untouched."""
     rng = np.random.default_rng(7)
-    lens, d, hkv = [70, 33], 128, 3
+    lens, hkv = [70, 33], 3
     full, hf = H.full_cache(rng, lens, hkv, d)
     comp, ctable = H.comp_cache(rng, 2, 100, hkv, d, bits, zero=True)
     kept = [np.arange(60, 70, dtype=np.int32), np.arange(30, 33, dtype=np.int32)]
@@ -66,6 +66,26 @@ def test_compress_append_offsets(bits):
     check(comp, ctable, hf, kept, bits, start=start)
     before = H.read_comp(comp.k_pages, ctable[0], 23, hkv, d, bits, "k")
     assert not before["packed"].any() and not before["scales"].any()
+    vbefore = H.read_comp(comp.v_pages, ctable[0], 23, hkv, d, bits, "v")
+    assert not vbefore["packed"].any() and not vbefore["zeros"].any()
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_compress_one_token_appends_match_bulk(bits):
+    """Appending one token per call (the draft loop's path) builds the same
+    bytes as compressing the whole range at once (the page-parallel path)."""
+    rng = np.random.default_rng(11)
+    lens, d, hkv = [45, 40], 128, 2
+    full, hf = H.full_cache(rng, lens, hkv, d)
+    kept = [np.arange(40, dtype=np.int32), np.arange(40, dtype=np.int32)]
+    c1, t1 = H.comp_cache(rng, 2, 48, hkv, d, bits, zero=True)
+    assert run_compress(full, c1, kept) == 0
+    c2, _ = H.comp_cache(rng, 2, 48, hkv, d, bits, zero=True)
+    import lossless_compressed_kv_gb300 as vc
+    c2 = vc.PagedKV(c2.k_pages, c2.v_pages, c1.block_table, c2.seq_lens, hkv, d, bits)
+    for i in range(40):
+        assert run_compress(full, c2, [np.array([i], np.int32)] * 2, comp_start=[i, i]) == 0
+    assert torch.equal(c1.k_pages, c2.k_pages) and torch.equal(c1.v_pages, c2.v_pages)
 
 
 def test_compress_bad_indices_are_reported_and_skipped():
