@@ -285,7 +285,7 @@ def draft_bytes(w, n_entries):
 # CPU oracle leg
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, st, seconds_target=12.0, max_requests=64):
+def oracle_sample(w, st, seconds_target=15.0, max_requests=128):
     """Time the oracle's draft attention on whole requests of the same
     workload (KV_comp built by the oracle's own compress from the same
     KV_full) until about `seconds_target` of CPU work."""
