@@ -14,7 +14,7 @@ using vtc::Args;
 namespace {
 
 template <int D, int QT>
-__global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS) verify_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS, vtc::Cfg<D, QT>::MIN_CTAS) verify_kernel(const __grid_constant__ Args a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     vtc::verify_tc_block<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }

@@ -7,17 +7,21 @@
 // two 128-row MMA tiles), so every K/V byte feeds n_q * G rows.
 //
 // Roles (one CTA = one (request, kv head, 4096-key split, row block)):
-//  - producer warp: one thread streams 64-key blocks (4 pages) of K and V
-//    into a 3-stage shared-memory ring with TMA tensor copies (one 16-row x
+//  - producer warp: one thread streams 32-key blocks (2 pages) of K and V
+//    into a 4-stage shared-memory ring with TMA tensor copies (one 16-row x
 //    64-channel box per page and 128-byte column chunk); the TMA unit writes
 //    the 128-byte-swizzled layout the tensor core reads.  Full / empty
 //    mbarriers per stage (transaction bytes / MMA completion).
-//  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 64,
-//    K 16 steps) into TMEM, then O += P V (M 128, N = D, V read MN-major).
+//  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 32,
+//    K 16 steps) into TMEM, then O += P V (M 128, N = D) with P read from
+//    TMEM as the A operand and V from shared memory (MN-major).
 //  - 4 softmax warps per 128-row tile: each thread owns one row = one TMEM
-//    lane; it loads the row's 64 scores from TMEM, masks, keeps a running max
-//    (rescaling O in TMEM only when the max grows by more than 2^8), writes
-//    P (bf16) as the next MMA's A operand, and finally reads O from TMEM.
+//    lane; it loads the row's 32 scores from TMEM, masks (only blocks that
+//    reach the query block), keeps a running max (rescaling O in TMEM only
+//    when the max grows by more than 2^8), writes P (bf16 pairs) over the
+//    first half of the S buffer it came from, and finally reads O.
+//  With one 128-row tile a CTA uses 97 KB of shared memory and 256 TMEM
+//  columns, so two CTAs share an SM and their softmax warps interleave.
 // Splits are fixed by key position and each row's arithmetic depends on that
 // row alone, so results do not depend on n_q, the row block or the batch.
 // Every mbarrier wait is bounded; a timeout is reported and the CTA drains.
@@ -30,7 +34,7 @@
 namespace vc {
 namespace vtc {
 
-constexpr int kBlockKeys = 64;   // keys per MMA block (4 pages)
+constexpr int kBlockKeys = 32;   // keys per MMA block (2 pages)
 constexpr int kSplitPages = 256; // 4096 keys per split, fixed by position
 constexpr int kTileRows = 128;
 
@@ -53,19 +57,20 @@ struct Args {
 template <int D, int QT>
 struct Cfg {
     static constexpr int NC = D / 64;                      // swizzle atoms along D
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = 4;
     static constexpr int QTILE = kTileRows * D * 2;        // one Q tile
     static constexpr int KTILE = kBlockKeys * D * 2;       // one K (or V) block
-    static constexpr int PTILE = kTileRows * kBlockKeys * 2;
     static constexpr int OFF_KV = QT * QTILE;
-    static constexpr int OFF_P = OFF_KV + STAGES * 2 * KTILE;
-    static constexpr int OFF_BAR = OFF_P + QT * 2 * PTILE;
+    static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * KTILE;
     static constexpr int NBAR = QT * 2 + QT * 2 + 2 + 2 * STAGES;  // s_ready, p_ready, pv_done, full, empty
     static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-    static constexpr int TMEM_COLS = (QT * 128 + QT * D) <= 256 ? 256 : 512;
+    static constexpr int TMEM_COLS = (QT * 2 * kBlockKeys + QT * D) <= 256 ? 256 : 512;
     static constexpr int THREADS = QT * 128 + 64;  // softmax warps + producer warp + MMA warp
-    __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) { return (uint32_t)(qt * 2 + buf) * 64; }
-    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * 128 + qt * D); }
+    static constexpr int MIN_CTAS = QT == 1 ? 2 : 1;  // resident CTAs per SM (TMEM: 256 columns each)
+    __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) {
+        return (uint32_t)(qt * 2 + buf) * kBlockKeys;
+    }
+    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * 2 * kBlockKeys + qt * D); }
 };
 
 // --- tcgen05 / descriptor helpers ------------------------------------------
@@ -84,6 +89,14 @@ __device__ inline void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t id
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// The same with the A operand (M lanes x 16 K elements, bf16 pairs per
+// 32-bit column) read from TMEM.
+__device__ inline void umma_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ inline void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -139,7 +152,6 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned
     uint8_t *sq = smem;
     uint8_t *skv = smem + C::OFF_KV;
-    uint8_t *sp = smem + C::OFF_P;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *s_ready = bars;             // [QT][2]
     uint64_t *p_ready = bars + QT * 2;    // [QT][2]
@@ -237,11 +249,11 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             auto issue_pv = [&](int j) {
                 const uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
                 for (int qt = 0; qt < QT; ++qt) {
-                    const uint8_t *pt = sp + (qt * 2 + (j & 1)) * C::PTILE;
+                    // P of block j: bf16 pairs in the first half of its S buffer
 #pragma unroll
                     for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-                        umma(tmem + C::O_COL(qt), sdesc(smem_u32(pt) + kk * 32, 16, 1024),
-                             sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
+                        umma_ta(tmem + C::O_COL(qt), tmem + C::S_COL(qt, j & 1) + kk * 8,
+                                sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
                 }
                 umma_commit(&pv_done[j & 1]);
                 umma_commit(&empty[j % C::STAGES]);
@@ -302,14 +314,22 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 for (int i = 0; i < 16; ++i) s[c0 + i] = v[i];
             }
             const int key0 = p0 * kPage + j * kBlockKeys;
-            float mb = -INFINITY;
+            // raw-score max; masking only where the block reaches the query
+            // block or the request's end (the same arithmetic either way, so a
+            // row's bits do not depend on n_q)
+            float mraw = -INFINITY;
+            if (key0 + kBlockKeys > len - a.n_q) {
 #pragma unroll
-            for (int c = 0; c < kBlockKeys; ++c) {
-                const int key = key0 + c;
-                const float v = (rvalid && key <= qpos && key < len) ? s[c] * a.scale_log2 : -INFINITY;
-                s[c] = v;
-                mb = fmaxf(mb, v);
+                for (int c = 0; c < kBlockKeys; ++c) {
+                    const int key = key0 + c;
+                    if (!(rvalid && key <= qpos && key < len)) s[c] = -INFINITY;
+                    mraw = fmaxf(mraw, s[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBlockKeys; ++c) mraw = fmaxf(mraw, s[c]);
             }
+            const float mb = mraw * a.scale_log2;
             // grow the reference max only when it rises by more than 2^8
             // (rare after the first block); O is rescaled in TMEM
             const bool grow = mb > m_used + 8.0f;
@@ -331,7 +351,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 l *= f;
                 m_used = mb;
             }
-            const float ms = m_used == -INFINITY ? 0.0f : m_used;
+            const float nms = m_used == -INFINITY ? 0.0f : -m_used;
             // slots past the request's end (or of pages past it) may hold any
             // bytes: zero their V rows so that 0 * NaN never reaches P V
             const int nvalid = len - key0;
@@ -341,26 +361,24 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                     const int kr = nvalid + e / (D / 8), c = e % (D / 8);
                     *reinterpret_cast<uint4 *>(vt + sw128(kr, c, kBlockKeys)) = make_uint4(0, 0, 0, 0);
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            // this P buffer was last read by block j - 2's P V
-            if (j >= 2) {
-                alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, a.status));
-                if (!alive) break;
-            }
-            uint8_t *prow = sp + (qt * 2 + (j & 1)) * C::PTILE;
+            // P (bf16 pairs) over the first half of this block's S buffer;
+            // the buffer's previous P was read by block j - 2's P V, which the
+            // MMA pipe finished before it wrote this block's S
 #pragma unroll
-            for (int c = 0; c < kBlockKeys / 8; ++c) {
-                float p[8];
+            for (int h = 0; h < kBlockKeys / 32; ++h) {
+                float pk[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = ex2(s[c * 8 + i] - ms);
-                    l += p[i];
+                for (int c = 0; c < 16; ++c) {
+                    const float p0v = ex2(fmaf(s[h * 32 + 2 * c], a.scale_log2, nms));
+                    const float p1v = ex2(fmaf(s[h * 32 + 2 * c + 1], a.scale_log2, nms));
+                    l += p0v;
+                    l += p1v;
+                    pk[c] = __uint_as_float(pack_bf16(p0v, p1v));
                 }
-                uint4 u = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                                     pack_bf16(p[6], p[7]));
-                *reinterpret_cast<uint4 *>(prow + sw128(r, c, kTileRows)) = u;
+                tmem_st16(tmem + lane_base + C::S_COL(qt, j & 1) + h * 16, pk);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive(&p_ready[qt * 2 + (j & 1)]);
             o_touched = true;
