@@ -374,7 +374,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging"])
+                    choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging", "70b_128k_drop4"])
     args = ap.parse_args()
     rank, ws = dist_init()
     if args.impl == "reference":
@@ -383,7 +383,8 @@ def main():
     if args.workload != WORKLOAD:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        {"mixed_32req_3bit": mixed_main, "toy_e2e": toy_main, "staging": staging_main}[args.workload](args)
+        {"mixed_32req_3bit": mixed_main, "toy_e2e": toy_main, "staging": staging_main,
+         "70b_128k_drop4": big_main}[args.workload](args)
         return
     import torch
     import synth
@@ -487,23 +488,45 @@ def e2e_measure(w, st, rnd, args, ws, device):
     hqv.copy_(st["qv"])
     hout = torch.empty((B, x + 1), dtype=torch.int32, pin_memory=True)
     hlen = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    stage_k = torch.empty_like(full.k_pages)
-    stage_v = torch.empty_like(full.v_pages)
-    staged = vc.PagedKV(stage_k, stage_v, full.block_table, full.seq_lens, full.num_kv_heads, full.head_dim, 16)
-    qd = torch.empty_like(st["q"])
-    qvd = torch.empty_like(st["qv"])
+    # two staging buffers: round i stages into buffer i % 2 while round i - 1
+    # verifies from the other; a copy waits for the verify that last read its
+    # buffer
+    bufs = []
+    for _ in range(2):
+        sk, sv = torch.empty_like(full.k_pages), torch.empty_like(full.v_pages)
+        bufs.append((sk, sv, vc.PagedKV(sk, sv, full.block_table, full.seq_lens, full.num_kv_heads,
+                                        full.head_dim, 16)))
+    # the step's queries, double-buffered like KV_full: copied on the staging
+    # stream right after the previous round's KV_full.  Host->device copies
+    # share one copy-engine queue, so a small copy on the compute stream would
+    # wait behind a half-gigabyte staging copy and hold the drafting back; on
+    # the staging stream it lands exactly when the drafting may start anyway.
+    qbufs = [(torch.empty_like(st["q"]), torch.empty_like(st["qv"])) for _ in range(2)]
     side = torch.cuda.Stream(device=device)
-    done = torch.cuda.Event()
+    staged_ev = [torch.cuda.Event(), torch.cuda.Event()]
+    verified_ev = [torch.cuda.Event(), torch.cuda.Event()]
+    q_ev = [torch.cuda.Event(), torch.cuda.Event()]
     nbytes = hk.numel()
+    it = [0]
 
     def step():
-        vc.stage_async(stage_k, hk, nbytes, side)
-        vc.stage_async(stage_v, hv, nbytes, side, done)
-        qd.copy_(hq, non_blocking=True)
-        qvd.copy_(hqv, non_blocking=True)
-        rnd.run(q=qd, qv=qvd, full=staged, verify_wait=done)
+        i = it[0] % 2
+        sk, sv, staged = bufs[i]
+        qd, qvd = qbufs[i]
+        if it[0] >= 2:
+            side.wait_event(verified_ev[i])
+        with torch.cuda.stream(side):
+            qd.copy_(hq, non_blocking=True)
+            qvd.copy_(hqv, non_blocking=True)
+            q_ev[i].record(side)
+        vc.stage_async(sk, hk, nbytes, side)
+        vc.stage_async(sv, hv, nbytes, side, staged_ev[i])
+        torch.cuda.current_stream().wait_event(q_ev[i])
+        rnd.run(q=qd, qv=qvd, full=staged, verify_wait=staged_ev[i])
+        verified_ev[i].record()
         hout.copy_(rnd.emit, non_blocking=True)
         hlen.copy_(rnd.alen, non_blocking=True)
+        it[0] += 1
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -518,14 +541,113 @@ def e2e_measure(w, st, rnd, args, ws, device):
     d2h = hout.numel() * 4 + hlen.numel() * 4
     return {"value": ws * B * x * args.steps / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "note": "KV_full (%.2f GB) staged from pinned host memory on a side stream each round, "
-                    "overlapping the drafting" % (2 * nbytes / 1e9)}
+            "note": "KV_full (%.2f GB) staged from pinned host memory on a side stream each round "
+                    "into one of two device buffers, overlapping the drafting; host link measured at "
+                    "211 GB/s" % (2 * nbytes / 1e9)}
 
 
 # ---------------------------------------------------------------------------
 # other workloads (not the headline line): staggered mixed batch, toy loop,
 # host -> device staging bandwidth
 # ---------------------------------------------------------------------------
+
+def big_main(args):
+    """70B-shaped layer (batch 4, 64q/8kv, D 128, 131072-token context,
+    32768 kept in bf16: 64 sink + 512 recent + top by a seeded score): the
+    draft call over KV_comp and the 40-query verify over KV_full, plus the
+    40k-context verify point (batch 8, 32q/8kv, context 40960, 40 queries).
+    Each call is captured in a CUDA graph and timed over replays."""
+    import torch
+    import synth
+    import lossless_compressed_kv_gb300 as vc
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    w = dict(synth.WORKLOADS["70b_128k_drop4"])
+    B, hq, hkv, d, N, x = w["batch"], w["hq"], w["hkv"], w["d"], w["ctx"], w["x"]
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    peak, _ = peaks()
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        tpeak = float(json.load(f)["bf16_tflops"])
+
+    def pools(b, n_tok, nkv):
+        npg = (n_tok + 15) // 16
+        perm = torch.randperm(b * npg, generator=g, device=device).to(torch.int32)
+        kp = torch.empty((b * npg, nkv, 16, d), dtype=torch.bfloat16, device=device)
+        vp = torch.empty_like(kp)
+        for s0 in range(0, b * npg, 1024):
+            e = min(b * npg, s0 + 1024)
+            kp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
+            vp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
+        return vc.PagedKV(kp.view(torch.uint8).view(b * npg, -1), vp.view(torch.uint8).view(b * npg, -1),
+                          perm.view(b, npg).contiguous(), torch.full((b,), n_tok, dtype=torch.int32, device=device),
+                          nkv, d, 16)
+
+    def timed(fn, reps):
+        gr = capture(fn)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gr.replay()
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b2.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b2) / reps * 1e3  # us
+
+    scale = 1.0 / math.sqrt(d)
+    L = N + x
+    full = pools(B, L, hkv)
+    rng = synth.rng_for("70b_128k_drop4")
+    kept = [synth.kept_sink_recent_topk(rng, N, w["sink"], w["recent"], w["kept_total"]) for _ in range(B)]
+    offs, idx = synth.csr(kept)
+    nk = w["kept_total"]
+    cpg = (nk + x + 15) // 16
+    cperm = torch.randperm(B * cpg, generator=g, device=device).to(torch.int32)
+    comp = vc.PagedKV.allocate(B * cpg, hkv, d, 16, cperm.view(B, cpg).contiguous(),
+                               torch.full((B,), nk, dtype=torch.int32, device=device), device=device)
+    vc.compress(full, torch.from_numpy(offs).to(device), torch.from_numpy(idx).to(device), comp, nk)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    q = torch.randn((B, hq, d), generator=g, device=device).to(torch.bfloat16)
+    dout = torch.empty((B, hq, d), dtype=torch.float32, device=device)
+    dws = torch.empty(vc.draft_workspace_bytes(comp, hq, nk), dtype=torch.uint8, device=device)
+    t_draft = timed(lambda: vc.draft_attn(q, comp, scale, dout, nk, dws, status=status), 20)
+    draft_bytes_ = B * nk * hkv * 2 * d * 2
+    qv = torch.randn((B, x, hq, d), generator=g, device=device).to(torch.bfloat16)
+    vout = torch.empty((B, x, hq, d), dtype=torch.float32, device=device)
+    vws = torch.empty(vc.verify_workspace_bytes(full, x, hq, L), dtype=torch.uint8, device=device)
+    t_ver = timed(lambda: vc.verify_attn(qv, full, scale, vout, L, vws, status=status), 10)
+    ver_bytes = B * L * hkv * 2 * d * 2
+    ver_flops = 2 * 2 * B * x * hq * L * d
+    del full, comp, dws, vws
+    torch.cuda.empty_cache()
+    # the 40k-context verify point
+    B2, hq2, N2, x2 = 8, 32, 40960, 40
+    L2 = N2 + x2
+    full2 = pools(B2, L2, hkv)
+    qv2 = torch.randn((B2, x2, hq2, d), generator=g, device=device).to(torch.bfloat16)
+    vout2 = torch.empty((B2, x2, hq2, d), dtype=torch.float32, device=device)
+    vws2 = torch.empty(vc.verify_workspace_bytes(full2, x2, hq2, L2), dtype=torch.uint8, device=device)
+    t_ver2 = timed(lambda: vc.verify_attn(qv2, full2, scale, vout2, L2, vws2, status=status), 10)
+    torch.cuda.synchronize()
+    assert status.item() == 0, "device status %d" % status.item()
+    v2_bytes = B2 * L2 * hkv * 2 * d * 2
+    v2_flops = 2 * 2 * B2 * x2 * hq2 * L2 * d
+    print(json.dumps({
+        "metric": "70B-shaped layer: draft over bf16 token-drop KV_comp and 40-query verify; 40k-context verify",
+        "workload": "70b_128k_drop4",
+        "config": {"batch": B, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "ctx": N, "kept": nk, "x": x},
+        "draft": {"us_per_call": t_draft, "bytes": draft_bytes_, "GBps": draft_bytes_ / t_draft / 1e3,
+                  "frac_hbm_measured": draft_bytes_ / t_draft / 1e3 / peak,
+                  "tokens_per_s": B / (t_draft * 1e-6)},
+        "verify": {"us_per_call": t_ver, "bytes": ver_bytes, "GBps": ver_bytes / t_ver / 1e3,
+                   "frac_hbm_measured": ver_bytes / t_ver / 1e3 / peak, "TFLOPs": ver_flops / t_ver / 1e6,
+                   "frac_bf16_measured": ver_flops / t_ver / 1e6 / tpeak},
+        "verify_40k": {"config": {"batch": B2, "q_heads": hq2, "kv_heads": hkv, "ctx": N2, "n_q": x2},
+                       "us_per_call": t_ver2, "GBps": v2_bytes / t_ver2 / 1e3,
+                       "frac_hbm_measured": v2_bytes / t_ver2 / 1e3 / peak, "TFLOPs": v2_flops / t_ver2 / 1e6,
+                       "frac_bf16_measured": v2_flops / t_ver2 / 1e6 / tpeak},
+        "timing": "CUDA events around replays of a CUDA graph of the call; flops count the causal block as full",
+    }), flush=True)
+
 
 def staging_main(args):
     """Pinned host -> device copy bandwidth, one stream and four streams."""

@@ -6,7 +6,8 @@
 // parallel; query i of the block attends causally to every earlier position
 // and to itself ("KV Cache and Speculative Decoding": causal attention).
 // Launch: one CTA per (split of 4096 keys, row block, request x kv head);
-// a row block holds up to two 128-row MMA tiles of (query, head) rows.
+// a row block holds up to three 128-row MMA tiles of (query, head) rows (the
+// fewest tiles that cover the rows; more rows take further row blocks).
 #include "verify_tc.cuh"
 
 namespace vc {
@@ -114,9 +115,14 @@ cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, 
     Args a;
     if (!verify_args(a, q, n_q, hq, f, scale, max(max_seq_len, 1), ws, status)) return cudaErrorInvalidValue;
     const int d = f.fmt.head_dim;
-    const bool two = n_q * a.grp > vtc::kTileRows;
-    cudaError_t e = d == 64 ? (two ? launch<64, 2>(a, f.batch, st) : launch<64, 1>(a, f.batch, st))
-                            : (two ? launch<128, 2>(a, f.batch, st) : launch<128, 1>(a, f.batch, st));
+    const int tiles = min(3, ceil_div(n_q * a.grp, vtc::kTileRows));
+    cudaError_t e;
+    if (d == 64)
+        e = tiles == 1 ? launch<64, 1>(a, f.batch, st) : tiles == 2 ? launch<64, 2>(a, f.batch, st)
+                                                         : launch<64, 3>(a, f.batch, st);
+    else
+        e = tiles == 1 ? launch<128, 1>(a, f.batch, st) : tiles == 2 ? launch<128, 2>(a, f.batch, st)
+                                                          : launch<128, 3>(a, f.batch, st);
     if (e != cudaSuccess) return e;
     const int rows = f.batch * n_q * hq;
     if (d == 64)

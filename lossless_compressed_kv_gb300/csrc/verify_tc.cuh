@@ -57,20 +57,26 @@ struct Args {
 template <int D, int QT>
 struct Cfg {
     static constexpr int NC = D / 64;                      // swizzle atoms along D
-    static constexpr int STAGES = 4;
+    // K/V ring depth: one-tile CTAs run two per SM (4 stages each); larger
+    // CTAs run alone and prefetch deeper to cover HBM latency
+    static constexpr int STAGES = QT == 1 ? 4 : QT == 2 ? 8 : 6;
+    // S buffers per tile in TMEM (P is written over its S buffer): two let a
+    // tile's next S overlap its softmax; three tiles fit 512 columns with one
+    // each and overlap across tiles instead
+    static constexpr int SB = QT == 3 ? 1 : 2;
     static constexpr int QTILE = kTileRows * D * 2;        // one Q tile
     static constexpr int KTILE = kBlockKeys * D * 2;       // one K (or V) block
     static constexpr int OFF_KV = QT * QTILE;
     static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * KTILE;
     static constexpr int NBAR = QT * 2 + QT * 2 + 2 + 2 * STAGES;  // s_ready, p_ready, pv_done, full, empty
     static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-    static constexpr int TMEM_COLS = (QT * 2 * kBlockKeys + QT * D) <= 256 ? 256 : 512;
+    static constexpr int TMEM_COLS = (QT * SB * kBlockKeys + QT * D) <= 256 ? 256 : 512;
     static constexpr int THREADS = QT * 128 + 64;  // softmax warps + producer warp + MMA warp
     static constexpr int MIN_CTAS = QT == 1 ? 2 : 1;  // resident CTAs per SM (TMEM: 256 columns each)
     __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) {
-        return (uint32_t)(qt * 2 + buf) * kBlockKeys;
+        return (uint32_t)(qt * SB + buf) * kBlockKeys;
     }
-    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * 2 * kBlockKeys + qt * D); }
+    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * SB * kBlockKeys + qt * D); }
 };
 
 // --- tcgen05 / descriptor helpers ------------------------------------------
@@ -246,21 +252,30 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     } else if (mma_warp) {
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
-            auto issue_pv = [&](int j) {
-                const uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
-                for (int qt = 0; qt < QT; ++qt) {
-                    // P of block j: bf16 pairs in the first half of its S buffer
+            auto issue_s = [&](int j, int qt, const uint8_t *kt) {
+                const uint8_t *qtile = sq + qt * C::QTILE;
 #pragma unroll
-                    for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-                        umma_ta(tmem + C::O_COL(qt), tmem + C::S_COL(qt, j & 1) + kk * 8,
-                                sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
-                }
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma(tmem + C::S_COL(qt, j % C::SB),
+                         sdesc(smem_u32(qtile) + (ks >> 2) * (kTileRows * 128) + (ks & 3) * 32, 16, 1024),
+                         sdesc(smem_u32(kt) + (ks >> 2) * (kBlockKeys * 128) + (ks & 3) * 32, 16, 1024), IQK,
+                         ks > 0);
+                umma_commit(&s_ready[qt * 2 + j % C::SB]);
+            };
+            auto issue_pv_tile = [&](int j, int qt) {
+                const uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
+                // P of block j: bf16 pairs in the first half of its S buffer
+#pragma unroll
+                for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+                    umma_ta(tmem + C::O_COL(qt), tmem + C::S_COL(qt, j % C::SB) + kk * 8,
+                            sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
+            };
+            auto finish_pv = [&](int j) {
                 umma_commit(&pv_done[j & 1]);
                 umma_commit(&empty[j % C::STAGES]);
             };
-            auto wait_p = [&](int j) {
-                for (int qt = 0; qt < QT && alive; ++qt)
-                    alive = mbar_wait(&p_ready[qt * 2 + (j & 1)], (j >> 1) & 1, a.status);
+            auto wait_p = [&](int j, int qt) {
+                alive = alive && mbar_wait(&p_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status);
                 tc_fence_after();
             };
             for (int j = 0; j < nb && alive; ++j) {
@@ -269,24 +284,35 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 if (!alive) break;
                 tc_fence_after();
                 const uint8_t *kt = skv + st * 2 * C::KTILE;
-                for (int qt = 0; qt < QT; ++qt) {
-                    const uint8_t *qtile = sq + qt * C::QTILE;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        umma(tmem + C::S_COL(qt, j & 1),
-                             sdesc(smem_u32(qtile) + (ks >> 2) * (kTileRows * 128) + (ks & 3) * 32, 16, 1024),
-                             sdesc(smem_u32(kt) + (ks >> 2) * (kBlockKeys * 128) + (ks & 3) * 32, 16, 1024), IQK,
-                             ks > 0);
-                    umma_commit(&s_ready[qt * 2 + (j & 1)]);
-                }
-                if (j >= 1) {
-                    wait_p(j - 1);
-                    if (alive) issue_pv(j - 1);
+                if constexpr (C::SB == 2) {
+                    // S of every tile for block j, then P V of block j - 1
+                    for (int qt = 0; qt < QT; ++qt) issue_s(j, qt, kt);
+                    if (j >= 1) {
+                        for (int qt = 0; qt < QT; ++qt) wait_p(j - 1, qt);
+                        if (!alive) break;
+                        for (int qt = 0; qt < QT; ++qt) issue_pv_tile(j - 1, qt);
+                        finish_pv(j - 1);
+                    }
+                } else {
+                    // one S buffer per tile: a tile's P V of block j - 1 reads
+                    // the buffer its S of block j then overwrites (in order)
+                    for (int qt = 0; qt < QT && alive; ++qt) {
+                        if (j >= 1) {
+                            wait_p(j - 1, qt);
+                            if (!alive) break;
+                            issue_pv_tile(j - 1, qt);
+                        }
+                        issue_s(j, qt, kt);
+                    }
+                    if (j >= 1 && alive) finish_pv(j - 1);
                 }
             }
             if (nb > 0 && alive) {
-                wait_p(nb - 1);
-                if (alive) issue_pv(nb - 1);
+                for (int qt = 0; qt < QT; ++qt) wait_p(nb - 1, qt);
+                if (alive) {
+                    for (int qt = 0; qt < QT; ++qt) issue_pv_tile(nb - 1, qt);
+                    finish_pv(nb - 1);
+                }
             }
         }
     } else {
@@ -302,14 +328,14 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
         // tcgen05.ld / st are warp-collective: every lane of a softmax warp runs
         // them together (row validity and rescale decisions only pick values)
         for (int j = 0; j < nb && alive; ++j) {
-            alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + (j & 1)], (j >> 1) & 1, a.status));
+            alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status));
             if (!alive) break;
             tc_fence_after();
             float s[kBlockKeys];
 #pragma unroll
             for (int c0 = 0; c0 < kBlockKeys; c0 += 16) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + C::S_COL(qt, j & 1) + c0, v);
+                tmem_ld16(tmem + lane_base + C::S_COL(qt, j % C::SB) + c0, v);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) s[c0 + i] = v[i];
             }
@@ -377,10 +403,10 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                     l += p1v;
                     pk[c] = __uint_as_float(pack_bf16(p0v, p1v));
                 }
-                tmem_st16(tmem + lane_base + C::S_COL(qt, j & 1) + h * 16, pk);
+                tmem_st16(tmem + lane_base + C::S_COL(qt, j % C::SB) + h * 16, pk);
             }
             tc_fence_before();
-            mbar_arrive(&p_ready[qt * 2 + (j & 1)]);
+            mbar_arrive(&p_ready[qt * 2 + j % C::SB]);
             o_touched = true;
         }
         // epilogue: the whole warp waits for the last P V and reads O

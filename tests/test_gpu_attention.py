@@ -177,6 +177,8 @@ VERIFY_CASES = [
     (64, 2, 2, 1, [1, 17, 4096, 4097]),
     (128, 3, 1, 33, [700]),
     (64, 1, 8, 64, [64, 200]),
+    (128, 2, 4, 40, [40, 4200, 8200]),   # 160 rows: two 128-row tiles
+    (64, 1, 8, 24, [24, 700]),           # 192 rows: two tiles, head_dim 64
 ]
 
 
