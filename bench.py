@@ -202,7 +202,9 @@ class Round:
         self.emit = torch.empty((B, x + 1), dtype=torch.int32, device=device)
         self.aws = torch.empty(vc.accept_workspace_bytes(B, x, w["vocab"], d), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.launches = x * (1 + 2) + 2 + 2
+        # kernels per round: x x (append + draft + draft reduce), verify + its
+        # reduce, accept's mean + logits + finalize
+        self.launches = x * (1 + 2) + 2 + 3
 
     def run(self, q=None, qv=None, ev=None, full=None, verify_wait=None):
         import torch

@@ -70,6 +70,9 @@ def lib():
         L.vco_verify_attn.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
                                       P, P, C.c_double, P]
         L.vco_accept.restype = C.c_int
+        L.vco_keynorm_scores.argtypes = [P, C.c_int, C.c_int, C.c_int, P]
+        L.vco_select_kept.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P]
+        L.vco_select_kept.restype = C.c_int
         L.vco_accept.argtypes = [P, C.c_int, C.c_int, P, C.c_int, C.c_int, P, C.c_int,
                                  P, P, P, P]
         _lib = L
@@ -315,3 +318,23 @@ def accept(hidden, w, drafts, want_ambiguous: bool = True):
                           _p(em), _p(amb))
     return dict(verified=ver, accept_len=int(al[0]), emitted=em, n_emitted=int(ne),
                 ambiguous=(amb.astype(bool) if amb is not None else None))
+
+
+def keynorm_scores(k) -> np.ndarray:
+    """Token importance: mean over kv heads of the fp32 key L2 norm.
+    k: bf16 bits [n][hkv][d] -> fp32 [n] (the guide's compressor)."""
+    k = _c(k, np.uint16)
+    n, hkv, d = k.shape
+    out = np.empty(n, np.float32)
+    lib().vco_keynorm_scores(_p(k), n, hkv, d, _p(out))
+    return out
+
+
+def select_kept(score, sink: int, recent: int, keep: int) -> np.ndarray:
+    """Ascending kept-index list: sink and recent positions plus the middle
+    positions of highest score (ties: lower position)."""
+    score = _c(score, np.float32)
+    n = int(score.shape[0])
+    out = np.empty(max(n, 1), np.int32)
+    c = lib().vco_select_kept(_p(score), n, int(sink), int(recent), int(keep), _p(out))
+    return out[:c].copy()

@@ -461,6 +461,83 @@ int vco_accept(const float *hidden, int n_pred, int hg, const float *w, int dm, 
     return ne;
 }
 
+/*
+ * Token importance of the guide's compressor ("VeriCache Guide",
+ * "Implementing VeriCache in Python and PyTorch", the compressor class: the
+ * key norm over the head dimension, averaged over heads, ranks the tokens).
+ * Reading fixed here so that a kept list is reproducible bit for bit: fp32,
+ * per kv head the sum of squares with one fused multiply-add per channel in
+ * increasing channel order, a correctly rounded square root, the heads'
+ * norms added in increasing head order, then divided by the head count.
+ * k: [n][hkv][d] bf16; score: [n].
+ */
+void vco_keynorm_scores(const uint16_t *k, int n, int hkv, int d, float *score)
+{
+    for (int t = 0; t < n; t++) {
+        float tot = 0.0f;
+        for (int h = 0; h < hkv; h++) {
+            const uint16_t *row = k + ((size_t)t * hkv + h) * d;
+            float ss = 0.0f;
+            for (int c = 0; c < d; c++) {
+                float x = vco_bf16_to_f32(row[c]);
+                ss = fmaf(x, x, ss);
+            }
+            tot = tot + sqrtf(ss);
+        }
+        score[t] = tot / (float)hkv;
+    }
+}
+
+/* (score, position) order of the selection: higher score first, equal
+ * scores by lower position */
+typedef struct {
+    float s;
+    int i;
+} vco_ranked;
+
+static int vco_rank_cmp(const void *a, const void *b)
+{
+    const vco_ranked *x = (const vco_ranked *)a, *y = (const vco_ranked *)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->i > y->i) - (x->i < y->i);
+}
+
+/*
+ * Kept-index list of one request (the guide's compressor: the top tokens by
+ * importance, then sorted by position; with the sink / recent window of the
+ * workloads): positions [0, sink) and [n - recent, n) always (clamped to n),
+ * plus the `keep - sink - recent` middle positions of highest score, equal
+ * scores by lower position, all written in ascending position order.  The
+ * middle takes max(0, min(n - sink - recent, keep - sink - recent))
+ * positions.  Returns the number of indices written.
+ */
+int vco_select_kept(const float *score, int n, int sink, int recent, int keep, int32_t *idx)
+{
+    if (sink > n) sink = n;
+    if (recent > n - sink) recent = n - sink;
+    int m = n - sink - recent;
+    int top = keep - sink - recent;
+    if (top < 0) top = 0;
+    if (top > m) top = m;
+    uint8_t *take = (uint8_t *)calloc((size_t)n + 1, 1);
+    vco_ranked *r = (vco_ranked *)malloc(sizeof(vco_ranked) * ((size_t)m + 1));
+    for (int j = 0; j < m; j++) {
+        r[j].s = score[sink + j];
+        r[j].i = sink + j;
+    }
+    qsort(r, (size_t)m, sizeof(vco_ranked), vco_rank_cmp);
+    for (int j = 0; j < top; j++) take[r[j].i] = 1;
+    for (int t = 0; t < sink; t++) take[t] = 1;
+    for (int t = n - recent; t < n; t++) take[t] = 1;
+    int c = 0;
+    for (int t = 0; t < n; t++)
+        if (take[t]) idx[c++] = t;
+    free(take);
+    free(r);
+    return c;
+}
+
 /* array helpers for the tests */
 void vco_f32_to_f16_array(const float *x, uint16_t *out, size_t n)
 {
