@@ -598,10 +598,26 @@ def big_main(args):
     scale = 1.0 / math.sqrt(d)
     L = N + x
     full = pools(B, L, hkv)
-    rng = synth.rng_for("70b_128k_drop4")
-    kept = [synth.kept_sink_recent_topk(rng, N, w["sink"], w["recent"], w["kept_total"]) for _ in range(B)]
-    offs, idx = synth.csr(kept)
+    # kept lists on the GPU (vc_select_kept) from the seeded scores; the
+    # workload generator's lists are the same (tests/test_gpu_select.py)
     nk = w["kept_total"]
+    scores = np.zeros((B, N), np.float32)
+    for b in range(B):
+        r = np.random.default_rng([w["seed"], 1, b])
+        scores[b, w["sink"]:N - w["recent"]] = r.random(N - w["sink"] - w["recent"], dtype=np.float32)
+    scores_d = torch.from_numpy(scores).to(device)
+    offs_d = torch.arange(0, (B + 1) * nk, nk, dtype=torch.int32, device=device)
+    idx_d = torch.empty(B * nk, dtype=torch.int32, device=device)
+    sel_status = torch.zeros(1, dtype=torch.int32, device=device)
+    t_sel = timed(lambda: vc.select_kept(full, offs_d, idx_d, w["sink"], w["recent"], scores=scores_d,
+                                         status=sel_status), 10)
+    sws = torch.empty(vc.select_workspace_bytes(B, N), dtype=torch.uint8, device=device)
+    idx_kn = torch.empty(B * nk, dtype=torch.int32, device=device)
+    t_sel_kn = timed(lambda: vc.select_kept(full, offs_d, idx_kn, w["sink"], w["recent"], score_stride=N,
+                                            workspace=sws, status=sel_status), 5)
+    torch.cuda.synchronize()
+    assert sel_status.item() == 0
+    offs, idx = offs_d.cpu().numpy(), idx_d.cpu().numpy()
     cpg = (nk + x + 15) // 16
     cperm = torch.randperm(B * cpg, generator=g, device=device).to(torch.int32)
     comp = vc.PagedKV.allocate(B * cpg, hkv, d, 16, cperm.view(B, cpg).contiguous(),
@@ -637,6 +653,10 @@ def big_main(args):
         "metric": "70B-shaped layer: draft over bf16 token-drop KV_comp and 40-query verify; 40k-context verify",
         "workload": "70b_128k_drop4",
         "config": {"batch": B, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "ctx": N, "kept": nk, "x": x},
+        "select_kept": {"us_seeded_scores": t_sel, "us_keynorm_scores": t_sel_kn,
+                        "keynorm_GBps": B * N * hkv * d * 2 / t_sel_kn / 1e3,
+                        "note": "4 x 131072 positions, 64 sink + 512 recent + top by score, 32768 kept per "
+                                "request; key-norm path reads every K row"},
         "draft": {"us_per_call": t_draft, "bytes": draft_bytes_, "GBps": draft_bytes_ / t_draft / 1e3,
                   "frac_hbm_measured": draft_bytes_ / t_draft / 1e3 / peak,
                   "tokens_per_s": B / (t_draft * 1e-6)},

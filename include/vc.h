@@ -122,6 +122,37 @@ VC_API size_t vc_page_bytes(const vc_kv_format *fmt);
 VC_API size_t vc_head_block_bytes(const vc_kv_format *fmt);
 
 /*
+ * vc_select_kept -- the kept-index list of a token-drop KV_comp ("VeriCache
+ * Guide", the compressor class of "Implementing VeriCache in Python and
+ * PyTorch": tokens ranked by the norm of their key over head_dim averaged
+ * over the heads, the top ones kept in position order).
+ *  full          bits == 16 cache; seq_lens[b] = n_b positions of request b.
+ *  scores        device fp32 [batch][score_stride] importance per position,
+ *                or NULL: computed from full's K pages (head_dim 64 or 128)
+ *                as, per kv head, sqrt of the sum of squares (one fused
+ *                multiply-add per channel in increasing order, correctly
+ *                rounded square root), added over heads in increasing order
+ *                and divided by the head count.  Positions >= score_stride
+ *                are not considered (n_b is capped to it).
+ *  kept_offsets  device int32 [batch + 1]: request b's list goes to
+ *                kept_idx[kept_offsets[b] .. kept_offsets[b + 1]); its
+ *                length keep_b must equal s + r + top with s = min(sink, n),
+ *                r = min(recent, n - s), top = min(n - s - r, keep_b - s - r)
+ *                (else VC_ERR_INVALID_ARG in dev_status, nothing written).
+ *  sink, recent  host: positions [0, s) and [n - r, n) are always kept.
+ *  kept_idx      device int32 out: ascending positions; the middle positions
+ *                are the `top` of highest score, equal scores by lower
+ *                position.
+ *  workspace     device, vc_select_workspace_bytes(batch, score_stride)
+ *                bytes when scores == NULL (may be NULL otherwise).
+ */
+VC_API size_t vc_select_workspace_bytes(int32_t batch, int32_t score_stride);
+VC_API vc_status vc_select_kept(const vc_paged_kv *full, const float *scores, int32_t score_stride,
+                                const int32_t *kept_offsets, int32_t sink, int32_t recent, int32_t *kept_idx,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                vc_stream_t stream);
+
+/*
  * vc_compress -- KV_comp entries from KV_full ("VeriCache Guide", "The
  * Uniform Compressor Interface"; the guide's compressor gathers K and V with
  * one sorted index list shared by all heads).

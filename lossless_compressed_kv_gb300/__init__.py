@@ -46,6 +46,9 @@ _SIG = {
     "vc_page_bytes": (C.c_size_t, [C.POINTER(KVFormat)]),
     "vc_head_block_bytes": (C.c_size_t, [C.POINTER(KVFormat)]),
     "vc_compress": (C.c_int, [C.POINTER(PagedKVStruct), _P, _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P, _P]),
+    "vc_select_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "vc_select_kept": (C.c_int, [C.POINTER(PagedKVStruct), _P, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P,
+                                 C.c_size_t, _P, _P]),
     "vc_draft_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32]),
     "vc_draft_attn": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32, _P,
                                 C.c_size_t, _P, _P]),
@@ -169,6 +172,23 @@ def compress(full: PagedKV, kept_offsets, kept_idx, comp: PagedKV, max_kept: int
     fs, cs = full.struct(), comp.struct()
     _check(_lib.vc_compress(C.byref(fs), _ptr(kept_offsets), _ptr(kept_idx), _ptr(comp_start), int(max_kept),
                             C.byref(cs), _ptr(status), _stream(stream)), "vc_compress")
+
+
+def select_workspace_bytes(batch: int, score_stride: int) -> int:
+    return int(_lib.vc_select_workspace_bytes(int(batch), int(score_stride)))
+
+
+def select_kept(full: PagedKV, kept_offsets, kept_idx, sink: int, recent: int, scores=None, score_stride=None,
+                workspace=None, status=None, stream=None):
+    """Kept-index list per request into kept_idx (CSR by kept_offsets):
+    sink + recent windows plus the middle positions of highest score (key
+    norm averaged over heads when scores is None)."""
+    fs = full.struct()
+    stride = int(score_stride if score_stride is not None else (scores.shape[-1] if scores is not None else 0))
+    nb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.vc_select_kept(C.byref(fs), _ptr(scores), stride, _ptr(kept_offsets), int(sink), int(recent),
+                               _ptr(kept_idx), _ptr(workspace), nb, _ptr(status), _stream(stream)),
+           "vc_select_kept")
 
 
 def draft_workspace_bytes(comp: PagedKV, num_q_heads: int, max_seq_len: int) -> int:

@@ -18,6 +18,10 @@ size_t verify_workspace(const vc_paged_kv &f, int n_q, int hq, int max_seq_len);
 cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, float scale, float *out,
                           int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
 size_t accept_workspace(int batch, int n_pred, int vocab, int d);
+size_t select_workspace(int batch, int max_seq_len);
+vc_status select_kept(const vc_paged_kv *full, const float *scores, int32_t score_stride,
+                      const int32_t *kept_offsets, int32_t sink, int32_t recent, int32_t *kept_idx, void *ws,
+                      size_t ws_bytes, int32_t *dev_status, cudaStream_t st);
 cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, const float *w, int d,
                           int vocab, const int32_t *drafts, int x, int32_t *verified, int32_t *accept_len,
                           int32_t *emitted, void *ws, cudaStream_t st);
@@ -60,6 +64,22 @@ vc_status vc_compress(const vc_paged_kv *full, const int32_t *kept_offsets, cons
         return VC_ERR_INVALID_ARG;
     return compress(full, kept_offsets, kept_idx, comp_start, max_kept, comp, dev_status,
                     (cudaStream_t)stream);
+}
+
+size_t vc_select_workspace_bytes(int32_t batch, int32_t score_stride) {
+    if (batch < 0 || score_stride < 1) return 0;
+    return select_workspace(batch, score_stride);
+}
+
+vc_status vc_select_kept(const vc_paged_kv *full, const float *scores, int32_t score_stride,
+                         const int32_t *kept_offsets, int32_t sink, int32_t recent, int32_t *kept_idx,
+                         void *workspace, size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream) {
+    if (!full || !full->seq_lens || !kept_offsets || !kept_idx || full->batch < 0 || sink < 0 || recent < 0 ||
+        score_stride < 1)
+        return VC_ERR_INVALID_ARG;
+    if (!scores && (!paged_ok(full) || !full->k_pages)) return VC_ERR_INVALID_ARG;
+    return select_kept(full, scores, score_stride, kept_offsets, sink, recent, kept_idx, workspace, workspace_bytes,
+                       dev_status, (cudaStream_t)stream);
 }
 
 size_t vc_draft_workspace_bytes(const vc_paged_kv *comp, int32_t num_q_heads, int32_t max_seq_len) {
