@@ -73,6 +73,9 @@ def lib():
         L.vco_keynorm_scores.argtypes = [P, C.c_int, C.c_int, C.c_int, P]
         L.vco_select_kept.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P]
         L.vco_select_kept.restype = C.c_int
+        L.vco_logits.argtypes = [P, C.c_int, C.c_int, P, C.c_int, C.c_int, P]
+        L.vco_accept_sampled.argtypes = [P, P, C.c_int, C.c_float, P, C.c_int, P, P, P, P, P]
+        L.vco_accept_sampled.restype = C.c_int
         L.vco_accept.argtypes = [P, C.c_int, C.c_int, P, C.c_int, C.c_int, P, C.c_int,
                                  P, P, P, P]
         _lib = L
@@ -338,3 +341,33 @@ def select_kept(score, sink: int, recent: int, keep: int) -> np.ndarray:
     out = np.empty(max(n, 1), np.int32)
     c = lib().vco_select_kept(_p(score), n, int(sink), int(recent), int(keep), _p(out))
     return out[:c].copy()
+
+
+def logits(hidden, w) -> np.ndarray:
+    """fp32 logits of hidden rows [rows][hg][d] (group mean, then one fused
+    multiply-add per hidden index in increasing order) -> [rows][vocab]."""
+    hidden = _c(hidden, np.float32)
+    if hidden.ndim == 2:
+        hidden = hidden[:, None, :]
+    w = _c(w, np.float32)
+    rows, hg, dm = hidden.shape
+    out = np.empty((rows, w.shape[1]), np.float32)
+    lib().vco_logits(_p(hidden), rows, hg, _p(w), dm, w.shape[1], _p(out))
+    return out
+
+
+def accept_sampled(target_logits, draft_logits, drafts, u, v, tau: float) -> dict:
+    """Rejection-sampling acceptance of one request (x drafts, x + 1 target
+    rows): accept_len, emitted [x + 1] (-1 padded), margins [x + 1]."""
+    tl = _c(target_logits, np.float32)
+    x = int(tl.shape[0]) - 1
+    vocab = int(tl.shape[1])
+    dl = _c(draft_logits, np.float32).reshape(max(x, 1), vocab) if x else np.zeros((1, vocab), np.float32)
+    dr = _c(drafts, np.int32).reshape(-1)
+    u = _c(u, np.float32).reshape(-1)
+    v = _c(v, np.float32).reshape(-1)
+    al = np.zeros(1, np.int32)
+    em = np.empty(x + 1, np.int32)
+    mg = np.empty(x + 1, np.float64)
+    lib().vco_accept_sampled(_p(tl), _p(dl), vocab, float(tau), _p(dr), x, _p(u), _p(v), _p(al), _p(em), _p(mg))
+    return dict(accept_len=int(al[0]), emitted=em, margins=mg)

@@ -538,6 +538,126 @@ int vco_select_kept(const float *score, int n, int sink, int recent, int keep, i
     return c;
 }
 
+/*
+ * Logits of hidden rows: mean of each row's hidden group (fp32, increasing
+ * j), then one fused multiply-add per hidden index in increasing order --
+ * the same arithmetic as vco_accept.  hidden [rows][hg][dm] -> out [rows][vocab].
+ */
+void vco_logits(const float *hidden, int rows, int hg, const float *w, int dm, int vocab, float *out)
+{
+    float *h = (float *)malloc(sizeof(float) * (size_t)dm);
+    for (int i = 0; i < rows; i++) {
+        for (int k = 0; k < dm; k++) {
+            float s = 0.0f;
+            for (int j = 0; j < hg; j++)
+                s = s + hidden[((size_t)i * hg + j) * dm + k];
+            h[k] = s / (float)hg;
+        }
+        for (int v = 0; v < vocab; v++) {
+            float acc = 0.0f;
+            for (int k = 0; k < dm; k++)
+                acc = fmaf(h[k], w[(size_t)k * vocab + v], acc);
+            out[(size_t)i * vocab + v] = acc;
+        }
+    }
+    free(h);
+}
+
+/* softmax(logits / tau) in fp64 */
+static void vco_softmax64(const float *l, int vocab, double tau, double *p)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < vocab; v++)
+        if ((double)l[v] / tau > m) m = (double)l[v] / tau;
+    double z = 0.0;
+    for (int v = 0; v < vocab; v++) {
+        p[v] = exp((double)l[v] / tau - m);
+        z += p[v];
+    }
+    for (int v = 0; v < vocab; v++) p[v] /= z;
+}
+
+/* inverse CDF: the first id whose cumulative weight exceeds u * total;
+ * *margin = distance of u * total to the nearest cumulative boundary,
+ * relative to total */
+static int vco_sample_cdf(const double *wgt, int vocab, double u, double *margin)
+{
+    double tot = 0.0;
+    for (int v = 0; v < vocab; v++) tot += wgt[v];
+    double thr = u * tot, cum = 0.0;
+    int pick = vocab - 1;
+    double best = INFINITY;
+    for (int v = 0; v < vocab; v++) {
+        if (wgt[v] <= 0.0) continue;
+        double next = cum + wgt[v];
+        double dm = fabs(next - thr);
+        if (dm < best) best = dm;
+        if (pick == vocab - 1 && next > thr) {
+            pick = v;
+        }
+        cum = next;
+    }
+    /* ids after the last positive weight are never picked */
+    if (pick == vocab - 1)
+        for (int v = vocab - 1; v >= 0; v--)
+            if (wgt[v] > 0.0) {
+                pick = v;
+                break;
+            }
+    *margin = tot > 0.0 ? best / tot : 0.0;
+    return pick;
+}
+
+/*
+ * Speculative acceptance with rejection sampling ("VeriCache Guide",
+ * "Mathematical Guarantee of Lossless Correctness"): draft token d_i is kept
+ * when u_i < alpha_i = min(1, p_target_i(d_i) / p_draft_i(d_i)); at the first
+ * rejection a token is drawn from the residual max(0, p_target_i -
+ * p_draft_i) (normalised) by inverse CDF with uniform v_i and the round
+ * ends; when all x drafts are kept a bonus token is drawn from
+ * p_target_x with v_x.  Distributions are softmax(logits / tau), in fp64.
+ * target_logits [x+1][vocab], draft_logits [x][vocab], u [x], v [x+1].
+ * emitted [x+1] (then -1); margins [x+1]: per decision taken, its distance
+ * to flipping (|u - alpha| for an accept test, the inverse-CDF boundary
+ * distance for a draw); returns the number of emitted tokens.
+ */
+int vco_accept_sampled(const float *target_logits, const float *draft_logits, int vocab, float tau,
+                       const int32_t *drafts, int x, const float *u, const float *v, int32_t *accept_len,
+                       int32_t *emitted, double *margins)
+{
+    double *pt = (double *)malloc(sizeof(double) * (size_t)vocab);
+    double *pd = (double *)malloc(sizeof(double) * (size_t)vocab);
+    int ne = 0, a = 0;
+    for (int j = 0; j < x + 1; j++) margins[j] = INFINITY;
+    for (; a < x; a++) {
+        vco_softmax64(target_logits + (size_t)a * vocab, vocab, (double)tau, pt);
+        vco_softmax64(draft_logits + (size_t)a * vocab, vocab, (double)tau, pd);
+        const int d = drafts[a];
+        const double alpha = pd[d] > 0.0 ? fmin(1.0, pt[d] / pd[d]) : 1.0;
+        margins[a] = fabs((double)u[a] - alpha);
+        if ((double)u[a] < alpha) {
+            emitted[ne++] = d;
+            continue;
+        }
+        for (int t = 0; t < vocab; t++) pd[t] = fmax(0.0, pt[t] - pd[t]);
+        double mg;
+        emitted[ne++] = vco_sample_cdf(pd, vocab, (double)v[a], &mg);
+        if (mg < margins[a]) margins[a] = mg;
+        break;
+    }
+    if (a == x) {
+        vco_softmax64(target_logits + (size_t)x * vocab, vocab, (double)tau, pt);
+        double mg;
+        emitted[ne++] = vco_sample_cdf(pt, vocab, (double)v[x], &mg);
+        margins[x] = mg;
+    }
+    *accept_len = a;
+    for (int j = ne; j < x + 1; j++) emitted[j] = -1;
+    free(pt);
+    free(pd);
+    return ne;
+}
+
 /* array helpers for the tests */
 void vco_f32_to_f16_array(const float *x, uint16_t *out, size_t n)
 {
