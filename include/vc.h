@@ -264,6 +264,32 @@ VC_API vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, i
                     void *workspace, size_t workspace_bytes, vc_stream_t stream);
 
 /*
+ * vc_accept_sampled -- acceptance for sampling at temperature tau > 0
+ * ("VeriCache Guide", "Mathematical Guarantee of Lossless Correctness"):
+ * draft i is kept while u[b][i] < min(1, p_target_i(d_i) / p_draft_i(d_i));
+ * at the first rejection a token is drawn from the normalised residual
+ * max(0, p_target_i - p_draft_i) by inverse CDF with v[b][i] and the round
+ * ends; when all x drafts are kept a bonus is drawn from p_target_x with
+ * v[b][x].  p = softmax(logits / tau), logits as in vc_accept (group mean of
+ * the hidden rows, fp32, one fused multiply-add per hidden index in
+ * increasing order); the softmax sums and the inverse CDF run in fp32.
+ *  target_hidden device fp32 [batch][x + 1][hidden_group][d]  (verifier rows)
+ *  draft_hidden  device fp32 [batch][x][hidden_group][d]      (drafter rows)
+ *  drafts        device int32 [batch][x]; an id outside [0, vocab) is rejected.
+ *  u, v          device fp32 [batch][x] and [batch][x + 1], uniform in [0, 1):
+ *                the caller's random numbers (the library draws none).
+ *  accept_len    device int32 [batch]; emitted device int32 [batch][x + 1]
+ *                (a kept drafts, then the drawn token; -1 after).
+ *  workspace     vc_accept_sampled_workspace_bytes(batch, x, vocab, d).
+ */
+VC_API size_t vc_accept_sampled_workspace_bytes(int32_t batch, int32_t x, int32_t vocab, int32_t d);
+VC_API vc_status vc_accept_sampled(const float *target_hidden, const float *draft_hidden, int32_t batch, int32_t x,
+                                   int32_t hidden_group, const float *lm_head, int32_t d, int32_t vocab,
+                                   float temperature, const int32_t *drafts, const float *u, const float *v,
+                                   int32_t *accept_len, int32_t *emitted, void *workspace, size_t workspace_bytes,
+                                   vc_stream_t stream);
+
+/*
  * vc_stage_async -- copy `bytes` from page-locked host memory to device
  * memory on the side stream `side` and record `done` (may be NULL) after it,
  * so a verify launch on another stream can wait for the staged KV_full

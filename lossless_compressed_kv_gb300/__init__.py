@@ -47,6 +47,9 @@ _SIG = {
     "vc_head_block_bytes": (C.c_size_t, [C.POINTER(KVFormat)]),
     "vc_compress": (C.c_int, [C.POINTER(PagedKVStruct), _P, _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P, _P]),
     "vc_select_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "vc_accept_sampled_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "vc_accept_sampled": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int32, C.c_int32, C.c_float,
+                                    _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "vc_select_kept": (C.c_int, [C.POINTER(PagedKVStruct), _P, C.c_int32, _P, C.c_int32, C.c_int32, _P, _P,
                                  C.c_size_t, _P, _P]),
     "vc_draft_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32]),
@@ -232,6 +235,24 @@ def accept(hidden, lm_head, drafts, verified, accept_len, emitted, workspace, hi
                           _ptr(drafts) if x else None, x, _ptr(verified), _ptr(accept_len), _ptr(emitted),
                           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "vc_accept")
+
+
+def accept_sampled_workspace_bytes(batch: int, x: int, vocab: int, d: int) -> int:
+    return int(_lib.vc_accept_sampled_workspace_bytes(int(batch), int(x), int(vocab), int(d)))
+
+
+def accept_sampled(target_hidden, draft_hidden, lm_head, drafts, u, v, temperature: float, accept_len, emitted,
+                   workspace, hidden_group: int = 1, stream=None):
+    """Rejection-sampling acceptance.  target_hidden [B][x+1][hg][d] (or
+    [B][x+1][d]), draft_hidden [B][x][hg][d], drafts [B][x] int32, u [B][x],
+    v [B][x+1] fp32 uniforms."""
+    b, x = int(target_hidden.shape[0]), int(target_hidden.shape[1]) - 1
+    d, vocab = int(lm_head.shape[0]), int(lm_head.shape[1])
+    _check(_lib.vc_accept_sampled(_ptr(target_hidden), _ptr(draft_hidden) if x else None, b, x, int(hidden_group),
+                                  _ptr(lm_head), d, vocab, float(temperature), _ptr(drafts) if x else None,
+                                  _ptr(u) if x else None, _ptr(v), _ptr(accept_len), _ptr(emitted),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "vc_accept_sampled")
 
 
 def stage_async(dst, pinned_src, nbytes: int, side_stream, done_event=None):

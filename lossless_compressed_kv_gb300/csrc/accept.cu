@@ -38,7 +38,7 @@ __device__ inline unsigned long long argmax_key(float v, int id) {
 __global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, float *h,
                                   unsigned long long *keys) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < rows) keys[i] = 0ull;
+    if (keys && i < rows) keys[i] = 0ull;
     if (i >= (int64_t)rows * d) return;
     const int64_t r = i / d, k = i % d;
     const float *hp = hidden + (r * hg) * d + k;
@@ -47,8 +47,11 @@ __global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, 
     h[i] = __fdiv_rn(s, (float)hg);
 }
 
+// STORE: write the logits [rows][vocab] instead of the argmax keys.
+template <bool STORE>
 __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
-                                                                 int vocab, unsigned long long *keys) {
+                                                                 int vocab, unsigned long long *keys,
+                                                                 float *logits) {
     __shared__ __align__(16) float hs[kKT][kRowsT];  // k-major: one k's 16 row values contiguous
     const int r0 = blockIdx.y * kRowsT;
     const int v0 = blockIdx.x * kCols + threadIdx.x * kColsT;
@@ -96,6 +99,15 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
             }
         }
     }
+    if constexpr (STORE) {
+#pragma unroll
+        for (int r = 0; r < kRowsT; ++r)
+            if (r0 + r < rows)
+#pragma unroll
+                for (int c = 0; c < kColsT; ++c)
+                    if (v0 + c < vocab) logits[(int64_t)(r0 + r) * vocab + v0 + c] = acc[r][c];
+        return;
+    }
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int r = 0; r < kRowsT; ++r) {
@@ -139,6 +151,156 @@ __global__ void accept_finalize_kernel(const unsigned long long *keys, int n_pre
     }
 }
 
+// ---------------------------------------------------------------------------
+// Rejection-sampling acceptance ("VeriCache Guide", "Mathematical Guarantee
+// of Lossless Correctness"): one CTA per request walks its drafts in order;
+// softmax(logits / tau) statistics by block reductions in fp32; a rejected
+// draft (or the bonus) is drawn by an inverse CDF over the residual (or the
+// target) distribution: per-thread contiguous chunks, a block scan of the
+// chunk sums, then the owning thread walks its chunk.
+// ---------------------------------------------------------------------------
+constexpr int kSampThreads = 512;
+
+__device__ float block_reduce(float x, bool is_max, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, x, off);
+        x = is_max ? fmaxf(x, o) : x + o;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        x = lane < kSampThreads / 32 ? red[lane] : (is_max ? -INFINITY : 0.0f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, x, off);
+            x = is_max ? fmaxf(x, o) : x + o;
+        }
+        if (lane == 0) red[32] = x;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+struct RowStats {
+    float m, z;  // max of logits / tau, sum of exp(logits / tau - m)
+};
+
+__device__ RowStats row_stats(const float *l, int vocab, float tau, float *red) {
+    float mx = -INFINITY;
+    for (int j = threadIdx.x; j < vocab; j += kSampThreads) mx = fmaxf(mx, __fdiv_rn(l[j], tau));
+    RowStats r;
+    r.m = block_reduce(mx, true, red);
+    float z = 0.0f;
+    for (int j = threadIdx.x; j < vocab; j += kSampThreads) z += __expf(__fdiv_rn(l[j], tau) - r.m);
+    r.z = block_reduce(z, false, red);
+    return r;
+}
+
+__device__ inline float prob(const float *l, int j, float tau, RowStats s) {
+    return __expf(__fdiv_rn(l[j], tau) - s.m) / s.z;
+}
+
+// Inverse CDF over weights w(j) >= 0: the first j whose cumulative weight
+// exceeds u * total (the last positive weight if rounding leaves none).
+template <class W>
+__device__ int draw(W w, int vocab, float u, float *red, float *scan, int *pick) {
+    const int chunk = (vocab + kSampThreads - 1) / kSampThreads;
+    const int c0 = min(vocab, threadIdx.x * chunk), c1 = min(vocab, c0 + chunk);
+    float cs = 0.0f;
+    int lastpos = -1;
+    for (int j = c0; j < c1; ++j) {
+        const float x = w(j);
+        if (x > 0.0f) {
+            cs += x;
+            lastpos = j;
+        }
+    }
+    scan[threadIdx.x] = cs;
+    if (threadIdx.x == 0) {
+        pick[0] = vocab;
+        pick[1] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // exclusive prefix of the chunk sums, in thread order
+        float run = 0.0f;
+        for (int i = 0; i < kSampThreads; ++i) {
+            const float c = scan[i];
+            scan[i] = run;
+            run += c;
+        }
+        red[33] = run;
+    }
+    __syncthreads();
+    atomicMax(&pick[1], lastpos);
+    const float thr = u * red[33];
+    float cum = scan[threadIdx.x];
+    if (cs > 0.0f && cum <= thr && thr < cum + cs) {
+        for (int j = c0; j < c1; ++j) {
+            const float x = w(j);
+            if (x > 0.0f) {
+                cum += x;
+                if (cum > thr) {
+                    atomicMin(&pick[0], j);
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int r = pick[0] < vocab ? pick[0] : max(pick[1], 0);
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kSampThreads) accept_sample_kernel(const float *tl, const float *dl, int vocab,
+                                                                    float tau, const int32_t *drafts, int x,
+                                                                    const float *u, const float *v,
+                                                                    int32_t *accept_len, int32_t *emitted) {
+    __shared__ float red[34];
+    __shared__ float scan[kSampThreads];
+    __shared__ int pick[2];
+    const int b = blockIdx.x;
+    const float *T = tl + (int64_t)b * (x + 1) * vocab;
+    const float *Dl = dl + (int64_t)b * x * vocab;
+    int32_t *em = emitted + (int64_t)b * (x + 1);
+    int a = 0, ne = 0;
+    for (; a < x; ++a) {
+        const float *lt = T + (int64_t)a * vocab, *ld = Dl + (int64_t)a * vocab;
+        const RowStats st = row_stats(lt, vocab, tau, red), sd = row_stats(ld, vocab, tau, red);
+        const int d = drafts[(int64_t)b * x + a];
+        float alpha = 0.0f;  // an out-of-range draft id is rejected
+        if (d >= 0 && d < vocab) {
+            const float pt = prob(lt, d, tau, st), pd = prob(ld, d, tau, sd);
+            alpha = pd > 0.0f ? fminf(1.0f, pt / pd) : 1.0f;
+        }
+        if (u[(int64_t)b * x + a] < alpha) {
+            if (threadIdx.x == 0) em[ne] = d;
+            ++ne;
+            continue;
+        }
+        const int t = draw([&](int j) { return fmaxf(0.0f, prob(lt, j, tau, st) - prob(ld, j, tau, sd)); },
+                           vocab, v[(int64_t)b * (x + 1) + a], red, scan, pick);
+        if (threadIdx.x == 0) em[ne] = t;
+        ++ne;
+        break;
+    }
+    if (a == x) {
+        const float *lt = T + (int64_t)x * vocab;
+        const RowStats st = row_stats(lt, vocab, tau, red);
+        const int t = draw([&](int j) { return prob(lt, j, tau, st); }, vocab, v[(int64_t)b * (x + 1) + x], red,
+                           scan, pick);
+        if (threadIdx.x == 0) em[ne] = t;
+        ++ne;
+    }
+    if (threadIdx.x == 0) {
+        accept_len[b] = a;
+        for (int j = ne; j < x + 1; ++j) em[j] = -1;
+    }
+}
+
 }  // namespace
 
 size_t accept_workspace(int batch, int n_pred, int vocab, int d) {
@@ -156,11 +318,45 @@ cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, co
     const int64_t nh = (int64_t)rows * d;
     group_mean_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hidden, rows, hg, d, h, keys);
     dim3 grid(ceil_div(vocab, kCols), ceil_div(rows, kRowsT));
-    logits_argmax_kernel<<<grid, kThreadsL, 0, st>>>(h, rows, w, d, vocab, keys);
+    logits_argmax_kernel<false><<<grid, kThreadsL, 0, st>>>(h, rows, w, d, vocab, keys, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     accept_finalize_kernel<<<batch, 128, n_pred * sizeof(int32_t), st>>>(keys, n_pred, drafts, x, verified,
                                                                          accept_len, emitted);
+    return cudaGetLastError();
+}
+
+}  // namespace vc
+
+namespace vc {
+
+size_t accept_sampled_workspace(int batch, int x, int vocab, int d) {
+    const size_t rt = (size_t)batch * (x + 1), rd = (size_t)batch * x;
+    return (rt + rd) * (size_t)d * sizeof(float) + (rt + rd) * (size_t)vocab * sizeof(float);
+}
+
+cudaError_t accept_sampled_launch(const float *target_hidden, const float *draft_hidden, int batch, int x, int hg,
+                                  const float *w, int d, int vocab, float tau, const int32_t *drafts,
+                                  const float *u, const float *v, int32_t *accept_len, int32_t *emitted, void *ws,
+                                  cudaStream_t st) {
+    const int rt = batch * (x + 1), rd = batch * x;
+    float *ht = reinterpret_cast<float *>(ws);
+    float *hd = ht + (size_t)rt * d;
+    float *lt = hd + (size_t)rd * d;
+    float *ld = lt + (size_t)rt * vocab;
+    group_mean_kernel<<<(unsigned)(((int64_t)rt * d + 255) / 256), 256, 0, st>>>(target_hidden, rt, hg, d, ht,
+                                                                                  nullptr);
+    logits_argmax_kernel<true><<<dim3(ceil_div(vocab, kCols), ceil_div(rt, kRowsT)), kThreadsL, 0, st>>>(
+        ht, rt, w, d, vocab, nullptr, lt);
+    if (rd > 0) {
+        group_mean_kernel<<<(unsigned)(((int64_t)rd * d + 255) / 256), 256, 0, st>>>(draft_hidden, rd, hg, d, hd,
+                                                                                      nullptr);
+        logits_argmax_kernel<true><<<dim3(ceil_div(vocab, kCols), ceil_div(rd, kRowsT)), kThreadsL, 0, st>>>(
+            hd, rd, w, d, vocab, nullptr, ld);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    accept_sample_kernel<<<batch, kSampThreads, 0, st>>>(lt, ld, vocab, tau, drafts, x, u, v, accept_len, emitted);
     return cudaGetLastError();
 }
 

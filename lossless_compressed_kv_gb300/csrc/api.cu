@@ -19,6 +19,11 @@ cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, 
                           int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
 size_t accept_workspace(int batch, int n_pred, int vocab, int d);
 size_t select_workspace(int batch, int max_seq_len);
+size_t accept_sampled_workspace(int batch, int x, int vocab, int d);
+cudaError_t accept_sampled_launch(const float *target_hidden, const float *draft_hidden, int batch, int x, int hg,
+                                  const float *w, int d, int vocab, float tau, const int32_t *drafts,
+                                  const float *u, const float *v, int32_t *accept_len, int32_t *emitted, void *ws,
+                                  cudaStream_t st);
 vc_status select_kept(const vc_paged_kv *full, const float *scores, int32_t score_stride,
                       const int32_t *kept_offsets, int32_t sink, int32_t recent, int32_t *kept_idx, void *ws,
                       size_t ws_bytes, int32_t *dev_status, cudaStream_t st);
@@ -134,6 +139,25 @@ vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t 
     if (!workspace || workspace_bytes < accept_workspace(batch, n_pred, vocab, d)) return VC_ERR_WORKSPACE;
     return from_cuda(accept_launch(hidden, batch, n_pred, hidden_group, lm_head, d, vocab, drafts, x, verified,
                                    accept_len, emitted, workspace, (cudaStream_t)stream));
+}
+
+size_t vc_accept_sampled_workspace_bytes(int32_t batch, int32_t x, int32_t vocab, int32_t d) {
+    if (batch < 0 || x < 0 || vocab < 1 || d < 1) return 0;
+    return accept_sampled_workspace(batch, x, vocab, d);
+}
+
+vc_status vc_accept_sampled(const float *target_hidden, const float *draft_hidden, int32_t batch, int32_t x,
+                            int32_t hidden_group, const float *lm_head, int32_t d, int32_t vocab, float temperature,
+                            const int32_t *drafts, const float *u, const float *v, int32_t *accept_len,
+                            int32_t *emitted, void *workspace, size_t workspace_bytes, vc_stream_t stream) {
+    if (!target_hidden || !lm_head || !accept_len || !emitted || !v || batch < 0 || x < 0 || hidden_group < 1 ||
+        d < 1 || vocab < 1 || !(temperature > 0.0f) || (x > 0 && (!draft_hidden || !drafts || !u)))
+        return VC_ERR_INVALID_ARG;
+    if (batch == 0) return VC_OK;
+    if (!workspace || workspace_bytes < accept_sampled_workspace(batch, x, vocab, d)) return VC_ERR_WORKSPACE;
+    return from_cuda(accept_sampled_launch(target_hidden, draft_hidden, batch, x, hidden_group, lm_head, d, vocab,
+                                           temperature, drafts, u, v, accept_len, emitted, workspace,
+                                           (cudaStream_t)stream));
 }
 
 vc_status vc_stage_async(void *dev_dst, const void *pinned_src, size_t bytes, vc_stream_t side,
