@@ -376,7 +376,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging", "70b_128k_drop4"])
+                    choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging", "70b_128k_drop4",
+                             "stagger_32req_3bit", "remote_prefix_8req_3bit"])
+    ap.add_argument("--cycles", type=int, default=2, help="measured cycles of the staggering workload")
     args = ap.parse_args()
     rank, ws = dist_init()
     if args.impl == "reference":
@@ -386,7 +388,8 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         {"mixed_32req_3bit": mixed_main, "toy_e2e": toy_main, "staging": staging_main,
-         "70b_128k_drop4": big_main}[args.workload](args)
+         "70b_128k_drop4": big_main, "stagger_32req_3bit": stagger_main,
+         "remote_prefix_8req_3bit": remote_main}[args.workload](args)
         return
     import torch
     import synth
@@ -802,6 +805,237 @@ def mixed_main(args):
             "algorithmic_GBps": (comp_bytes + full_bytes) / (t_mixed * 1e-3) / 1e9,
             "verify_tflops": flops / (t_mixed * 1e-3) / 1e12, "stage_GBps": 2 * stage_bytes / (t_stage * 1e-3) / 1e9,
             "stage_bytes": 2 * stage_bytes}
+    print(json.dumps(line), flush=True)
+
+
+def stagger_rig(w, device):
+    """The staggering workload: per layer, KV_full of every request (bf16,
+    N(0,1), room for blocks of up to max_x tokens, a request's pages
+    contiguous) in page-locked host memory and KV_comp of its context (every
+    token, w["bits"]) resident on the device; per-layer queries.  Returns
+    (engine, q_draft per layer [B][Hq][D], q_verify per layer [B][max_x][Hq][D])."""
+    import torch
+    import synth
+    import lossless_compressed_kv_gb300 as vc
+    from lossless_compressed_kv_gb300.stagger import StaggerEngine
+    B, hq, hkv, d, bits, L, mx = w["batch"], w["hq"], w["hkv"], w["d"], w["bits"], w["layers"], w["max_x"]
+    rng = np.random.default_rng(w["seed"])
+    ctx = rng.integers(w["ctx_lo"], w["ctx_hi"] + 1, size=B).astype(np.int64)
+    npg = (ctx + mx + 15) // 16
+    first = np.concatenate([[0], np.cumsum(npg)[:-1]]).astype(np.int64)
+    P = int(npg.sum())
+    pb = vc.page_bytes(hkv, d, 16)
+    tab = np.full((B, int(npg.max())), -1, np.int32)
+    for b in range(B):
+        tab[b, :npg[b]] = np.arange(first[b], first[b] + npg[b], dtype=np.int32)
+    cpg = (ctx + 15) // 16
+    ctab = np.full((B, int(cpg.max())), -1, np.int32)
+    c0 = np.concatenate([[0], np.cumsum(cpg)[:-1]])
+    for b in range(B):
+        ctab[b, :cpg[b]] = np.arange(c0[b], c0[b] + cpg[b], dtype=np.int32)
+    tabd, ctabd = torch.from_numpy(tab).to(device), torch.from_numpy(ctab).to(device)
+    lens_full = torch.from_numpy((ctx + mx).astype(np.int32)).to(device)
+    lens_comp = torch.from_numpy(ctx.astype(np.int32)).to(device)
+    offs, idx = synth.csr([np.arange(n, dtype=np.int32) for n in ctx])
+    offs, idx = torch.from_numpy(offs).to(device), torch.from_numpy(idx).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(w["seed"])
+    comps, hk, hv = [], [], []
+    for _ in range(L):
+        kp = torch.empty((P, pb // 2), dtype=torch.bfloat16, device=device)
+        vp = torch.empty_like(kp)
+        for s0 in range(0, P, 4096):
+            e = min(P, s0 + 4096)
+            kp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
+            vp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
+        full = vc.PagedKV(kp.view(torch.uint8), vp.view(torch.uint8), tabd, lens_full, hkv, d, 16)
+        comp = vc.PagedKV.allocate(int(cpg.sum()), hkv, d, bits, ctabd, lens_comp, device=device)
+        vc.compress(full, offs, idx, comp, int(ctx.max()))
+        comps.append(comp)
+        for src, dst in ((kp, hk), (vp, hv)):
+            h = torch.empty((P, pb), dtype=torch.uint8, pin_memory=True)
+            h.copy_(src.view(torch.uint8))
+            dst.append(h)
+        del kp, vp, full
+    torch.cuda.synchronize()
+    qd = [torch.randn((B, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
+    qv = [torch.randn((B, mx, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
+    eng = StaggerEngine(comps, hk, hv, first, ctx, hkv, d, hq, mx, device=device)
+    return eng, qd, qv
+
+
+def stagger_main(args):
+    """Staggering scheduler on the 32-request, 2-layer workload: lock step
+    (every request drafts x tokens, then all verify; one staging buffer for
+    all of KV_full) against the balanced staggered plan (two staging slots),
+    both at x = 25, and the staggered plan at the scheduler's smallest
+    stall-free horizon.  Each run: one warm-up cycle, then `--cycles`
+    measured cycles.  The scheduler's cost model is calibrated from timed
+    all-draft / all-verify / idle ticks and the measured link rate; its
+    predictions are printed beside the measurements."""
+    import torch
+    import synth
+    import lossless_compressed_kv_gb300 as vc
+    from lossless_compressed_kv_gb300.stagger import phase_schedule
+    w = dict(synth.WORKLOADS["stagger_32req_3bit"])
+    dev = torch.device("cuda")
+    t0 = time.perf_counter()
+    eng, qd, qv = stagger_rig(w, dev)
+    t_build = time.perf_counter() - t0
+    B, L, x, mx = w["batch"], w["layers"], w["x"], w["max_x"]
+    cycles = max(1, args.cycles)
+
+    def qvx(n):
+        return [q[:, :n].contiguous() for q in qv]
+
+    # cost model: ms per tick (all layers) with fixed roles
+    it = 5
+    t_idle = eng.time_roles(np.full(B, 2), x, it, qd, qvx(x))
+    t_draft = eng.time_roles(np.zeros(B), x, it, qd, qvx(x))
+    fulls = eng.device_full(x)
+    t_verify = eng.time_roles(np.ones(B), x, it, qd, qvx(x), fulls)
+    del fulls
+    torch.cuda.empty_cache()
+    cb = eng.comp_bytes().astype(np.float64)
+    fb = eng.pages(x).astype(np.float64)
+    d_ns = (t_draft - t_idle) * 1e6 * cb / cb.sum()
+    v_ns = (t_verify - t_idle) * 1e6 * fb / fb.sum()
+    tick_ns = t_idle * 1e6
+    sb = eng.stage_bytes(x)
+    P = x + 1
+
+    def one(phase, n_phases, xx, slots):
+        roles = phase_schedule(phase, n_phases, cycles + 1)
+        r = eng.run(roles, xx, slots, qd, qvx(xx), measure_from=n_phases)
+        r["cycle_ms"] = r["wall_ms"] / cycles
+        r["draft_tokens_per_s"] = r["draft_tokens"] / (r["wall_ms"] * 1e-3)
+        r["stall_ms_per_cycle"] = r["stall_ms"] / cycles
+        r["stage_ms_per_cycle"] = r["stage_ms"] / cycles
+        return r
+
+    lock = one(np.full(B, P - 1, np.int32), P, x, 1)
+    bw = lock["link_GBps"]                                       # bytes per ns
+    pred = lambda ph, n_ph, slots, s=sb: vc.stagger_simulate(  # noqa: E731
+        ph, n_ph, s, d_ns, v_ns, bw, n_slots=slots, n_layers=L, tick_ns=tick_ns)
+    lock["predicted"] = pred(np.full(B, P - 1, np.int32), P, 1)
+    ph, phb = vc.stagger_plan(sb, P)
+    stag = one(ph, P, x, 2)
+    stag["predicted"] = pred(ph, P, 2)
+    stag["max_phase_requests"] = int(np.bincount(ph, minlength=P).max())
+    sbm = eng.stage_bytes(mx)
+    xh, phh, predh = vc.stagger_horizon(sbm, d_ns, v_ns, bw, 1, mx, n_slots=2, n_layers=L, tick_ns=tick_ns)
+    hor = one(phh, xh + 1, xh, 2)
+    hor["predicted"] = pred(phh, xh + 1, 2, eng.stage_bytes(xh))
+    hor["x"] = xh
+    # the guide's per-token swap cost T_swap / L for the mean request at x
+    t_swap_ms = float(sb.mean()) / (bw * 1e6)
+    keep = ("cycle_ms", "stall_ms_per_cycle", "stage_ms_per_cycle", "overlap", "link_GBps", "max_tick_ms",
+            "mean_tick_ms", "draft_tokens_per_s", "peak_stage_bytes", "launches")
+    pk = ("cycle_ns", "stall_ns", "stage_ns", "overlap", "peak_stage_bytes")
+
+    def pick(r):
+        out = {k: r[k] for k in keep}
+        out["predicted"] = {k: r["predicted"][k] for k in pk}
+        for k in ("x", "max_phase_requests"):
+            if k in r:
+                out[k] = r[k]
+        return out
+
+    line = {"metric": "staggered verification across requests, layers and rounds: cycle time, staging stall "
+                      "and overlap (lock step vs balanced stagger vs scheduler horizon)",
+            "workload": "stagger_32req_3bit",
+            "config": {"batch": B, "ctx": "U[%d,%d]" % (w["ctx_lo"], w["ctx_hi"]), "layers": L, "q_heads": w["hq"],
+                       "kv_heads": w["hkv"], "head_dim": w["d"], "bits": w["bits"], "x": x, "cycles": cycles,
+                       "kv_full_host_GB": float(eng.stage_bytes(mx).sum()) / 1e9},
+            "cost_model_ms": {"idle_tick": t_idle, "all_draft_tick": t_draft, "all_verify_tick": t_verify,
+                              "link_GBps": bw},
+            "t_swap_mean_request_ms": t_swap_ms, "t_swap_per_drafted_token_ms": t_swap_ms / x,
+            "lock_step": pick(lock), "staggered": pick(stag), "staggered_at_horizon": pick(hor),
+            "build_s": t_build}
+    print(json.dumps(line), flush=True)
+
+
+def remote_rig(w, device):
+    """Remote prefix caching workload: per layer bf16 KV_full (prefix + x
+    tokens, N(0,1)) and its KV_comp (every prefix token, w["bits"]) on the
+    device, and their bytes in page-locked host memory (the store).  Returns
+    (engine, q_draft, q_verify [B][x], q_one [B][1], KV_full views with
+    seq_lens = prefix + 1 for the one-token baseline), all per layer."""
+    import torch
+    import synth
+    import lossless_compressed_kv_gb300 as vc
+    from lossless_compressed_kv_gb300.remote import RemotePrefixEngine
+    B, hq, hkv, d, bits, L, n, x = (w["batch"], w["hq"], w["hkv"], w["d"], w["bits"], w["layers"], w["ctx"],
+                                    w["x"])
+    npg, cpg = (n + x + 15) // 16, (n + 15) // 16
+    pb = vc.page_bytes(hkv, d, 16)
+    tabd = torch.arange(B * npg, dtype=torch.int32, device=device).view(B, npg).contiguous()
+    ctabd = torch.arange(B * cpg, dtype=torch.int32, device=device).view(B, cpg).contiguous()
+    full_lens = torch.full((B,), n + x, dtype=torch.int32, device=device)
+    one_lens = torch.full((B,), n + 1, dtype=torch.int32, device=device)
+    comp_lens = torch.full((B,), n, dtype=torch.int32, device=device)
+    offs, idx = synth.csr([np.arange(n, dtype=np.int32)] * B)
+    offs, idx = torch.from_numpy(offs).to(device), torch.from_numpy(idx).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(w["seed"])
+    fulls, comps, ones, fh, ch = [], [], [], [], []
+
+    def pinned(t):
+        h = torch.empty(t.numel(), dtype=torch.uint8, pin_memory=True)
+        h.copy_(t.view(-1))
+        return h
+
+    for _ in range(L):
+        kp = torch.empty((B * npg, pb // 2), dtype=torch.bfloat16, device=device)
+        vp = torch.empty_like(kp)
+        for s0 in range(0, B * npg, 4096):
+            e = min(B * npg, s0 + 4096)
+            kp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
+            vp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
+        full = vc.PagedKV(kp.view(torch.uint8), vp.view(torch.uint8), tabd, full_lens, hkv, d, 16)
+        comp = vc.PagedKV.allocate(B * cpg, hkv, d, bits, ctabd, comp_lens, device=device)
+        vc.compress(full, offs, idx, comp, n)
+        torch.cuda.synchronize()
+        fulls.append(full)
+        comps.append(comp)
+        ones.append(vc.PagedKV(full.k_pages, full.v_pages, tabd, one_lens, hkv, d, 16))
+        fh.append((pinned(full.k_pages), pinned(full.v_pages)))
+        ch.append((pinned(comp.k_pages), pinned(comp.v_pages)))
+    qd = [torch.randn((B, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
+    qv = [torch.randn((B, x, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
+    q1 = [torch.randn((B, 1, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
+    eng = RemotePrefixEngine(comps, fulls, ch, fh, hq, n + x)
+    return eng, qd, qv, q1, ones
+
+
+def remote_main(args):
+    """Remote prefix caching: time to the first drafted token and to the
+    first verified block when only KV_comp crosses the slow link (KV_full on
+    a fast link), against one-token decoding after KV_full crossed the slow
+    link; the same number of tokens (every draft accepted) for both."""
+    import torch
+    import synth
+    w = dict(synth.WORKLOADS["remote_prefix_8req_3bit"])
+    dev = torch.device("cuda")
+    eng, qd, qv, q1, ones = remote_rig(w, dev)
+    rate, chunk = w["slow_GBps"], int(w["chunk_MB"]) << 20
+    # warm-up (module loading, first launches) on an unthrottled link
+    eng.run_vericache(qd, qv, 1, 1000.0, chunk)
+    eng.run_full_kv_remote(q1, ones, 2, 1000.0, chunk)
+    vr = eng.run_vericache(qd, qv, w["rounds"], rate, chunk)
+    steps = w["rounds"] * (w["x"] + 1)
+    br = eng.run_full_kv_remote(q1, ones, steps, rate, chunk)
+    line = {"metric": "remote prefix caching: startup and time to N tokens, KV_comp over a slow link vs KV_full "
+                      "over it", "workload": "remote_prefix_8req_3bit",
+            "config": {k: w[k] for k in ("batch", "hq", "hkv", "d", "ctx", "layers", "bits", "x", "rounds",
+                                         "slow_GBps", "chunk_MB")},
+            "slow_link_bytes": {"vericache_kv_comp": vr["slow_bytes"], "baseline_kv_full": vr["fast_bytes"]},
+            "compression_ratio": vr["fast_bytes"] / vr["slow_bytes"],
+            "vericache": vr, "full_kv_remote": br,
+            "startup_speedup": br["first_token_ms"] / vr["first_draft_ms"],
+            "time_to_tokens_speedup": br["total_ms"] / vr["total_ms"],
+            "note": "attention work of the schedule only; token counts assume every draft accepted; both links "
+                    "share this machine's host->device path"}
     print(json.dumps(line), flush=True)
 
 

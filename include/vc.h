@@ -301,13 +301,43 @@ VC_API vc_status vc_stage_async(void *dev_dst, const void *pinned_src, size_t by
                          vc_stream_t side, vc_event_t done);
 
 /*
+ * A slower link emulated on one machine (remote prefix caching: "VeriCache:
+ * Making Lossy KV Compression Exact", the two serving settings -- the
+ * compressed cache of a stored prefix is sent to the serving GPU, the full
+ * cache stays reachable for verification; study notes "VeriCache: Turning
+ * Lossy KV Cache into Lossless LLM Inference", case 3 -- KV_comp over the slow
+ * link to the drafter, KV_full over a fast link to the verifier).
+ *  vc_link_clock         writes the device global timer (ns) to *origin_ns
+ *                        (device int64) on `stream`: the link's time origin.
+ *  vc_stage_paced_async  the copy of vc_stage_async in chunks of chunk_bytes;
+ *                        chunk k (bytes [k c, min((k+1) c, bytes))) is issued on
+ *                        `side` only after the timer has reached
+ *                        *origin_ns + (link_offset_bytes + end of chunk k) /
+ *                        bytes_per_ns, so data arrive no faster than a link of
+ *                        bytes_per_ns that had already carried
+ *                        link_offset_bytes since the origin.  The origin must be
+ *                        written (vc_link_clock, ordered before on `side`)
+ *                        first.  VC_ERR_INVALID_ARG for a null pointer, chunk 0,
+ *                        a rate <= 0 or a span over 60 s of link time;
+ *                        VC_ERR_STAGING when src is not page-locked.  Each wait
+ *                        is a one-thread kernel that ends at its deadline (and
+ *                        in any case within 60 s).
+ */
+VC_API vc_status vc_link_clock(int64_t *origin_ns, vc_stream_t stream);
+VC_API vc_status vc_stage_paced_async(void *dev_dst, const void *pinned_src, size_t bytes, size_t chunk_bytes,
+                                      double bytes_per_ns, const int64_t *origin_ns, size_t link_offset_bytes,
+                                      vc_stream_t side, vc_event_t done);
+
+/*
  * vc_mixed_attn -- one launch in which requests with role[b] == 0 run the
  * draft attention over `comp` and requests with role[b] == 1 run the
  * verification attention of an n_q block over `full` (cross-resource
  * staggering: some requests draft while others verify).  Arguments are
  * those of vc_draft_attn / vc_verify_attn; both caches describe the same
  * batch; role is device int32 [batch].  Outputs of a request are written
- * only to the buffer of its role.  Workspace: vc_mixed_workspace_bytes.
+ * only to the buffer of its role; a request whose role is neither 0 nor 1 is
+ * skipped (idle this launch: its block-table rows in either cache are not
+ * read).  Workspace: vc_mixed_workspace_bytes.
  */
 VC_API size_t vc_mixed_workspace_bytes(const vc_paged_kv *comp, const vc_paged_kv *full, int32_t n_q,
                                 int32_t num_q_heads, int32_t max_seq_len);
@@ -316,6 +346,78 @@ VC_API vc_status vc_mixed_attn(const int32_t *role, const void *q_draft, const v
                         const vc_paged_kv *full, float *out_verify, int32_t num_q_heads,
                         float softmax_scale, int32_t max_seq_len, void *workspace,
                         size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * Staggering scheduler (host code; no device pointers, no CUDA calls).
+ *
+ * "VeriCache: Making Lossy KV Compression Exact", "Verifying Without Giving
+ * Back the Speedup" and Figure 2 (verifications spread over time so one
+ * request's full-cache transfer overlaps the others' drafting); study notes
+ * "VeriCache: Turning Lossy KV Cache into Lossless LLM Inference", case 2
+ * (stagger who verifies so few full caches cross the link at once);
+ * "VeriCache Guide", "The Amortized Drafting Horizon" (swap cost per token
+ * T_swap / L) and "Best Practice 1" (size the horizon to hide the swap).
+ *
+ * Model: request r cycles through P = x + 1 ticks, verifying at the ticks t
+ * with t mod P == phase[r] and drafting one token at every other tick.  A tick
+ * runs all n_layers layers; its compute time is tick_ns plus, over its
+ * drafting requests, draft_ns[r] and, over its verifying requests,
+ * verify_ns[r] (each for all layers, split evenly over the layers).  The
+ * verifying requests of a tick form one staging job: their stage_bytes
+ * (KV_full, all layers) cross the link at link_bytes_per_ns, layer by layer,
+ * into one of n_slots staging buffers.  Jobs run in tick order; a job starts
+ * when the previous one is done and its slot's previous job's tick has ended.
+ * Layer l of a verifying tick waits for layer l of its job; waiting is stall.
+ */
+typedef struct {
+    int32_t n_requests;
+    const int64_t *stage_bytes; /* host [n]: KV_full bytes staged per verification   */
+    const double *draft_ns;     /* host [n]: one draft step, all layers (ns)          */
+    const double *verify_ns;    /* host [n]: one verification, all layers (ns)        */
+    double tick_ns;             /* fixed cost of a tick (launch latencies), >= 0      */
+    double link_bytes_per_ns;   /* staging bandwidth, > 0                             */
+    int32_t n_slots;            /* staging buffers, >= 1                              */
+    int32_t n_layers;           /* >= 1                                               */
+} vc_stagger_model;
+
+typedef struct {             /* steady state: the last of the simulated cycles */
+    double cycle_ns;         /* wall time of one cycle (P ticks)                  */
+    double compute_ns;       /* sum of the cycle's tick compute times             */
+    double stall_ns;         /* time ticks waited for staged layers               */
+    double stage_ns;         /* link time of the cycle's staged bytes (T_swap sum) */
+    double overlap;          /* 1 - stall / stage, in [0, 1] (1 when nothing staged) */
+    int64_t peak_stage_bytes;       /* n_slots x the largest job                   */
+    int64_t draft_tokens_per_cycle; /* n_requests x (P - 1)                        */
+} vc_stagger_result;
+
+/*
+ * vc_stagger_plan -- assign each of n requests a phase in [0, n_phases).
+ * (1) Longest processing time first into G = min(n, n_phases) groups:
+ * requests in decreasing stage_bytes order (ties: lower index first), each to
+ * the group with the fewest bytes so far (ties: lower group).  (2) Groups in
+ * decreasing byte order (ties: lower group), interleaved largest, smallest,
+ * second largest, ...  (3) The k-th group of that sequence verifies at phase
+ * floor(k * n_phases / G), so groups are evenly spaced over the cycle and a
+ * large staging job follows a small one.  phase: host int32 [n];
+ * phase_bytes: host int64 [n_phases] or NULL (bytes verified per phase).
+ * VC_ERR_INVALID_ARG on a negative size or a null array.
+ */
+VC_API vc_status vc_stagger_plan(const int64_t *stage_bytes, int32_t n, int32_t n_phases, int32_t *phase,
+                                 int64_t *phase_bytes);
+/*
+ * vc_stagger_simulate -- run the model above for n_cycles cycles of n_phases
+ * ticks from a cold start (staging begins at time 0) and report the last
+ * cycle.  VC_ERR_INVALID_ARG on a bad model or a phase out of range.
+ */
+VC_API vc_status vc_stagger_simulate(const vc_stagger_model *m, int32_t n_phases, const int32_t *phase,
+                                     int32_t n_cycles, vc_stagger_result *out);
+/*
+ * vc_stagger_horizon -- the smallest draft horizon x in [x_lo, x_hi] whose
+ * balanced plan (P = x + 1 phases) has no steady-state stall, else x_hi; writes
+ * x, its plan (phase: host int32 [n]) and its simulated result.
+ */
+VC_API vc_status vc_stagger_horizon(const vc_stagger_model *m, int32_t x_lo, int32_t x_hi, int32_t n_cycles,
+                                    int32_t *x_out, int32_t *phase, vc_stagger_result *out);
 
 /*
  * Decoder-layer operations for the end-to-end greedy loop (prefill, draft

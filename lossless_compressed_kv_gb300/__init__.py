@@ -11,7 +11,11 @@ follow): ``compress`` (KV_full -> KV_comp gather / 2-3-4-bit quantisation),
 ``draft_attn`` (decode attention over KV_comp), ``verify_attn`` (causal
 block attention over KV_full), ``accept`` (argmax + longest matching prefix
 + correction / bonus), ``stage_async`` (pinned host -> device copy on a side
-stream) and ``mixed_attn`` (draft and verify requests in one launch).
+stream) and ``mixed_attn`` (draft and verify requests in one launch); the
+staggering scheduler (``stagger_plan`` / ``stagger_simulate`` /
+``stagger_horizon``, host code in the library; engine in ``stagger.py``) and
+the paced copy of an emulated slow link (``link_clock`` /
+``stage_paced_async``; remote-prefix engine in ``remote.py``).
 """
 from __future__ import annotations
 
@@ -40,6 +44,18 @@ class PagedKVStruct(C.Structure):
                 ("max_blocks", C.c_int32), ("fmt", KVFormat)]
 
 
+class StaggerModel(C.Structure):
+    _fields_ = [("n_requests", C.c_int32), ("stage_bytes", C.c_void_p), ("draft_ns", C.c_void_p),
+                ("verify_ns", C.c_void_p), ("tick_ns", C.c_double), ("link_bytes_per_ns", C.c_double),
+                ("n_slots", C.c_int32), ("n_layers", C.c_int32)]
+
+
+class StaggerResult(C.Structure):
+    _fields_ = [("cycle_ns", C.c_double), ("compute_ns", C.c_double), ("stall_ns", C.c_double),
+                ("stage_ns", C.c_double), ("overlap", C.c_double), ("peak_stage_bytes", C.c_int64),
+                ("draft_tokens_per_cycle", C.c_int64)]
+
+
 _P = C.c_void_p
 _lib = C.CDLL(LIB_PATH)
 _SIG = {
@@ -62,6 +78,8 @@ _SIG = {
     "vc_accept": (C.c_int, [_P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
                             _P, _P, C.c_size_t, _P]),
     "vc_stage_async": (C.c_int, [_P, _P, C.c_size_t, _P, _P]),
+    "vc_link_clock": (C.c_int, [_P, _P]),
+    "vc_stage_paced_async": (C.c_int, [_P, _P, C.c_size_t, C.c_size_t, C.c_double, _P, C.c_size_t, _P, _P]),
     "vc_mixed_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.POINTER(PagedKVStruct), C.c_int32,
                                               C.c_int32, C.c_int32]),
     "vc_mixed_attn": (C.c_int, [_P, _P, C.POINTER(PagedKVStruct), _P, _P, C.c_int32, C.POINTER(PagedKVStruct), _P,
@@ -74,6 +92,10 @@ _SIG = {
                                    _P]),
     "vc_draft_attn_static": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32, _P, _P]),
     "vc_static_scratch_bytes": (C.c_size_t, []),
+    "vc_stagger_plan": (C.c_int, [_P, C.c_int32, C.c_int32, _P, _P]),
+    "vc_stagger_simulate": (C.c_int, [C.POINTER(StaggerModel), C.c_int32, _P, C.c_int32, C.POINTER(StaggerResult)]),
+    "vc_stagger_horizon": (C.c_int, [C.POINTER(StaggerModel), C.c_int32, C.c_int32, C.c_int32,
+                                     C.POINTER(C.c_int32), _P, C.POINTER(StaggerResult)]),
     "vc_status_string": (C.c_char_p, [C.c_int]),
     "vc_version": (C.c_char_p, []),
 }
@@ -256,9 +278,30 @@ def accept_sampled(target_hidden, draft_hidden, lm_head, drafts, u, v, temperatu
 
 
 def stage_async(dst, pinned_src, nbytes: int, side_stream, done_event=None):
-    ev = None if done_event is None else C.c_void_p(done_event.cuda_event)
+    """vc_stage_async; done_event (a torch.cuda.Event, created lazily by
+    torch) is recorded on side_stream after the copy."""
     _check(_lib.vc_stage_async(C.c_void_p(dst.data_ptr()), C.c_void_p(pinned_src.data_ptr()), int(nbytes),
-                               C.c_void_p(side_stream.cuda_stream), ev), "vc_stage_async")
+                               C.c_void_p(side_stream.cuda_stream), None), "vc_stage_async")
+    if done_event is not None:
+        done_event.record(side_stream)
+
+
+def link_clock(origin, stream=None):
+    """Write the device timer (ns) into origin (int64 device tensor, 1 element)."""
+    if origin.dtype != torch.int64:
+        raise ValueError("origin must be an int64 device tensor")
+    _check(_lib.vc_link_clock(_ptr(origin), _stream(stream)), "vc_link_clock")
+
+
+def stage_paced_async(dst, pinned_src, nbytes: int, chunk_bytes: int, bytes_per_ns: float, origin,
+                      link_offset_bytes: int, side_stream, done_event=None):
+    """vc_stage_async paced as a link of bytes_per_ns that has carried
+    link_offset_bytes since the origin written by link_clock."""
+    _check(_lib.vc_stage_paced_async(C.c_void_p(dst.data_ptr()), C.c_void_p(pinned_src.data_ptr()), int(nbytes),
+                                     int(chunk_bytes), float(bytes_per_ns), _ptr(origin), int(link_offset_bytes),
+                                     C.c_void_p(side_stream.cuda_stream), None), "vc_stage_paced_async")
+    if done_event is not None:
+        done_event.record(side_stream)
 
 
 def mixed_workspace_bytes(comp: PagedKV, full: PagedKV, n_q: int, num_q_heads: int, max_seq_len: int) -> int:
@@ -274,6 +317,69 @@ def mixed_attn(role, q_draft, comp: PagedKV, out_draft, q_verify, full: PagedKV,
                               float(softmax_scale), int(max_seq_len), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
            "vc_mixed_attn")
+
+
+# ---------------------------------------------------------------------------
+# staggering scheduler (host code in the library; numpy in, numpy / dict out)
+# ---------------------------------------------------------------------------
+
+def _np_ptr(a):
+    return C.c_void_p(a.ctypes.data)
+
+
+def stagger_plan(stage_bytes, n_phases: int):
+    """Balanced verify phases (vc_stagger_plan): returns (phase [n] int32,
+    phase_bytes [n_phases] int64)."""
+    import numpy as np
+    sb = np.ascontiguousarray(stage_bytes, dtype=np.int64)
+    ph = np.zeros(max(1, len(sb)), np.int32)
+    pb = np.zeros(n_phases, np.int64)
+    _check(_lib.vc_stagger_plan(_np_ptr(sb), len(sb), int(n_phases), _np_ptr(ph), _np_ptr(pb)), "vc_stagger_plan")
+    return ph[:len(sb)], pb
+
+
+class _Model:
+    """Keeps the numpy arrays a vc_stagger_model points to alive."""
+
+    def __init__(self, stage_bytes, draft_ns, verify_ns, link_bytes_per_ns, n_slots, n_layers, tick_ns):
+        import numpy as np
+        self.sb = np.ascontiguousarray(stage_bytes, dtype=np.int64)
+        self.d = np.ascontiguousarray(draft_ns, dtype=np.float64)
+        self.v = np.ascontiguousarray(verify_ns, dtype=np.float64)
+        if not (len(self.sb) == len(self.d) == len(self.v)):
+            raise ValueError("stage_bytes, draft_ns and verify_ns differ in length")
+        self.s = StaggerModel(len(self.sb), self.sb.ctypes.data, self.d.ctypes.data, self.v.ctypes.data,
+                              float(tick_ns), float(link_bytes_per_ns), int(n_slots), int(n_layers))
+
+
+def _result(r: StaggerResult) -> dict:
+    return {f: getattr(r, f) for f, _ in StaggerResult._fields_}
+
+
+def stagger_simulate(phase, n_phases: int, stage_bytes, draft_ns, verify_ns, link_bytes_per_ns: float,
+                     n_slots: int = 2, n_layers: int = 1, tick_ns: float = 0.0, n_cycles: int = 4) -> dict:
+    """Steady-state cycle of a phase plan under the staging model (vc_stagger_simulate)."""
+    import numpy as np
+    m = _Model(stage_bytes, draft_ns, verify_ns, link_bytes_per_ns, n_slots, n_layers, tick_ns)
+    ph = np.ascontiguousarray(phase, dtype=np.int32)
+    r = StaggerResult()
+    _check(_lib.vc_stagger_simulate(C.byref(m.s), int(n_phases), _np_ptr(ph), int(n_cycles), C.byref(r)),
+           "vc_stagger_simulate")
+    return _result(r)
+
+
+def stagger_horizon(stage_bytes, draft_ns, verify_ns, link_bytes_per_ns: float, x_lo: int, x_hi: int,
+                    n_slots: int = 2, n_layers: int = 1, tick_ns: float = 0.0, n_cycles: int = 4):
+    """Smallest stall-free draft horizon in [x_lo, x_hi] (vc_stagger_horizon):
+    returns (x, phase [n] int32, result dict)."""
+    import numpy as np
+    m = _Model(stage_bytes, draft_ns, verify_ns, link_bytes_per_ns, n_slots, n_layers, tick_ns)
+    ph = np.zeros(max(1, len(m.sb)), np.int32)
+    x = C.c_int32(0)
+    r = StaggerResult()
+    _check(_lib.vc_stagger_horizon(C.byref(m.s), int(x_lo), int(x_hi), int(n_cycles), C.byref(x), _np_ptr(ph),
+                                   C.byref(r)), "vc_stagger_horizon")
+    return int(x.value), ph[:len(m.sb)], _result(r)
 
 
 # ---------------------------------------------------------------------------

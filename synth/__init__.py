@@ -203,6 +203,21 @@ WORKLOADS = {
              "requests verify x=25 over KV_full staged from pinned host memory",
         batch=32, hq=32, hkv=8, d=128, ctx_lo=8192, ctx_hi=65536, outliers=0,
         outlier_scale=1.0, bits=3, x=25, seed=4),
+    "stagger_32req_3bit": dict(
+        desc="staggering scheduler across requests, layers and rounds: 32 requests, "
+             "context U[8192,65536], 2 attention layers of 32q/8kv, head_dim 128, "
+             "3-bit group-32 KV_comp resident, bf16 KV_full in page-locked host "
+             "memory staged for each verification; x=25 (block of 25 queries), "
+             "room for blocks up to 64",
+        batch=32, hq=32, hkv=8, d=128, ctx_lo=8192, ctx_hi=65536, layers=2, bits=3, x=25,
+        max_x=64, seed=6),
+    "remote_prefix_8req_3bit": dict(
+        desc="remote prefix caching on one box: 8 stored prefixes of 32768 tokens, 2 "
+             "attention layers of 32q/8kv, head_dim 128; the 3-bit KV_comp crosses a "
+             "slow link paced at 25 GB/s, the bf16 KV_full a fast link (plain staging); "
+             "x=25, 4 rounds; baseline: KV_full over the slow link, one-token decoding",
+        batch=8, hq=32, hkv=8, d=128, ctx=32768, layers=2, bits=3, x=25, rounds=4,
+        slow_GBps=25.0, chunk_MB=4, seed=7),
     "toy_e2e": dict(
         desc="2-layer decoder d_model 1024, 8q/2kv heads, head_dim 128, SwiGLU 4096, "
              "vocab 32000, weights N(0,0.02); batch 4, prompt 16384; 4-bit KV_comp; "

@@ -60,6 +60,8 @@ def test_page_sizes_follow_the_layout(vc):
 def test_struct_layout_matches_c(vc):
     assert C.sizeof(vc.KVFormat) == 12
     assert C.sizeof(vc.PagedKVStruct) == 64
+    assert C.sizeof(vc.StaggerModel) == 56      # static_assert'ed in the library too
+    assert C.sizeof(vc.StaggerResult) == 56
 
 
 def test_host_side_argument_errors(vc):
