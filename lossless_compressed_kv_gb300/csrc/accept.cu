@@ -37,6 +37,7 @@ __device__ inline unsigned long long argmax_key(float v, int id) {
 // h[r][k] = (sum_j hidden[r][j][k], in increasing j) / hg, once per row.
 __global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, float *h,
                                   unsigned long long *keys) {
+    pdl_begin();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (keys && i < rows) keys[i] = 0ull;
     if (i >= (int64_t)rows * d) return;
@@ -52,6 +53,7 @@ template <bool STORE>
 __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
                                                                  int vocab, unsigned long long *keys,
                                                                  float *logits) {
+    pdl_begin();
     __shared__ __align__(16) float hs[kKT][kRowsT];  // k-major: one k's 16 row values contiguous
     const int r0 = blockIdx.y * kRowsT;
     const int v0 = blockIdx.x * kCols + threadIdx.x * kColsT;
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
 
 __global__ void accept_finalize_kernel(const unsigned long long *keys, int n_pred, const int32_t *drafts, int x,
                                        int32_t *verified, int32_t *accept_len, int32_t *emitted) {
+    pdl_begin();
     extern __shared__ int32_t ver[];  // [n_pred]
     const int b = blockIdx.x;
     for (int i = threadIdx.x; i < n_pred; i += blockDim.x) {
@@ -259,6 +262,7 @@ __global__ void __launch_bounds__(kSampThreads) accept_sample_kernel(const float
                                                                     float tau, const int32_t *drafts, int x,
                                                                     const float *u, const float *v,
                                                                     int32_t *accept_len, int32_t *emitted) {
+    pdl_begin();
     __shared__ float red[34];
     __shared__ float scan[kSampThreads];
     __shared__ int pick[2];
@@ -316,13 +320,13 @@ cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, co
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(ws);
     float *h = reinterpret_cast<float *>(keys + rows);
     const int64_t nh = (int64_t)rows * d;
-    group_mean_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hidden, rows, hg, d, h, keys);
+    launch_pdl(group_mean_kernel, (unsigned)((nh + 255) / 256), 256, 0, st, hidden, rows, hg, d, h, keys);
     dim3 grid(ceil_div(vocab, kCols), ceil_div(rows, kRowsT));
-    logits_argmax_kernel<false><<<grid, kThreadsL, 0, st>>>(h, rows, w, d, vocab, keys, nullptr);
+    launch_pdl(logits_argmax_kernel<false>, grid, kThreadsL, 0, st, h, rows, w, d, vocab, keys, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    accept_finalize_kernel<<<batch, 128, n_pred * sizeof(int32_t), st>>>(keys, n_pred, drafts, x, verified,
-                                                                         accept_len, emitted);
+    launch_pdl(accept_finalize_kernel, batch, 128, n_pred * sizeof(int32_t), st, keys, n_pred, drafts, x, verified,
+               accept_len, emitted);
     return cudaGetLastError();
 }
 
@@ -344,19 +348,20 @@ cudaError_t accept_sampled_launch(const float *target_hidden, const float *draft
     float *hd = ht + (size_t)rt * d;
     float *lt = hd + (size_t)rd * d;
     float *ld = lt + (size_t)rt * vocab;
-    group_mean_kernel<<<(unsigned)(((int64_t)rt * d + 255) / 256), 256, 0, st>>>(target_hidden, rt, hg, d, ht,
-                                                                                  nullptr);
-    logits_argmax_kernel<true><<<dim3(ceil_div(vocab, kCols), ceil_div(rt, kRowsT)), kThreadsL, 0, st>>>(
-        ht, rt, w, d, vocab, nullptr, lt);
+    launch_pdl(group_mean_kernel, (unsigned)(((int64_t)rt * d + 255) / 256), 256, 0, st, target_hidden, rt, hg, d,
+               ht, nullptr);
+    launch_pdl(logits_argmax_kernel<true>, dim3(ceil_div(vocab, kCols), ceil_div(rt, kRowsT)), kThreadsL, 0, st,
+               ht, rt, w, d, vocab, nullptr, lt);
     if (rd > 0) {
-        group_mean_kernel<<<(unsigned)(((int64_t)rd * d + 255) / 256), 256, 0, st>>>(draft_hidden, rd, hg, d, hd,
-                                                                                      nullptr);
-        logits_argmax_kernel<true><<<dim3(ceil_div(vocab, kCols), ceil_div(rd, kRowsT)), kThreadsL, 0, st>>>(
-            hd, rd, w, d, vocab, nullptr, ld);
+        launch_pdl(group_mean_kernel, (unsigned)(((int64_t)rd * d + 255) / 256), 256, 0, st, draft_hidden, rd, hg,
+                   d, hd, nullptr);
+        launch_pdl(logits_argmax_kernel<true>, dim3(ceil_div(vocab, kCols), ceil_div(rd, kRowsT)), kThreadsL, 0,
+                   st, hd, rd, w, d, vocab, nullptr, ld);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    accept_sample_kernel<<<batch, kSampThreads, 0, st>>>(lt, ld, vocab, tau, drafts, x, u, v, accept_len, emitted);
+    launch_pdl(accept_sample_kernel, batch, kSampThreads, 0, st, lt, ld, vocab, tau, drafts, x, u, v, accept_len,
+               emitted);
     return cudaGetLastError();
 }
 

@@ -112,6 +112,7 @@ constexpr int kTokenPathMax = 32;
 
 template <int BITS, int D>
 __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(CompressArgs a) {
+    pdl_begin();
     constexpr int HB = 2 * D * (BITS + 1);    // head block bytes
     constexpr int CR = kPage * D * BITS / 8;  // code region bytes
     constexpr int G = D / kGroup, CPL = D / 32, LPG = kGroup / CPL;
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
 // AND / OR reductions (one thread per word, in program order).
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32) compress_token_kernel(CompressArgs a) {
+    pdl_begin();
     constexpr int CPL = D / 32, LPG = kGroup / CPL, G = D / kGroup;
     constexpr int HB = 2 * D * (BITS + 1), CR = kPage * D * BITS / 8, RW = D * BITS / 32;  // K row words
     __shared__ uint32_t krow[kWarps][RW];
@@ -282,6 +284,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_token_kernel(CompressArg
 // bf16 token drop: one warp per (kept entry, kv head) copies the row.
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) compress_bf16_kernel(CompressArgs a) {
+    pdl_begin();
     constexpr int CPL = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
@@ -319,14 +322,14 @@ template <int BITS, int D>
 cudaError_t launch_bd(const CompressArgs &a, int batch, int max_kept, cudaStream_t st) {
     if constexpr (BITS == 16) {
         dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
-        compress_bf16_kernel<D><<<grid, kWarps * 32, 0, st>>>(a);
+        launch_pdl(compress_bf16_kernel<D>, grid, kWarps * 32, 0, st, a);
     } else if (max_kept <= kTokenPathMax) {
         dim3 grid(ceil_div(max_kept * a.hkv, kWarps), batch);
-        compress_token_kernel<BITS, D><<<grid, kWarps * 32, 0, st>>>(a);
+        launch_pdl(compress_token_kernel<BITS, D>, grid, kWarps * 32, 0, st, a);
     } else {
         // a range of max_kept slots starting anywhere touches at most this many pages
         dim3 grid(ceil_div(max_kept, kPage) + 1, a.hkv, batch);
-        compress_page_kernel<BITS, D><<<grid, kPageWarps * 32, 0, st>>>(a);
+        launch_pdl(compress_page_kernel<BITS, D>, grid, kPageWarps * 32, 0, st, a);
     }
     return cudaGetLastError();
 }

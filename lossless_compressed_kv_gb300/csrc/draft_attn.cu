@@ -42,12 +42,14 @@ constexpr int kMinCtas = 4;
 
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(DraftArgs a) {
+    pdl_begin();
     extern __shared__ __align__(128) uint8_t smem[];
     draft::draft_block<BITS, D, kWarps>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }
 
 template <int D>
 __global__ void draft_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, float *out) {
+    pdl_begin();
     const int64_t row = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;  // b * Hq + h
     draft::reduce_row<D>(ws_o, ws_ml, n_splits, row, out, threadIdx.x, blockDim.x);
 }
@@ -118,7 +120,7 @@ cudaError_t launch(const DraftArgs &a, int batch, cudaStream_t st) {
     using C = Cfg<BITS, D, kWarps>;
     occupancy<BITS, D>();  // sets the shared-memory attribute once
     dim3 grid(a.n_splits, a.hkv, batch);
-    draft_kernel<BITS, D><<<grid, kWarps * 32, C::SMEM, st>>>(a);
+    launch_pdl(draft_kernel<BITS, D>, grid, kWarps * 32, C::SMEM, st, a);
     return cudaGetLastError();
 }
 
@@ -168,9 +170,9 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     if (e != cudaSuccess) return e;
     dim3 rg(hq, c.batch);
     if (d == 64)
-        draft_reduce_kernel<64><<<rg, 64, 0, st>>>(a.ws_o, a.ws_ml, p.n_splits, out);
+        launch_pdl(draft_reduce_kernel<64>, rg, 64, 0, st, a.ws_o, a.ws_ml, p.n_splits, out);
     else
-        draft_reduce_kernel<128><<<rg, 128, 0, st>>>(a.ws_o, a.ws_ml, p.n_splits, out);
+        launch_pdl(draft_reduce_kernel<128>, rg, 128, 0, st, a.ws_o, a.ws_ml, p.n_splits, out);
     return cudaGetLastError();
 }
 

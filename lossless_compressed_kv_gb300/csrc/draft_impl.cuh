@@ -3,6 +3,8 @@
 // comp_layout.cuh for the code placement this body reads.
 #pragma once
 
+#include <type_traits>
+
 #include "vc_internal.cuh"
 
 namespace vc {
@@ -454,71 +456,98 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         constexpr float kVhi = VReg<BITS, D>::VHI == 4 ? 0.0625f : 0.25f;
         const uint32_t vhi_scale = pack_f16(kVhi, kVhi);
 
-        // One page: k = page index of the warp, st = its ring stage (a
-        // compile-time constant in the unrolled driver below).
-        auto page = [&](int k, int st, uint32_t parity) -> bool {
-            if (!mbar_wait(&bars[st], parity, a.status)) return false;
-            const uint8_t *kb = ring + st * C::STAGE;
-            uint8_t *vb = ring + st * C::STAGE + C::HB;
-            const int pg = p0 + warp + NW * k;
-            // slots >= nvalid are past the end; a bad page id (reported at
-            // issue time, nothing copied) masks the whole stage
-            const int nvalid = sflag[st] ? len - pg * kPage : 0;
+        // NPG (1 or 2) consecutive pages of the warp: k = the first page's
+        // index, its ring stage S0 and S0 + 1 compile-time constants of the
+        // unrolled driver below.  Two pages share the query-fragment loads,
+        // the rescale check and the copy bookkeeping, and give the scheduler
+        // two independent MMA chains.
+        auto body = [&](int k, auto s0c, uint32_t parity, auto npc) -> bool {
+            constexpr int S0 = decltype(s0c)::value;
+            constexpr int NPG = decltype(npc)::value;
+            int nvalid[NPG];
+#pragma unroll
+            for (int i = 0; i < NPG; ++i) {
+                if (!mbar_wait(&bars[S0 + i], parity, a.status)) return false;
+                // slots >= nvalid are past the end; a bad page id (reported
+                // at issue time, nothing copied) masks the whole stage
+                const int pg = p0 + warp + NW * (k + i);
+                nvalid[i] = sflag[S0 + i] ? len - pg * kPage : 0;
+            }
 
-            // ---- shared-memory reads of the page (K rows, V strings, parameters) ----
-            KRow<BITS, D> r0, r1;  // tokens g (rows g) and g+8 (rows g+8)
-            r0.load(kb + g * (D * BITS / 8), t);
-            r1.load(kb + (g + 8) * (D * BITS / 8), t);
-            const __half *ksc = reinterpret_cast<const __half *>(kb + C::CR);
-            const __half *kzr = ksc + kPage * C::NG;
-            float sc0[C::NG], sc1[C::NG];
-            load_halves<C::NG>(ksc + g * C::NG, sc0);
-            load_halves<C::NG>(ksc + (g + 8) * C::NG, sc1);
-            uint32_t kza0 = 0u, kza1 = 0u;
-            if (zuse) {
-                kza0 = *reinterpret_cast<const uint32_t *>(kzr + g * C::NG + 2 * zp);
-                kza1 = *reinterpret_cast<const uint32_t *>(kzr + (g + 8) * C::NG + 2 * zp);
+            // ---- shared-memory reads of the pages' K rows and parameters ----
+            KRow<BITS, D> r0[NPG], r1[NPG];  // tokens g (rows g) and g+8 (rows g+8)
+            float sc0[NPG][C::NG], sc1[NPG][C::NG];
+            uint32_t kza0[NPG], kza1[NPG];
+#pragma unroll
+            for (int i = 0; i < NPG; ++i) {
+                const uint8_t *kb = ring + (S0 + i) * C::STAGE;
+                r0[i].load(kb + g * (D * BITS / 8), t);
+                r1[i].load(kb + (g + 8) * (D * BITS / 8), t);
+                const __half *ksc = reinterpret_cast<const __half *>(kb + C::CR);
+                const __half *kzr = ksc + kPage * C::NG;
+                load_halves<C::NG>(ksc + g * C::NG, sc0[i]);
+                load_halves<C::NG>(ksc + (g + 8) * C::NG, sc1[i]);
+                kza0[i] = kza1[i] = 0u;
+                if (zuse) {
+                    kza0[i] = *reinterpret_cast<const uint32_t *>(kzr + g * C::NG + 2 * zp);
+                    kza1[i] = *reinterpret_cast<const uint32_t *>(kzr + (g + 8) * C::NG + 2 * zp);
+                }
             }
             // ---- S^T = K Q^T per group, scaled and summed ----
-            f2 s01 = {0.f, 0.f}, s23 = {0.f, 0.f};
+            f2 s01[NPG], s23[NPG];
+#pragma unroll
+            for (int i = 0; i < NPG; ++i) s01[i] = s23[i] = f2{0.f, 0.f};
 #pragma unroll
             for (int gr = 0; gr < C::NG; ++gr) {
-                float acc[4];
                 const uint4 qb = *reinterpret_cast<const uint4 *>(qfrag + (gr * 32 + lane) * 4);
-                {
-                    const int ks = 2 * gr;
-                    const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
-                    mma_f16_z(acc, af, qb.x, qb.y);
+#pragma unroll
+                for (int i = 0; i < NPG; ++i) {
+                    float acc[4];
+                    {
+                        const int ks = 2 * gr;
+                        const uint32_t af[4] = {r0[i].reg(2 * ks), r1[i].reg(2 * ks), r0[i].reg(2 * ks + 1),
+                                                r1[i].reg(2 * ks + 1)};
+                        mma_f16_z(acc, af, qb.x, qb.y);
+                    }
+                    {
+                        const int ks = 2 * gr + 1;
+                        const uint32_t af[4] = {r0[i].reg(2 * ks), r1[i].reg(2 * ks), r0[i].reg(2 * ks + 1),
+                                                r1[i].reg(2 * ks + 1)};
+                        mma_f16(acc, af, qb.z, qb.w);
+                    }
+                    s01[i].x = fmaf(sc0[i][gr], acc[0], s01[i].x);
+                    s01[i].y = fmaf(sc0[i][gr], acc[1], s01[i].y);
+                    s23[i].x = fmaf(sc1[i][gr], acc[2], s23[i].x);
+                    s23[i].y = fmaf(sc1[i][gr], acc[3], s23[i].y);
                 }
-                {
-                    const int ks = 2 * gr + 1;
-                    const uint32_t af[4] = {r0.reg(2 * ks), r1.reg(2 * ks), r0.reg(2 * ks + 1), r1.reg(2 * ks + 1)};
-                    mma_f16(acc, af, qb.z, qb.w);
-                }
-                s01.x = fmaf(sc0[gr], acc[0], s01.x);
-                s01.y = fmaf(sc0[gr], acc[1], s01.y);
-                s23.x = fmaf(sc1[gr], acc[2], s23.x);
-                s23.y = fmaf(sc1[gr], acc[3], s23.y);
             }
             // zero-point term, accumulated onto minus the running max
-            float z[4];
-            {
-                const uint32_t za[4] = {kza0, kza1, 0u, 0u};
+            float x[NPG][4];  // log2 score - running max
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < NPG; ++i) {
+                float z[4];
+                const uint32_t za[4] = {kza0[i], kza1[i], 0u, 0u};
                 mma_f16_c(z, za, bz, 0u, nm);
-            }
-            const f2 x01 = fma2(s01, f2{kscale, kscale}, f2{z[0], z[1]});
-            const f2 x23 = fma2(s23, f2{kscale, kscale}, f2{z[2], z[3]});
-            float x[4] = {x01.x, x01.y, x23.x, x23.y};  // log2 score - running max
-            if (nvalid < kPage) {  // ragged last page: mask the scores of empty slots
-                if (g >= nvalid) x[0] = x[1] = -INFINITY;
-                if (g + 8 >= nvalid) x[2] = x[3] = -INFINITY;
+                const f2 x01 = fma2(s01[i], f2{kscale, kscale}, f2{z[0], z[1]});
+                const f2 x23 = fma2(s23[i], f2{kscale, kscale}, f2{z[2], z[3]});
+                x[i][0] = x01.x; x[i][1] = x01.y; x[i][2] = x23.x; x[i][3] = x23.y;
+                if (nvalid[i] < kPage) {  // ragged last page: mask the scores of empty slots
+                    if (g >= nvalid[i]) x[i][0] = x[i][1] = -INFINITY;
+                    if (g + 8 >= nvalid[i]) x[i][2] = x[i][3] = -INFINITY;
+                }
+                mx = fmaxf(mx, fmaxf(fmaxf(x[i][0], x[i][1]), fmaxf(x[i][2], x[i][3])));
             }
 
             // ---- online softmax: rescale only when a score beats the running max ----
-            const float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
             if (__any_sync(0xffffffffu, mx > 0.0f || fresh)) {
-                float sv[4] = {x[0] + ms0, x[1] + ms1, x[2] + ms0, x[3] + ms1};
-                float mx0 = fmaxf(sv[0], sv[2]), mx1 = fmaxf(sv[1], sv[3]);
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < NPG; ++i) {
+                    x[i][0] += ms0; x[i][1] += ms1; x[i][2] += ms0; x[i][3] += ms1;
+                    mx0 = fmaxf(mx0, fmaxf(x[i][0], x[i][2]));
+                    mx1 = fmaxf(mx1, fmaxf(x[i][1], x[i][3]));
+                }
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -541,79 +570,98 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 ms1 = mn1 == -INFINITY ? 0.0f : mn1;
                 nm[0] = nm[2] = -ms0;
                 nm[1] = nm[3] = -ms1;
-                x[0] = sv[0] - ms0; x[1] = sv[1] - ms1; x[2] = sv[2] - ms0; x[3] = sv[3] - ms1;
-            }
-            const uint8_t *vpar = vb + C::CR;
-            uint32_t vsc[2 * C::NG];  // per group: scales of tokens (2t, 2t+1), then (2t+8, 2t+9)
-            {
-                const uint32_t *pp = reinterpret_cast<const uint32_t *>(vpar + t * 8 * C::NG);
 #pragma unroll
-                for (int i = 0; i < 2 * C::NG; i += 4) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(pp + i);
-                    vsc[i] = u.x; vsc[i + 1] = u.y; vsc[i + 2] = u.z; vsc[i + 3] = u.w;
+                for (int i = 0; i < NPG; ++i) {
+                    x[i][0] -= ms0; x[i][1] -= ms1; x[i][2] -= ms0; x[i][3] -= ms1;
                 }
             }
-            // A of the V zero-point MMA: rows 0..G-1 the group's zero points of
-            // tokens (2t, 2t+1) / (2t+8, 2t+9); row G ones, so the MMA also sums
-            // P over the page (the softmax denominator)
-            uint32_t vza0 = 0u, vza2 = 0u;
-            if (g < C::NG) {
-                const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
-                vza0 = u.x;
-                vza2 = u.y;
-            } else if (g == C::NG) {
-                vza0 = vza2 = 0x3C003C00u;
-            }
+#pragma unroll
+            for (int i = 0; i < NPG; ++i) {
+                const uint8_t *vb = ring + (S0 + i) * C::STAGE + C::HB;
+                const uint8_t *vpar = vb + C::CR;
+                uint32_t vsc[2 * C::NG];  // per group: scales of tokens (2t, 2t+1), then (2t+8, 2t+9)
+                {
+                    const uint32_t *pp = reinterpret_cast<const uint32_t *>(vpar + t * 8 * C::NG);
+#pragma unroll
+                    for (int j = 0; j < 2 * C::NG; j += 4) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(pp + j);
+                        vsc[j] = u.x; vsc[j + 1] = u.y; vsc[j + 2] = u.z; vsc[j + 3] = u.w;
+                    }
+                }
+                // A of the V zero-point MMA: rows 0..G-1 the group's zero
+                // points of tokens (2t, 2t+1) / (2t+8, 2t+9); row G ones, so
+                // the MMA also sums P over the page (the softmax denominator)
+                uint32_t vza0 = 0u, vza2 = 0u;
+                if (g < C::NG) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
+                    vza0 = u.x;
+                    vza2 = u.y;
+                } else if (g == C::NG) {
+                    vza0 = vza2 = 0x3C003C00u;
+                }
+                if (nvalid[i] < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
+                    const int nv = nvalid[i];
+                    const uint32_t mlo = (2 * t < nv ? 0x0000FFFFu : 0u) | (2 * t + 1 < nv ? 0xFFFF0000u : 0u);
+                    const uint32_t mhi = (2 * t + 8 < nv ? 0x0000FFFFu : 0u) | (2 * t + 9 < nv ? 0xFFFF0000u : 0u);
+#pragma unroll
+                    for (int gr = 0; gr < C::NG; ++gr) {
+                        vsc[2 * gr] &= mlo;
+                        vsc[2 * gr + 1] &= mhi;
+                    }
+                    vza0 &= mlo;
+                    vza2 &= mhi;
+                }
+                VReg<BITS, D> vs;
+                vs.load(vb, g, t);
+                const float p[4] = {ex2(x[i][0]), ex2(x[i][1]), ex2(x[i][2]), ex2(x[i][3])};
 
-            if (nvalid < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
-                const uint32_t mlo = (2 * t < nvalid ? 0x0000FFFFu : 0u) | (2 * t + 1 < nvalid ? 0xFFFF0000u : 0u);
-                const uint32_t mhi = (2 * t + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t + 9 < nvalid ? 0xFFFF0000u : 0u);
+                // ---- P^T as the B operand (k-slot = token, column = head):
+                // the score fragment rows 0-7 / 8-15 transposed ----
+                const uint32_t blo = movmatrix_t(pack_f16(p[0], p[1]));
+                const uint32_t bhi = movmatrix_t(pack_f16(p[2], p[3]));
+                const uint32_t bhi_s = hmul2(bhi, vhi_scale);
+
+                // ---- O^T += V^T (P s)^T, zero points as one more MMA ----
 #pragma unroll
                 for (int gr = 0; gr < C::NG; ++gr) {
-                    vsc[2 * gr] &= mlo;
-                    vsc[2 * gr + 1] &= mhi;
-                }
-                vza0 &= mlo;
-                vza2 &= mhi;
-            }
-            VReg<BITS, D> vs;
-            vs.load(vb, g, t);
-            const float p[4] = {ex2(x[0]), ex2(x[1]), ex2(x[2]), ex2(x[3])};
-
-            // ---- P^T as the B operand (k-slot = token, column = head): the
-            // score fragment rows 0-7 / 8-15 (tokens 0-7 / 8-15) transposed ----
-            const uint32_t blo = movmatrix_t(pack_f16(p[0], p[1]));
-            const uint32_t bhi = movmatrix_t(pack_f16(p[2], p[3]));
-            const uint32_t bhi_s = hmul2(bhi, vhi_scale);
-
-            // ---- O^T += V^T (P s)^T, zero points as one more MMA ----
+                    const uint32_t b0 = hmul2(blo, vsc[2 * gr]), b1 = hmul2(bhi_s, vsc[2 * gr + 1]);
 #pragma unroll
-            for (int gr = 0; gr < C::NG; ++gr) {
-                const uint32_t b0 = hmul2(blo, vsc[2 * gr]), b1 = hmul2(bhi_s, vsc[2 * gr + 1]);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int mt = 2 * gr + h2;
-                    uint32_t af[4];
-                    vs.regs(mt, af);
-                    mma_f16(o[mt], af, b0, b1);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int mt = 2 * gr + h2;
+                        uint32_t af[4];
+                        vs.regs(mt, af);
+                        mma_f16(o[mt], af, b0, b1);
+                    }
                 }
-            }
-            {
-                const uint32_t za[4] = {vza0, 0u, vza2, 0u};
-                mma_f16(oz, za, blo, bhi);
+                {
+                    const uint32_t za[4] = {vza0, 0u, vza2, 0u};
+                    mma_f16(oz, za, blo, bhi);
+                }
             }
             __syncwarp();
-            if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+#pragma unroll
+            for (int i = 0; i < NPG; ++i)
+                if (k + i + C::NSTAGE < nw) issue(k + i + C::NSTAGE);
             return true;
         };
-        // driver: stages in order, the ring index known at compile time
+        // driver: pairs of stages in order, the ring indices known at compile
+        // time (NSTAGE = 4: pages k0, k0+1 in stages 0, 1; k0+2, k0+3 in 2, 3)
+        static_assert(C::NSTAGE == 4, "the driver below unrolls a 4-stage ring");
+        using I0 = std::integral_constant<int, 0>;
+        using I1 = std::integral_constant<int, 1>;
+        using I2 = std::integral_constant<int, 2>;
         for (int k0 = 0; k0 < nw; k0 += C::NSTAGE) {
             const uint32_t parity = (uint32_t)(k0 / C::NSTAGE) & 1u;
-            bool ok = true;
-#pragma unroll
-            for (int j = 0; j < C::NSTAGE; ++j) {
-                if (k0 + j < nw && ok) ok = page(k0 + j, j, parity);
-            }
+            bool ok;
+            if (k0 + 1 < nw)
+                ok = body(k0, I0{}, parity, I2{});
+            else
+                ok = body(k0, I0{}, parity, I1{});
+            if (!ok) break;
+            if (k0 + 3 < nw)
+                ok = body(k0 + 2, I2{}, parity, I2{});
+            else if (k0 + 2 < nw)
+                ok = body(k0 + 2, I2{}, parity, I1{});
             if (!ok) break;
         }
         l[0] = __shfl_sync(0xffffffffu, oz[0], C::NG * 4 + t);

@@ -40,6 +40,7 @@ struct MCfg {
 
 template <int BITS, int D>
 __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ MixedArgs m) {
+    pdl_begin();
     extern __shared__ __align__(1024) uint8_t smem[];
     int bid = blockIdx.x;
     if (bid < m.n_verify_blocks) {
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__
 
 template <int D>
 __global__ void mixed_reduce_kernel(MixedArgs m, float *out_draft, float *out_verify, int draft_rows) {
+    pdl_begin();
     const int row = blockIdx.x;
     if (row < draft_rows) {  // row = b * Hq + h
         if (m.role[row / m.d.hq] != 0) return;
@@ -82,12 +84,15 @@ int sms() {
     return n;
 }
 
-// Draft chunking of the mixed launch: about two draft blocks per SM over the
-// whole batch (blocks of verifying requests exit at once).
+// Draft chunking of the mixed launch: at least two draft blocks per SM over
+// the whole batch, and at most 258 pages (43 per warp) per block, so that
+// requests of very different lengths (blocks past a request's end exit at
+// once, as do blocks of verifying requests) still spread evenly over the SMs.
 void draft_plan(int batch, int hkv, int max_seq_len, int &chunk, int &splits) {
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
     int s = (int)((2LL * sms() + units - 1) / units);
+    s = max(s, ceil_div(max_pages, 43 * kDraftWarps));
     s = max(1, min(s, ceil_div(max_pages, kDraftWarps)));
     chunk = ceil_div(max_pages, s);
     chunk = max(kDraftWarps, ceil_div(chunk, kDraftWarps) * kDraftWarps);
@@ -109,11 +114,11 @@ cudaError_t launch(const MixedArgs &m, int batch, float *out_draft, float *out_v
         attr = true;
     }
     const int nd = m.d.n_splits * m.d.hkv * batch;
-    mixed_kernel<BITS, D><<<m.n_verify_blocks + nd, kThreads, C::SMEM, st>>>(m);
+    launch_pdl(mixed_kernel<BITS, D>, m.n_verify_blocks + nd, kThreads, C::SMEM, st, m);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int draft_rows = batch * m.d.hq, verify_rows = batch * m.v.n_q * m.v.hq;
-    mixed_reduce_kernel<D><<<draft_rows + verify_rows, D, 0, st>>>(m, out_draft, out_verify, draft_rows);
+    launch_pdl(mixed_reduce_kernel<D>, draft_rows + verify_rows, D, 0, st, m, out_draft, out_verify, draft_rows);
     return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ namespace {
 
 __global__ void embed_kernel(const int32_t *ids, int m, const float *table, int d, int vocab, float *out,
                              int32_t *status) {
+    pdl_begin();
     const int r = blockIdx.x;
     const int id = ids[r];
     const bool ok = id >= 0 && id < vocab;
@@ -25,6 +26,7 @@ __global__ void embed_kernel(const int32_t *ids, int m, const float *table, int 
 // y = x / sqrt(mean(x^2) + eps) * w; per-thread strided sums, then a fixed
 // shuffle / shared-memory tree.
 __global__ void rmsnorm_kernel(const float *x, int d, const float *w, float eps, float *out) {
+    pdl_begin();
     __shared__ float part[32];
     const int64_t r = blockIdx.x;
     const float *xr = x + r * d;
@@ -48,6 +50,7 @@ __global__ void rmsnorm_kernel(const float *x, int d, const float *w, float eps,
 constexpr int TM = 64, TN = 128, TK = 32;
 __global__ void __launch_bounds__(256) linear_kernel(const float *x, const uint16_t *w, float *out, int m, int k,
                                                      int n, int accumulate) {
+    pdl_begin();
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs[TK][TN];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -102,6 +105,7 @@ __global__ void __launch_bounds__(256) linear_kernel(const float *x, const uint1
 
 // silu(g) * u, g = gu[:, :f], u = gu[:, f:]
 __global__ void swiglu_kernel(const float *gu, int m, int f, float *out) {
+    pdl_begin();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)m * f) return;
     const int64_t r = i / f, c = i % f;
@@ -115,6 +119,7 @@ __global__ void swiglu_kernel(const float *gu, int m, int f, float *out) {
 __global__ void rope_kv_kernel(const float *qkv, const int32_t *row_req, const int32_t *row_pos, int hq, int hkv,
                                int d, float theta, uint16_t *q_out, uint8_t *kp, uint8_t *vp, int64_t n_pages,
                                const int32_t *table, int maxb, int batch, int32_t *status) {
+    pdl_begin();
     const int r = blockIdx.x;
     const int b = row_req[r], pos = row_pos[r];
     const bool req_ok = b >= 0 && b < batch;
@@ -163,7 +168,7 @@ vc_status vc_embed(const int32_t *ids, int32_t m, const float *table, int32_t d,
                    int32_t *dev_status, vc_stream_t stream) {
     if (!ids || !table || !out || m < 0 || d < 1 || vocab < 1) return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
-    embed_kernel<<<m, 256, 0, (cudaStream_t)stream>>>(ids, m, table, d, vocab, out, dev_status);
+    launch_pdl(embed_kernel, m, 256, 0, (cudaStream_t)stream, ids, m, table, d, vocab, out, dev_status);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
@@ -171,7 +176,7 @@ vc_status vc_rmsnorm(const float *x, int32_t m, int32_t d, const float *weight, 
                      vc_stream_t stream) {
     if (!x || !weight || !out || m < 0 || d < 1) return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
-    rmsnorm_kernel<<<m, 256, 0, (cudaStream_t)stream>>>(x, d, weight, eps, out);
+    launch_pdl(rmsnorm_kernel, m, 256, 0, (cudaStream_t)stream, x, d, weight, eps, out);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
@@ -180,7 +185,8 @@ vc_status vc_linear(const float *x, const void *w_bf16, float *out, int32_t m, i
     if (!x || !w_bf16 || !out || m < 0 || k < 1 || n < 1) return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
     dim3 grid(ceil_div(n, TN), ceil_div(m, TM));
-    linear_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, (const uint16_t *)w_bf16, out, m, k, n, accumulate);
+    launch_pdl(linear_kernel, grid, 256, 0, (cudaStream_t)stream, x, (const uint16_t *)w_bf16, out, m, k, n,
+               accumulate);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
@@ -188,7 +194,7 @@ vc_status vc_swiglu(const float *gu, int32_t m, int32_t f, float *out, vc_stream
     if (!gu || !out || m < 0 || f < 1) return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
     const int64_t n = (int64_t)m * f;
-    swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(gu, m, f, out);
+    launch_pdl(swiglu_kernel, (unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream, gu, m, f, out);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 
@@ -199,10 +205,10 @@ vc_status vc_rope_kv_write(const float *qkv, int32_t m, const int32_t *row_req, 
         !full->block_table || m < 0 || num_q_heads < 1 || full->fmt.bits != 16 || full->fmt.head_dim % 2)
         return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
-    rope_kv_kernel<<<m, 256, 0, (cudaStream_t)stream>>>(
-        qkv, row_req, row_pos, num_q_heads, full->fmt.num_kv_heads, full->fmt.head_dim, rope_theta,
-        (uint16_t *)q_out, (uint8_t *)full->k_pages, (uint8_t *)full->v_pages, full->num_pages, full->block_table,
-        full->max_blocks, full->batch, dev_status);
+    launch_pdl(rope_kv_kernel, m, 256, 0, (cudaStream_t)stream,
+               qkv, row_req, row_pos, num_q_heads, full->fmt.num_kv_heads, full->fmt.head_dim, rope_theta,
+               (uint16_t *)q_out, (uint8_t *)full->k_pages, (uint8_t *)full->v_pages, full->num_pages,
+               full->block_table, full->max_blocks, full->batch, dev_status);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

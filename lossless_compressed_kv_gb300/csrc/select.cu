@@ -31,6 +31,7 @@ __device__ inline uint32_t order_key(float f) {  // larger float <=> larger key
 template <int D>
 __global__ void keynorm_kernel(const uint8_t *kp, int64_t n_pages, const int32_t *table, const int32_t *lens,
                                int maxb, int hkv, float *scores, int stride, int32_t *status) {
+    pdl_begin();
     const int b = blockIdx.y;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= lens[b] || t >= stride) return;
@@ -63,6 +64,7 @@ __global__ void keynorm_kernel(const uint8_t *kp, int64_t n_pages, const int32_t
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const float *scores, int stride, const int32_t *lens,
                                                              const int32_t *offs, int sink_in, int recent_in,
                                                              int32_t *idx, int32_t *status) {
+    pdl_begin();
     __shared__ unsigned int hist[256];
     __shared__ unsigned int wsum[2][kSelThreads / 32];
     __shared__ uint32_t s_prefix, s_mask;
@@ -178,18 +180,18 @@ vc_status select_kept(const vc_paged_kv *full, const float *scores, int32_t scor
         float *w = reinterpret_cast<float *>(ws);
         dim3 grid(ceil_div(score_stride, 256), batch);
         if (d == 64)
-            keynorm_kernel<64><<<grid, 256, 0, st>>>((const uint8_t *)full->k_pages, full->num_pages,
-                                                     full->block_table, full->seq_lens, full->max_blocks,
-                                                     full->fmt.num_kv_heads, w, score_stride, dev_status);
+            launch_pdl(keynorm_kernel<64>, grid, 256, 0, st, (const uint8_t *)full->k_pages, full->num_pages,
+                       full->block_table, full->seq_lens, full->max_blocks,
+                       full->fmt.num_kv_heads, w, score_stride, dev_status);
         else
-            keynorm_kernel<128><<<grid, 256, 0, st>>>((const uint8_t *)full->k_pages, full->num_pages,
-                                                      full->block_table, full->seq_lens, full->max_blocks,
-                                                      full->fmt.num_kv_heads, w, score_stride, dev_status);
+            launch_pdl(keynorm_kernel<128>, grid, 256, 0, st, (const uint8_t *)full->k_pages, full->num_pages,
+                       full->block_table, full->seq_lens, full->max_blocks,
+                       full->fmt.num_kv_heads, w, score_stride, dev_status);
         if (cudaGetLastError() != cudaSuccess) return VC_ERR_CUDA;
         sc = w;
     }
-    select_kernel<<<batch, kSelThreads, 0, st>>>(sc, stride, full->seq_lens, kept_offsets, sink, recent, kept_idx,
-                                                 dev_status);
+    launch_pdl(select_kernel, batch, kSelThreads, 0, st, sc, stride, full->seq_lens, kept_offsets, sink, recent,
+               kept_idx, dev_status);
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "vc.h"
 
 namespace vc {
@@ -180,5 +182,41 @@ __device__ inline float ex2(float x) {
 __device__ inline float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Kernels are launched with programmatic
+// stream serialisation, so a kernel may be scheduled while the previous one
+// on its stream is finishing (its launch and block set-up overlap that
+// kernel's tail).  Every kernel starts with pdl_wait(): griddepcontrol.wait
+// blocks until the previous kernel has completed and its memory is visible
+// (so nothing it wrote or reads is touched before).  pdl_trigger()
+// (griddepcontrol.launch_dependents) lets the next kernel be scheduled once
+// every block of this one has called it or exited: short kernels call it at
+// once (pdl_begin), long multi-wave kernels after their main loop, so that
+// waiting blocks of the next kernel do not sit on SMs that still run this
+// one's last wave.  Without the launch attribute both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace vc

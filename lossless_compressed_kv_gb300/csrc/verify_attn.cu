@@ -6,8 +6,8 @@
 // parallel; query i of the block attends causally to every earlier position
 // and to itself ("KV Cache and Speculative Decoding": causal attention).
 // Launch: one CTA per (split of 4096 keys, row block, request x kv head);
-// a row block holds up to three 128-row MMA tiles of (query, head) rows (the
-// fewest tiles that cover the rows; more rows take further row blocks).
+// a row block holds one 128-row MMA tile of (query, head) rows when there
+// are at most 128 rows, else two (more rows take further row blocks).
 #include "verify_tc.cuh"
 
 namespace vc {
@@ -16,12 +16,14 @@ namespace {
 
 template <int D, int QT>
 __global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS, vtc::Cfg<D, QT>::MIN_CTAS) verify_kernel(const __grid_constant__ Args a) {
+    pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem[];
     vtc::verify_tc_block<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }
 
 template <int D>
 __global__ void verify_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, float *out) {
+    pdl_begin();
     vtc::reduce_row<D>(ws_o, ws_ml, n_splits, blockIdx.x, out, threadIdx.x, blockDim.x);
 }
 
@@ -35,7 +37,7 @@ cudaError_t launch(Args &a, int batch, cudaStream_t st) {
     }
     a.rows_per_cta = QT * vtc::kTileRows;
     dim3 grid(a.n_splits, ceil_div(a.n_q * a.grp, a.rows_per_cta), batch * a.hkv);
-    verify_kernel<D, QT><<<grid, C::THREADS, C::SMEM, st>>>(a);
+    launch_pdl(verify_kernel<D, QT>, grid, C::THREADS, C::SMEM, st, a);
     return cudaGetLastError();
 }
 
@@ -115,20 +117,21 @@ cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, 
     Args a;
     if (!verify_args(a, q, n_q, hq, f, scale, max(max_seq_len, 1), ws, status)) return cudaErrorInvalidValue;
     const int d = f.fmt.head_dim;
-    const int tiles = min(3, ceil_div(n_q * a.grp, vtc::kTileRows));
+    // one tile for up to 128 rows, else row blocks of two tiles (the last
+    // one may hold a single used tile): every configuration uses the same
+    // 64-key blocks, so a row's bits do not depend on n_q
+    const int tiles = min(2, ceil_div(n_q * a.grp, vtc::kTileRows));
     cudaError_t e;
     if (d == 64)
-        e = tiles == 1 ? launch<64, 1>(a, f.batch, st) : tiles == 2 ? launch<64, 2>(a, f.batch, st)
-                                                         : launch<64, 3>(a, f.batch, st);
+        e = tiles == 1 ? launch<64, 1>(a, f.batch, st) : launch<64, 2>(a, f.batch, st);
     else
-        e = tiles == 1 ? launch<128, 1>(a, f.batch, st) : tiles == 2 ? launch<128, 2>(a, f.batch, st)
-                                                          : launch<128, 3>(a, f.batch, st);
+        e = tiles == 1 ? launch<128, 1>(a, f.batch, st) : launch<128, 2>(a, f.batch, st);
     if (e != cudaSuccess) return e;
     const int rows = f.batch * n_q * hq;
     if (d == 64)
-        verify_reduce_kernel<64><<<rows, 64, 0, st>>>(a.ws_o, a.ws_ml, a.n_splits, out);
+        launch_pdl(verify_reduce_kernel<64>, rows, 64, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
     else
-        verify_reduce_kernel<128><<<rows, 128, 0, st>>>(a.ws_o, a.ws_ml, a.n_splits, out);
+        launch_pdl(verify_reduce_kernel<128>, rows, 128, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
     return cudaGetLastError();
 }
 

@@ -3,27 +3,32 @@
 // "VeriCache: Making Lossy KV Compression Exact", "The Core Idea" items 3-5:
 // one pass over KV_full checks every drafted position; query i of the block
 // attends causally to the prefix and the block up to itself.  The rows of a
-// CTA are (query, head) pairs of one kv head's GQA group (up to 256 rows =
-// two 128-row MMA tiles), so every K/V byte feeds n_q * G rows.
+// CTA are (query, head) pairs of one kv head's GQA group (one 128-row MMA
+// tile, or two for more than 128 rows), so every K/V byte feeds n_q * G rows.
 //
 // Roles (one CTA = one (request, kv head, 4096-key split, row block)):
-//  - producer warp: one thread streams 32-key blocks (2 pages) of K and V
-//    into a 4-stage shared-memory ring with TMA tensor copies (one 16-row x
-//    64-channel box per page and 128-byte column chunk); the TMA unit writes
-//    the 128-byte-swizzled layout the tensor core reads.  Full / empty
-//    mbarriers per stage (transaction bytes / MMA completion).
-//  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 32,
+//  - producer warp: one thread streams 64-key blocks (4 pages) of K and V
+//    into a shared-memory ring (3 stages for one tile, 4 for two) with TMA
+//    tensor copies (one 16-row x 64-channel box per page and 128-byte column
+//    chunk); the TMA unit writes the 128-byte-swizzled layout the tensor core
+//    reads.  Full / empty mbarriers per stage (transaction bytes / MMA
+//    completion).
+//  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 64,
 //    K 16 steps) into TMEM, then O += P V (M 128, N = D) with P read from
-//    TMEM as the A operand and V from shared memory (MN-major).
+//    TMEM as the A operand and V from shared memory (MN-major).  A one-tile
+//    CTA keeps Q in TMEM too (its S MMAs read only the K block from shared
+//    memory); a two-tile CTA keeps it in shared memory.
 //  - 4 softmax warps per 128-row tile: each thread owns one row = one TMEM
-//    lane; it loads the row's 32 scores from TMEM, masks (only blocks that
+//    lane; it loads the row's 64 scores from TMEM, masks (only blocks that
 //    reach the query block), keeps a running max (rescaling O in TMEM only
 //    when the max grows by more than 2^8), writes P (bf16 pairs) over the
 //    first half of the S buffer it came from, and finally reads O.
-//  With one 128-row tile a CTA uses 97 KB of shared memory and 256 TMEM
-//  columns, so two CTAs share an SM and their softmax warps interleave.
-// Splits are fixed by key position and each row's arithmetic depends on that
-// row alone, so results do not depend on n_q, the row block or the batch.
+//  A one-tile CTA uses 96 KB of shared memory and 256 TMEM columns with one
+//  S buffer, so two CTAs share an SM and overlap each other's S / softmax /
+//  P V chain; a two-tile CTA holds two S buffers per tile and runs alone.
+// Every configuration uses the same 64-key blocks and each row's arithmetic
+// depends on that row alone, with splits fixed by key position, so results
+// do not depend on n_q, the row block or the batch.
 // Every mbarrier wait is bounded; a timeout is reported and the CTA drains.
 #pragma once
 
@@ -57,26 +62,43 @@ struct Args {
 template <int D, int QT>
 struct Cfg {
     static constexpr int NC = D / 64;                      // swizzle atoms along D
-    // K/V ring depth: one-tile CTAs run two per SM (4 stages each); larger
-    // CTAs run alone and prefetch deeper to cover HBM latency
-    static constexpr int STAGES = QT == 1 ? 4 : QT == 2 ? 8 : 6;
+    static_assert(QT == 1 || QT == 2, "one or two 128-row tiles per CTA");
+    // keys per block: the softmax round trip between the MMA warp and the
+    // softmax warps (barrier wake-ups, TMEM load and store latencies) is paid
+    // once per 64 keys
+    static constexpr int BK = 64;
     // S buffers per tile in TMEM (P is written over its S buffer): two let a
-    // tile's next S overlap its softmax; three tiles fit 512 columns with one
-    // each and overlap across tiles instead
-    static constexpr int SB = QT == 3 ? 1 : 2;
+    // tile's next S overlap its softmax; one-tile CTAs (two per SM, 256
+    // columns each) take one so that Q fits in TMEM and the shared memory
+    // holds three K/V stages -- the two CTAs of an SM overlap instead
+    static constexpr int SB = QT == 2 ? 2 : 1;
+    // Q as the TMEM A operand of S = Q K^T when it fits next to the S and O
+    // columns (then the S MMAs read only the K block from shared memory);
+    // otherwise Q stays in shared memory
+    static constexpr int TMEM_LIMIT = QT == 1 ? 256 : 512;  // one-tile CTAs run two per SM
+    static constexpr bool QTM = QT * SB * BK + QT * D + QT * D / 2 <= TMEM_LIMIT;
     static constexpr int QTILE = kTileRows * D * 2;        // one Q tile
-    static constexpr int KTILE = kBlockKeys * D * 2;       // one K (or V) block
-    static constexpr int OFF_KV = QT * QTILE;
+    static constexpr int KTILE = BK * D * 2;               // one K (or V) block
+    static constexpr int OFF_KV = QTM ? 0 : QT * QTILE;
+    // K/V ring depth within the shared memory of the CTAs an SM holds
+    static constexpr int STAGE_BYTES = 2 * KTILE;
+    static constexpr int STAGES_FIT = ((QT == 1 ? 110 : 220) * 1024 - OFF_KV) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+    static_assert(STAGES >= 2, "K/V ring needs two stages");
     static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * KTILE;
     static constexpr int NBAR = QT * 2 + QT * 2 + 2 + 2 * STAGES;  // s_ready, p_ready, pv_done, full, empty
     static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
-    static constexpr int TMEM_COLS = (QT * SB * kBlockKeys + QT * D) <= 256 ? 256 : 512;
+    static constexpr int TMEM_USED = QT * SB * BK + QT * D + (QTM ? QT * D / 2 : 0);
+    static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+    static_assert(TMEM_USED <= TMEM_LIMIT, "S, O (and Q) columns exceed TMEM");
     static constexpr int THREADS = QT * 128 + 64;  // softmax warps + producer warp + MMA warp
     static constexpr int MIN_CTAS = QT == 1 ? 2 : 1;  // resident CTAs per SM (TMEM: 256 columns each)
-    __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) {
-        return (uint32_t)(qt * SB + buf) * kBlockKeys;
+    __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) { return (uint32_t)(qt * SB + buf) * BK; }
+    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * SB * BK + qt * D); }
+    // Q tile qt as bf16 pairs (D / 2 columns), when QTM
+    __host__ __device__ static constexpr uint32_t Q_COL(int qt) {
+        return (uint32_t)(QT * SB * BK + QT * D + qt * (D / 2));
     }
-    __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * SB * kBlockKeys + qt * D); }
 };
 
 // --- tcgen05 / descriptor helpers ------------------------------------------
@@ -144,6 +166,62 @@ __device__ inline void tmem_st16(uint32_t taddr, const float (&v)[16]) {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// N (32 or 64) consecutive columns of this thread's lane: one load, one wait
+template <int N>
+__device__ inline void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
+    static_assert(N == 32 || N == 64, "x32 or x64 loads");
+    uint32_t r[N];
+    if constexpr (N == 32) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+            : "r"(taddr)
+            : "memory");
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// max of N values as a tree (log2 N dependent steps); exact, so the order
+// does not change the result
+template <int N>
+__device__ inline float max_tree(const float (&v)[N]) {
+    float m[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) m[i] = fmaxf(v[i], v[i + N / 2]);
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+
+// 16 columns of this thread's lane, without waiting (tcgen05.wait::st follows)
+__device__ inline void tmem_st16_nowait(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
 // offset of (row, 16-byte chunk c) in a 128-byte-swizzled K-major tile whose
 // rows are `rows` long per 64-element atom column
 __device__ inline int sw128(int row, int c, int rows) {
@@ -177,8 +255,11 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     const int p0 = split * kSplitPages;
     const int p1 = min(p0 + kSplitPages, npages);
     const int nkeys = max(0, min(p1 * kPage, len) - p0 * kPage);
-    const int nb = ceil_div(nkeys, kBlockKeys);
+    const int nb = ceil_div(nkeys, C::BK);
     const int nrows = a.n_q * a.grp;
+    // tiles of this row block holding at least one row (the last row block
+    // may fill fewer than QT): the others issue no MMA and run no softmax
+    const int nt = min(QT, ceil_div(max(0, min(a.rows_per_cta, nrows - rb * a.rows_per_cta)), kTileRows));
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
     // ---- set-up: barriers, TMEM, Q tiles ----
@@ -200,25 +281,59 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                      "r"(C::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    for (int e = tid; e < QT * kTileRows * (D / 8); e += C::THREADS) {
-        const int r = e / (D / 8), c = e % (D / 8);     // r: row within the CTA, c: 16-byte chunk
-        const int rg = rb * a.rows_per_cta + r;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (rg < nrows) {
-            const int i = rg / a.grp, n = rg % a.grp;
-            v = *reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D +
-                                                 c * 8);
+    if constexpr (!C::QTM) {
+        for (int e = tid; e < QT * kTileRows * (D / 8); e += C::THREADS) {
+            const int r = e / (D / 8), c = e % (D / 8);     // r: row within the CTA, c: 16-byte chunk
+            const int rg = rb * a.rows_per_cta + r;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (rg < nrows) {
+                const int i = rg / a.grp, n = rg % a.grp;
+                v = *reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) *
+                                                               D +
+                                                     c * 8);
+            }
+            *reinterpret_cast<uint4 *>(sq + (r >> 7) * C::QTILE + sw128(r & 127, c, kTileRows)) = v;
         }
-        *reinterpret_cast<uint4 *>(sq + (r >> 7) * C::QTILE + sw128(r & 127, c, kTileRows)) = v;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if constexpr (C::QTM) {
+        // each softmax thread writes its own row (= TMEM lane) of its tile's
+        // Q as bf16 pairs (element 2c in the low half of column c)
+        if (warp < QT * 4) {
+            const int qt = warp >> 2;
+            const int r = (warp & 3) * 32 + lane;
+            const int rg = rb * a.rows_per_cta + qt * kTileRows + r;
+            const uint4 *src = nullptr;
+            if (rg < nrows) {
+                const int i = rg / a.grp, n = rg % a.grp;
+                src = reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D);
+            }
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+#pragma unroll
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 u = src ? src[c0 / 4 + j] : make_uint4(0, 0, 0, 0);
+                    v[4 * j] = __uint_as_float(u.x);
+                    v[4 * j + 1] = __uint_as_float(u.y);
+                    v[4 * j + 2] = __uint_as_float(u.z);
+                    v[4 * j + 3] = __uint_as_float(u.w);
+                }
+                tmem_st16(tmem + lane_base + C::Q_COL(qt) + c0, v);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     bool alive = true;
 
-    constexpr uint32_t IQK = idesc_bf16(128, kBlockKeys, false);
+    constexpr uint32_t IQK = idesc_bf16(128, C::BK, false);
     constexpr uint32_t IPV = idesc_bf16(128, D, true);
     if (producer) {
         // ================= producer: TMA tensor copies into the stage ring =================
@@ -229,8 +344,8 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 if (!alive) break;
                 uint8_t *kt = skv + st * 2 * C::KTILE;
                 mbar_arrive_expect_tx(&full[st], 2 * C::KTILE);
-                for (int pg = 0; pg < kBlockKeys / kPage; ++pg) {
-                    const int pidx = p0 + j * (kBlockKeys / kPage) + pg;
+                for (int pg = 0; pg < C::BK / kPage; ++pg) {
+                    const int pidx = p0 + j * (C::BK / kPage) + pg;
                     int id = 0;
                     if (pidx < npages) {  // pages past the request's end: any valid page (masked / zeroed)
                         id = pidx < a.maxb ? trow[pidx] : -1;
@@ -242,8 +357,8 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                     const int y = (id * a.hkv + kvh) * kPage;
 #pragma unroll
                     for (int c = 0; c < C::NC; ++c) {
-                        tma2d(kt + c * (kBlockKeys * 128) + pg * (kPage * 128), &a.kmap, c * 64, y, &full[st]);
-                        tma2d(kt + C::KTILE + c * (kBlockKeys * 128) + pg * (kPage * 128), &a.vmap, c * 64, y,
+                        tma2d(kt + c * (C::BK * 128) + pg * (kPage * 128), &a.kmap, c * 64, y, &full[st]);
+                        tma2d(kt + C::KTILE + c * (C::BK * 128) + pg * (kPage * 128), &a.vmap, c * 64, y,
                               &full[st]);
                     }
                 }
@@ -253,22 +368,30 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
             auto issue_s = [&](int j, int qt, const uint8_t *kt) {
-                const uint8_t *qtile = sq + qt * C::QTILE;
+                if constexpr (C::QTM) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    umma(tmem + C::S_COL(qt, j % C::SB),
-                         sdesc(smem_u32(qtile) + (ks >> 2) * (kTileRows * 128) + (ks & 3) * 32, 16, 1024),
-                         sdesc(smem_u32(kt) + (ks >> 2) * (kBlockKeys * 128) + (ks & 3) * 32, 16, 1024), IQK,
-                         ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_ta(tmem + C::S_COL(qt, j % C::SB), tmem + C::Q_COL(qt) + ks * 8,
+                                sdesc(smem_u32(kt) + (ks >> 2) * (C::BK * 128) + (ks & 3) * 32, 16, 1024), IQK,
+                                ks > 0);
+                } else {
+                    const uint8_t *qtile = sq + qt * C::QTILE;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma(tmem + C::S_COL(qt, j % C::SB),
+                             sdesc(smem_u32(qtile) + (ks >> 2) * (kTileRows * 128) + (ks & 3) * 32, 16, 1024),
+                             sdesc(smem_u32(kt) + (ks >> 2) * (C::BK * 128) + (ks & 3) * 32, 16, 1024), IQK,
+                             ks > 0);
+                }
                 umma_commit(&s_ready[qt * 2 + j % C::SB]);
             };
             auto issue_pv_tile = [&](int j, int qt) {
                 const uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
                 // P of block j: bf16 pairs in the first half of its S buffer
 #pragma unroll
-                for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+                for (int kk = 0; kk < C::BK / 16; ++kk)
                     umma_ta(tmem + C::O_COL(qt), tmem + C::S_COL(qt, j % C::SB) + kk * 8,
-                            sdesc(smem_u32(vt) + kk * 16 * 128, kBlockKeys * 128, 1024), IPV, (j > 0 || kk > 0));
+                            sdesc(smem_u32(vt) + kk * 16 * 128, C::BK * 128, 1024), IPV, (j > 0 || kk > 0));
             };
             auto finish_pv = [&](int j) {
                 umma_commit(&pv_done[j & 1]);
@@ -286,17 +409,17 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 const uint8_t *kt = skv + st * 2 * C::KTILE;
                 if constexpr (C::SB == 2) {
                     // S of every tile for block j, then P V of block j - 1
-                    for (int qt = 0; qt < QT; ++qt) issue_s(j, qt, kt);
+                    for (int qt = 0; qt < nt; ++qt) issue_s(j, qt, kt);
                     if (j >= 1) {
-                        for (int qt = 0; qt < QT; ++qt) wait_p(j - 1, qt);
+                        for (int qt = 0; qt < nt; ++qt) wait_p(j - 1, qt);
                         if (!alive) break;
-                        for (int qt = 0; qt < QT; ++qt) issue_pv_tile(j - 1, qt);
+                        for (int qt = 0; qt < nt; ++qt) issue_pv_tile(j - 1, qt);
                         finish_pv(j - 1);
                     }
                 } else {
                     // one S buffer per tile: a tile's P V of block j - 1 reads
                     // the buffer its S of block j then overwrites (in order)
-                    for (int qt = 0; qt < QT && alive; ++qt) {
+                    for (int qt = 0; qt < nt && alive; ++qt) {
                         if (j >= 1) {
                             wait_p(j - 1, qt);
                             if (!alive) break;
@@ -308,13 +431,15 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 }
             }
             if (nb > 0 && alive) {
-                for (int qt = 0; qt < QT; ++qt) wait_p(nb - 1, qt);
+                for (int qt = 0; qt < nt; ++qt) wait_p(nb - 1, qt);
                 if (alive) {
-                    for (int qt = 0; qt < QT; ++qt) issue_pv_tile(nb - 1, qt);
+                    for (int qt = 0; qt < nt; ++qt) issue_pv_tile(nb - 1, qt);
                     finish_pv(nb - 1);
                 }
             }
         }
+    } else if ((warp >> 2) >= nt) {
+        // a tile without rows in this row block: nothing to do
     } else {
         // ================= softmax / epilogue: one thread per row =================
         const int qt = warp >> 2;
@@ -331,30 +456,20 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status));
             if (!alive) break;
             tc_fence_after();
-            float s[kBlockKeys];
-#pragma unroll
-            for (int c0 = 0; c0 < kBlockKeys; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + C::S_COL(qt, j % C::SB) + c0, v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) s[c0 + i] = v[i];
-            }
-            const int key0 = p0 * kPage + j * kBlockKeys;
+            float s[C::BK];
+            tmem_ld_row<C::BK>(tmem + lane_base + C::S_COL(qt, j % C::SB), s);
+            const int key0 = p0 * kPage + j * C::BK;
             // raw-score max; masking only where the block reaches the query
             // block or the request's end (the same arithmetic either way, so a
             // row's bits do not depend on n_q)
-            float mraw = -INFINITY;
-            if (key0 + kBlockKeys > len - a.n_q) {
+            if (key0 + C::BK > len - a.n_q) {
 #pragma unroll
-                for (int c = 0; c < kBlockKeys; ++c) {
+                for (int c = 0; c < C::BK; ++c) {
                     const int key = key0 + c;
                     if (!(rvalid && key <= qpos && key < len)) s[c] = -INFINITY;
-                    mraw = fmaxf(mraw, s[c]);
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBlockKeys; ++c) mraw = fmaxf(mraw, s[c]);
             }
+            const float mraw = max_tree<C::BK>(s);
             const float mb = mraw * a.scale_log2;
             // grow the reference max only when it rises by more than 2^8
             // (rare after the first block); O is rescaled in TMEM
@@ -381,34 +496,42 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             // slots past the request's end (or of pages past it) may hold any
             // bytes: zero their V rows so that 0 * NaN never reaches P V
             const int nvalid = len - key0;
-            if (nvalid < kBlockKeys && qt == 0) {
+            if (nvalid < C::BK && qt == 0) {
                 uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
-                for (int e = r; e < (kBlockKeys - nvalid) * (D / 8); e += kTileRows) {
+                for (int e = r; e < (C::BK - nvalid) * (D / 8); e += kTileRows) {
                     const int kr = nvalid + e / (D / 8), c = e % (D / 8);
-                    *reinterpret_cast<uint4 *>(vt + sw128(kr, c, kBlockKeys)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(vt + sw128(kr, c, C::BK)) = make_uint4(0, 0, 0, 0);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             // P (bf16 pairs) over the first half of this block's S buffer;
-            // the buffer's previous P was read by block j - 2's P V, which the
-            // MMA pipe finished before it wrote this block's S
+            // the buffer's previous P was read by block j - SB's P V, which the
+            // MMA pipe finished before it wrote this block's S.  The block's P
+            // sum in four interleaved partial sums (a fixed order, short
+            // dependent chains).
+            {
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < kBlockKeys / 32; ++h) {
-                float pk[16];
+                for (int h = 0; h < C::BK / 32; ++h) {
+                    float pk[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0v = ex2(fmaf(s[h * 32 + 2 * c], a.scale_log2, nms));
-                    const float p1v = ex2(fmaf(s[h * 32 + 2 * c + 1], a.scale_log2, nms));
-                    l += p0v;
-                    l += p1v;
-                    pk[c] = __uint_as_float(pack_bf16(p0v, p1v));
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0v = ex2(fmaf(s[h * 32 + 2 * c], a.scale_log2, nms));
+                        const float p1v = ex2(fmaf(s[h * 32 + 2 * c + 1], a.scale_log2, nms));
+                        ls[(2 * c) & 3] += p0v;
+                        ls[(2 * c + 1) & 3] += p1v;
+                        pk[c] = __uint_as_float(pack_bf16(p0v, p1v));
+                    }
+                    tmem_st16_nowait(tmem + lane_base + C::S_COL(qt, j % C::SB) + h * 16, pk);
                 }
-                tmem_st16(tmem + lane_base + C::S_COL(qt, j % C::SB) + h * 16, pk);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             }
             tc_fence_before();
             mbar_arrive(&p_ready[qt * 2 + j % C::SB]);
             o_touched = true;
         }
+        pdl_trigger();  // the main loop is done: the next kernel may be scheduled
         // epilogue: the whole warp waits for the last P V and reads O
         float *dst = nullptr;
         int64_t row = 0;

@@ -205,18 +205,21 @@ def test_verify_short_request_reports_bad_index():
     assert st == 3 and np.all(got[0] == 0) and np.all(np.isfinite(got[1]))
 
 
-def test_verify_rows_invariant_to_block_and_batch():
+@pytest.mark.parametrize("grp,n_q,rows_i", [(4, 33, (0, 7, 32)), (8, 40, (0, 31, 32, 39))])
+def test_verify_rows_invariant_to_block_and_batch(grp, n_q, rows_i):
     """A query's output is the same bits whether it is verified alone (n_q =
-    1, batch 1) or as row i of a block of 33 in a batch of 3: split
-    boundaries are fixed by position and rows are independent."""
-    rng = np.random.default_rng(11)
-    d, hkv, grp, n_q = 128, 2, 4, 33
+    1, batch 1, one 128-row tile) or as row i of a block of n_q in a batch of
+    3 (two tiles; with grp 8 and 40 queries 320 rows, so queries 32.. sit in
+    a second row block): split boundaries are fixed by position and rows are
+    independent."""
+    rng = np.random.default_rng(11 + grp)
+    d, hkv = 128, 2
     lens = [5000, 9000, 333]
     full, hf = H.full_cache(rng, lens, hkv, d)
     qn, qd = q_bf16(rng, (3, n_q, hkv * grp, d))
     blk, _ = gpu_verify(full, qd, 0.088, max(lens))
     m = vc()
-    for i in (0, 7, 32):
+    for i in rows_i:
         # request 1 alone, truncated so that query i is the last position
         L = lens[1] - n_q + i + 1
         one = m.PagedKV(full.k_pages, full.v_pages, full.block_table[1:2].contiguous(),

@@ -2,7 +2,8 @@
 host memory into a ring of slots while other requests draft) gives, at every
 tick and layer, verification rows bit-identical to vc_verify_attn over a
 device-resident KV_full and draft rows equal to vc_draft_attn over KV_comp
-(up to the different split of pages over warps).  A missing or misplaced
+within the attention tolerance (the two launches split pages over warps
+differently).  A missing or misplaced
 wait on a staged layer would read another job's pages: the ring reuses slots
 within the run.  Lock step (one slot for every request's KV_full) and a
 schedule with idle requests are checked the same way."""
@@ -65,7 +66,9 @@ def run_and_check(rig, roles, x, slots):
                 assert np.array_equal(ov[b], rv[l][b]), (t, l, b)
                 n_ver += 1
             elif roles[t, b] == 0:
-                assert H.row_err(od[b], rd[l][b]) <= 1e-4, (t, l, b)
+                # different page-to-warp splits round P to fp16 against
+                # different running maxima: equal within the oracle tolerance
+                assert H.row_err(od[b], rd[l][b]) <= H.TOL, (t, l, b)
                 n_dr += 1
     assert n_ver > 0 and n_dr > 0
     assert r["link_GBps"] > 0 and r["stage_ms"] > 0 and r["wall_ms"] > 0
