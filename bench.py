@@ -3,8 +3,9 @@
 One step = one VeriCache round of one attention layer for the 8B-shaped
 workload (batch 8, 32 query / 8 kv heads, head_dim 128, 32768-token context,
 KV_comp = every token at 2-bit group-32):
-  for i in 0..x-1:  vc_compress   append drafted token i to KV_comp (2-bit)
-                    vc_draft_attn decode attention over KV_comp (N + i + 1)
+  for i in 0..x-1:  vc_draft_step append drafted token i's K / V rows to
+                                  KV_comp (2-bit) and attend over its
+                                  N + i + 1 entries, one launch (+ combine)
   vc_verify_attn    the x = 32 block queries over bf16 KV_full (causal):
                     the pending token and the first x - 1 drafts, whose
                     predictions check all x drafts (the workload's "verify
@@ -169,9 +170,13 @@ def build(w, seed, device):
     vc.compress(full, offs, idx, comp, N)
     q = torch.randn((x, B, hq, d), generator=g, device=device).to(torch.bfloat16)
     qv = q.permute(1, 0, 2, 3).contiguous()    # [B][x][Hq][D] verify block (same queries as the drafts)
+    # the K / V rows of drafted token i (position N + i), as a model step
+    # hands them over: [x][B][Hkv][D]
+    kn = torch.stack([kp[table[:, (N + i) // 16].long(), :, (N + i) % 16, :] for i in range(x)]).contiguous()
+    vn = torch.stack([vp[table[:, (N + i) // 16].long(), :, (N + i) % 16, :] for i in range(x)]).contiguous()
     lm = torch.randn((d, w["vocab"]), generator=g, device=device) * w["lm_std"]
     drafts = torch.randint(0, w["vocab"], (B, x), generator=g, device=device).to(torch.int32)
-    return dict(full=full, comp=comp, q=q, qv=qv, lm=lm, drafts=drafts, oc=oc, L=L)
+    return dict(full=full, comp=comp, q=q, qv=qv, kn=kn, vn=vn, lm=lm, drafts=drafts, oc=oc, L=L)
 
 
 class Round:
@@ -185,9 +190,7 @@ class Round:
         self.B, self.N, self.x, self.hq, self.d = B, N, x, hq, d
         full, comp = st["full"], st["comp"]
         self.scale = 1.0 / math.sqrt(d)
-        # per draft step: append offsets / lengths (device, built once)
-        self.app_offs = torch.arange(0, B + 1, dtype=torch.int32, device=device)
-        self.app_idx = [torch.full((B,), N + i, dtype=torch.int32, device=device) for i in range(x)]
+        # per draft step: the new entry's KV_comp position and the attended lengths
         self.app_start = [torch.full((B,), N + i, dtype=torch.int32, device=device) for i in range(x)]
         self.comp_i = [vc.PagedKV(comp.k_pages, comp.v_pages, comp.block_table,
                                   torch.full((B,), N + i + 1, dtype=torch.int32, device=device),
@@ -202,9 +205,9 @@ class Round:
         self.emit = torch.empty((B, x + 1), dtype=torch.int32, device=device)
         self.aws = torch.empty(vc.accept_workspace_bytes(B, x, w["vocab"], d), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        # kernels per round: x x (append + draft + draft reduce), verify + its
+        # kernels per round: x x (draft step + its reduce), verify + its
         # reduce, accept's mean + logits + finalize
-        self.launches = x * (1 + 2) + 2 + 3
+        self.launches = x * 2 + 2 + 3
 
     def run(self, q=None, qv=None, ev=None, full=None, verify_wait=None):
         import torch
@@ -213,12 +216,11 @@ class Round:
         qv = st["qv"] if qv is None else qv
         full = st["full"] if full is None else full
         for i in range(self.x):
-            vc.compress(full, self.app_offs, self.app_idx[i], st["comp"], 1, comp_start=self.app_start[i],
-                        status=self.status)
-            if ev is not None:
+            if ev is not None and i in ev:
                 ev[i][0].record()
-            vc.draft_attn(q[i], self.comp_i[i], self.scale, self.dout, self.N + self.x, self.dws, status=self.status)
-            if ev is not None:
+            vc.draft_step(q[i], self.comp_i[i], st["kn"][i], st["vn"][i], self.app_start[i], self.scale, self.dout,
+                          self.N + self.x, self.dws, status=self.status)
+            if ev is not None and i in ev:
                 ev[i][1].record()
         if verify_wait is not None:
             torch.cuda.current_stream().wait_event(verify_wait)
@@ -230,15 +232,14 @@ class Round:
     def stage_calls(self):
         """The round split into its stages (each a list of API calls)."""
         vc, st = self.vc, self.st
-        comp = [lambda i=i: vc.compress(st["full"], self.app_offs, self.app_idx[i], st["comp"], 1,
-                                        comp_start=self.app_start[i], status=self.status) for i in range(self.x)]
-        draft = [lambda i=i: vc.draft_attn(st["q"][i], self.comp_i[i], self.scale, self.dout, self.N + self.x,
-                                           self.dws, status=self.status) for i in range(self.x)]
+        draft = [lambda i=i: vc.draft_step(st["q"][i], self.comp_i[i], st["kn"][i], st["vn"][i], self.app_start[i],
+                                           self.scale, self.dout, self.N + self.x, self.dws, status=self.status)
+                 for i in range(self.x)]
         verify = [lambda: vc.verify_attn(st["qv"], st["full"], self.scale, self.vout, st["L"], self.vws,
                                          status=self.status)]
         accept = [lambda: vc.accept(self.vout, st["lm"], st["drafts"], self.ver, self.alen, self.emit, self.aws,
                                     hidden_group=self.hq)]
-        return {"compress_append": comp, "draft_attn": draft, "verify_attn": verify, "accept": accept}
+        return {"draft_step": draft, "verify_attn": verify, "accept": accept}
 
     def breakdown(self, reps=5):
         """Per-stage device time: each stage's calls captured in a CUDA graph
@@ -408,11 +409,15 @@ def main():
     assert rnd.status.item() == 0, "device status %d" % rnd.status.item()
 
     # the whole round as one CUDA graph: the host launches it once per step.
-    # Event-record nodes around each draft call time the draft kernels of the
-    # timed replays themselves (the last replay's values are read after).
+    # Event-record nodes around three of the draft calls (a quarter, half and
+    # three quarters into the round) time the draft kernels of the timed
+    # replays themselves (the last replay's values are read after).  Event
+    # nodes split the graph's programmatic launch edges and cost a few us
+    # each, so the other calls carry none.
+    timed_calls = (x // 4, x // 2, (3 * x) // 4)
     try:
-        pairs = [(torch.cuda.Event(enable_timing=True, external=True),
-                  torch.cuda.Event(enable_timing=True, external=True)) for _ in range(x)]
+        pairs = {i: (torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True)) for i in timed_calls}
     except TypeError:
         pairs = None
     graph = capture(lambda: rnd.run(ev=pairs))
@@ -431,13 +436,15 @@ def main():
     ms_step = t_ms / args.steps
     stages = rnd.breakdown()
     # algorithmic bytes of call i: N + i + 1 entries
-    bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in range(x)]))
     if pairs is not None:
-        draft_src = "CUDA events around each draft call inside the timed graph replays"
-        t_draft = float(np.mean([a.elapsed_time(b) for (a, b) in pairs])) * 1e-3
+        draft_src = ("CUDA events around draft calls %s of 0..%d inside the timed graph replays"
+                     % (list(timed_calls), x - 1))
+        bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in timed_calls]))
+        t_draft = float(np.mean([pairs[i][0].elapsed_time(pairs[i][1]) for i in timed_calls])) * 1e-3
     else:
         draft_src = "CUDA events around replays of a graph of the round's draft calls"
-        t_draft = stages["draft_attn"]["us_per_call"] * 1e-6
+        bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in range(x)]))
+        t_draft = stages["draft_step"]["us_per_call"] * 1e-6
     peak, peak_kind = peaks()
     achieved = bytes_avg / t_draft / 1e9
     value = ws * B * x / (ms_step * 1e-3)
@@ -470,7 +477,7 @@ def main():
                 "stages": stages,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                             "kernel": "draft_kernel<2,128> + draft_reduce_kernel"},
+                             "kernel": "draft_kernel<2,128> (incl. the step's append) + draft_reduce_kernel"},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": rnd.launches * args.steps,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)

@@ -196,6 +196,25 @@ VC_API vc_status vc_draft_attn(const void *q, int32_t num_q_heads, const vc_page
                         size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream);
 
 /*
+ * vc_draft_step -- one drafting step: each request's new entry (the K and V
+ * rows of the token just produced, "The Core Idea" item 2: each drafted
+ * token's state is appended to KV_comp) is written into KV_comp at position
+ * slot[b] in comp's format (quantised exactly as vc_compress would, or
+ * copied for bits == 16), then the draft attention of vc_draft_attn runs
+ * over the comp->seq_lens[b] entries, which should include slot[b].  One
+ * launch: the block that reads slot[b]'s page writes the entry first.
+ *  k_new, v_new  device bf16 [batch][num_kv_heads][head_dim]
+ *  slot          device int32 [batch]; 0 <= slot[b] < seq_lens[b] (else
+ *                VC_ERR_INVALID_ARG in dev_status and nothing written for b)
+ * Other arguments and the workspace are vc_draft_attn's.  The KV_comp bytes
+ * equal those of vc_compress appending the same rows at the same position.
+ */
+VC_API vc_status vc_draft_step(const void *q, int32_t num_q_heads, const vc_paged_kv *comp, const void *k_new,
+                               const void *v_new, const int32_t *slot, float softmax_scale, float *out,
+                               int32_t max_seq_len, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               vc_stream_t stream);
+
+/*
  * vc_draft_attn_static -- vc_draft_attn without a caller workspace.
  * The pages have no counterpart of this entry point.  It is for callers that
  * cannot allocate device memory where they call the library: a plugin run by

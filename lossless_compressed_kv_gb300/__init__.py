@@ -71,6 +71,8 @@ _SIG = {
     "vc_draft_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32]),
     "vc_draft_attn": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32, _P,
                                 C.c_size_t, _P, _P]),
+    "vc_draft_step": (C.c_int, [_P, C.c_int32, C.POINTER(PagedKVStruct), _P, _P, _P, C.c_float, _P, C.c_int32, _P,
+                                C.c_size_t, _P, _P]),
     "vc_verify_workspace_bytes": (C.c_size_t, [C.POINTER(PagedKVStruct), C.c_int32, C.c_int32, C.c_int32]),
     "vc_verify_attn": (C.c_int, [_P, C.c_int32, C.c_int32, C.POINTER(PagedKVStruct), C.c_float, _P, C.c_int32,
                                  _P, C.c_size_t, _P, _P]),
@@ -227,6 +229,17 @@ def draft_attn(q, comp: PagedKV, softmax_scale: float, out, max_seq_len: int, wo
     _check(_lib.vc_draft_attn(_ptr(q), int(q.shape[-2]), C.byref(cs), float(softmax_scale), _ptr(out),
                               int(max_seq_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _ptr(status), _stream(stream)), "vc_draft_attn")
+
+
+def draft_step(q, comp: PagedKV, k_new, v_new, slot, softmax_scale: float, out, max_seq_len: int, workspace,
+               status=None, stream=None):
+    """vc_draft_step: write each request's new entry (bf16 K / V rows
+    [B][Hkv][D]) to KV_comp position slot[b], then draft attention."""
+    cs = comp.struct()
+    _check(_lib.vc_draft_step(_ptr(q), int(q.shape[1]), C.byref(cs), _ptr(k_new), _ptr(v_new), _ptr(slot),
+                              float(softmax_scale), _ptr(out), int(max_seq_len), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)),
+           "vc_draft_step")
 
 
 def verify_workspace_bytes(full: PagedKV, n_q: int, num_q_heads: int, max_seq_len: int) -> int:

@@ -12,7 +12,8 @@ vc_status compress(const vc_paged_kv *full, const int32_t *kept_offsets, const i
 bool draft_supported(const vc_kv_format &f, int hq);
 size_t draft_workspace(const vc_paged_kv &c, int hq, int max_seq_len);
 cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scale, float *out,
-                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
+                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st,
+                         const void *k_new = nullptr, const void *v_new = nullptr, const int32_t *slot = nullptr);
 bool verify_supported(const vc_kv_format &f, int hq, int n_q);
 size_t verify_workspace(const vc_paged_kv &f, int n_q, int hq, int max_seq_len);
 cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, float scale, float *out,
@@ -102,6 +103,19 @@ vc_status vc_draft_attn(const void *q, int32_t num_q_heads, const vc_paged_kv *c
     if (!workspace || workspace_bytes < need) return VC_ERR_WORKSPACE;
     return from_cuda(draft_launch(q, num_q_heads, *comp, softmax_scale, out, max_seq_len > 0 ? max_seq_len : 1,
                                   workspace, dev_status, (cudaStream_t)stream));
+}
+
+vc_status vc_draft_step(const void *q, int32_t num_q_heads, const vc_paged_kv *comp, const void *k_new,
+                        const void *v_new, const int32_t *slot, float softmax_scale, float *out,
+                        int32_t max_seq_len, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                        vc_stream_t stream) {
+    if (!q || !out || !k_new || !v_new || !slot || !paged_ok(comp) || max_seq_len < 0) return VC_ERR_INVALID_ARG;
+    if (!bits_ok(comp->fmt.bits) || !draft_supported(comp->fmt, num_q_heads)) return VC_ERR_UNSUPPORTED;
+    if (comp->batch == 0) return VC_OK;
+    const size_t need = draft_workspace(*comp, num_q_heads, max_seq_len > 0 ? max_seq_len : 1);
+    if (!workspace || workspace_bytes < need) return VC_ERR_WORKSPACE;
+    return from_cuda(draft_launch(q, num_q_heads, *comp, softmax_scale, out, max_seq_len > 0 ? max_seq_len : 1,
+                                  workspace, dev_status, (cudaStream_t)stream, k_new, v_new, slot));
 }
 
 size_t vc_verify_workspace_bytes(const vc_paged_kv *full, int32_t n_q, int32_t num_q_heads,

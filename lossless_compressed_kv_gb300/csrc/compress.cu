@@ -14,6 +14,7 @@
 // writes both blocks back whole.  Slots outside the range keep their bytes.
 // bf16 token drop: one warp per (kept entry, kv head) copies the row.
 #include "comp_layout.cuh"
+#include "quant_row.cuh"
 #include "vc_internal.cuh"
 
 namespace vc {
@@ -34,70 +35,6 @@ struct CompressArgs {
     int hkv;
     int32_t *status;
 };
-
-__device__ inline uint16_t f16_store(float f) {  // saturate to +-65504, round to nearest even
-    f = fminf(fmaxf(f, -65504.0f), 65504.0f);
-    return __half_as_ushort(__float2half_rn(f));
-}
-
-// Quantise one row (D channels, CPL = D/32 consecutive ones per lane):
-// codes of the lane's channels, and the fp16 scale / zero of its group.
-template <int BITS, int D>
-__device__ void quantize_row(const uint16_t (&x)[D / 32], uint8_t (&code)[D / 32], uint16_t &sh, uint16_t &zh) {
-    constexpr int CPL = D / 32;             // channels per lane
-    constexpr int LPG = kGroup / CPL;       // lanes per group
-    constexpr int QMAX = (1 << BITS) - 1;
-    float v[CPL];
-    float mn, mx;
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) v[i] = bf16_bits_to_f32(x[i]);
-    mn = v[0];
-    mx = v[0];
-#pragma unroll
-    for (int i = 1; i < CPL; ++i) {
-        mn = fminf(mn, v[i]);
-        mx = fmaxf(mx, v[i]);
-    }
-#pragma unroll
-    for (int o = 1; o < LPG; o <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    mn = __fadd_rn(mn, 0.0f);  // -0 -> +0
-    const float range = __fsub_rn(mx, mn);
-    const float sdot = __fdiv_rn(range, (float)QMAX);
-    sh = f16_store(sdot);
-    zh = f16_store(mn);
-    const float s = __half2float(__ushort_as_half(sh));
-    const float z = __half2float(__ushort_as_half(zh));
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        int c = 0;
-        if (s != 0.0f) {
-            float t = __fdiv_rn(__fsub_rn(v[i], z), s);
-            float r = rintf(t);
-            r = fminf(fmaxf(r, 0.0f), (float)QMAX);
-            c = (int)r;
-        }
-        code[i] = (uint8_t)c;
-    }
-}
-
-// Load the bf16 row a lane quantises: D/32 consecutive channels per lane.
-template <int D>
-__device__ inline void load_lane_row(const uint8_t *src, int lane, uint16_t (&x)[D / 32]) {
-    constexpr int CPL = D / 32;
-    if constexpr (CPL == 4) {
-        uint2 u = reinterpret_cast<const uint2 *>(src)[lane];
-        x[0] = u.x & 0xffff; x[1] = u.x >> 16; x[2] = u.y & 0xffff; x[3] = u.y >> 16;
-    } else if constexpr (CPL == 2) {
-        uint32_t u = reinterpret_cast<const uint32_t *>(src)[lane];
-        x[0] = u & 0xffff; x[1] = u >> 16;
-    } else {
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) x[i] = reinterpret_cast<const uint16_t *>(src)[lane * CPL + i];
-    }
-}
 
 // Replace the `width` bits at bit offset `off` of a shared-memory block.
 __device__ inline void put_bits(uint32_t *blk, int off, int width, uint32_t v) {
@@ -147,8 +84,8 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
         fp = (t >= 0 && t < a.f_lens[b] && t / kPage < a.f_maxb) ? a.f_table[(int64_t)b * a.f_maxb + t / kPage] : -1;
         if (fp >= 0 && fp < a.f_pages) {
             const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
-            load_lane_row<D>(a.fk + fbase, lane, xk);
-            load_lane_row<D>(a.fv + fbase, lane, xv);
+            qrow::load_lane_row<D>(a.fk + fbase, lane, xk);
+            qrow::load_lane_row<D>(a.fv + fbase, lane, xv);
         } else {
             fp = -1;
         }
@@ -170,7 +107,7 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
         for (int kv = 0; kv < 2; ++kv) {
             uint8_t code[CPL];
             uint16_t sh, zh;
-            quantize_row<BITS, D>(kv ? xv : xk, code, sh, zh);
+            qrow::quantize_row<BITS, D>(kv ? xv : xk, code, sh, zh);
 #pragma unroll
             for (int i = 0; i < CPL; ++i) {
                 const int ch = lane * CPL + i;
@@ -207,8 +144,7 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32) compress_token_kernel(CompressArgs a) {
     pdl_begin();
-    constexpr int CPL = D / 32, LPG = kGroup / CPL, G = D / kGroup;
-    constexpr int HB = 2 * D * (BITS + 1), CR = kPage * D * BITS / 8, RW = D * BITS / 32;  // K row words
+    constexpr int HB = 2 * D * (BITS + 1), RW = D * BITS / 32;  // K row words
     __shared__ uint32_t krow[kWarps][RW];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
@@ -232,53 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_token_kernel(CompressArg
     const int64_t fbase = ((int64_t)fp * a.hkv + h) * fhb + (int64_t)(t % kPage) * D * 2;
     uint8_t *gk = a.ck + ((int64_t)cp * a.hkv + h) * HB;
     uint8_t *gv = a.cv + ((int64_t)cp * a.hkv + h) * HB;
-    const int slot = slot_pos % kPage;
-    uint16_t xk[CPL], xv[CPL];
-    load_lane_row<D>(a.fk + fbase, lane, xk);
-    load_lane_row<D>(a.fv + fbase, lane, xv);
-    for (int i = lane; i < RW; i += 32) krow[warp][i] = 0u;
-    __syncwarp();
-#pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
-        uint8_t code[CPL];
-        uint16_t sh, zh;
-        quantize_row<BITS, D>(kv ? xv : xk, code, sh, zh);
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-            const int ch = lane * CPL + i;
-            if (kv == 0) {  // K: the token's own row, built in shared memory
-#pragma unroll
-                for (int pl = 0; pl < (BITS == 3 ? 2 : 1); ++pl) {
-                    const int w = BITS == 3 ? (pl ? 1 : 2) : BITS;
-                    const uint32_t v = BITS == 3 ? (pl ? code[i] >> 2 : code[i] & 3u) : code[i];
-                    const int o = layout::k_bit(BITS, D, slot, ch, pl) - slot * D * BITS;
-                    atomicOr(&krow[warp][o >> 5], v << (o & 31));
-                    (void)w;
-                }
-            } else {  // V: words shared with the page's other tokens
-#pragma unroll
-                for (int pl = 0; pl < (BITS == 3 ? 2 : 1); ++pl) {
-                    const int w = BITS == 3 ? (pl ? 1 : 2) : BITS;
-                    const uint32_t v = BITS == 3 ? (pl ? code[i] >> 2 : code[i] & 3u) : code[i];
-                    const int o = layout::v_bit(BITS, D, slot, ch, pl);
-                    const uint32_t m = ((1u << w) - 1u) << (o & 31);
-                    uint32_t *word = reinterpret_cast<uint32_t *>(gv) + (o >> 5);
-                    atomicAnd(word, ~m);
-                    atomicOr(word, (v << (o & 31)) & m);
-                }
-            }
-        }
-        if (lane % LPG == 0) {
-            const int gr = lane / LPG;
-            const int e = kv ? layout::v_param(G, slot, gr) : slot * G + gr;
-            uint16_t *par = reinterpret_cast<uint16_t *>((kv ? gv : gk) + CR);
-            par[e] = sh;
-            par[kPage * G + e] = zh;
-        }
-    }
-    __syncwarp();
-    uint32_t *kd = reinterpret_cast<uint32_t *>(gk + slot * (D * BITS / 8));
-    for (int i = lane; i < RW; i += 32) kd[i] = krow[warp][i];
+    qrow::append_entry<BITS, D>(a.fk + fbase, a.fv + fbase, gk, gv, slot_pos % kPage, lane, krow[warp]);
 }
 
 // bf16 token drop: one warp per (kept entry, kv head) copies the row.
@@ -311,7 +201,7 @@ __global__ void __launch_bounds__(kWarps * 32) compress_bf16_kernel(CompressArgs
 #pragma unroll
     for (int kv = 0; kv < 2; ++kv) {
         uint16_t x[CPL];
-        load_lane_row<D>((kv ? a.fv : a.fk) + fbase, lane, x);
+        qrow::load_lane_row<D>((kv ? a.fv : a.fk) + fbase, lane, x);
         uint16_t *d16 = reinterpret_cast<uint16_t *>((kv ? a.cv : a.ck) + cbase);
 #pragma unroll
         for (int i = 0; i < CPL; ++i) d16[lane * CPL + i] = x[i];

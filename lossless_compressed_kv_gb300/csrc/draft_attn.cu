@@ -139,7 +139,8 @@ size_t draft_workspace(const vc_paged_kv &c, int hq, int max_seq_len) {
 }
 
 cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scale, float *out,
-                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st) {
+                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st, const void *k_new,
+                         const void *v_new, const int32_t *slot) {
     const int d = c.fmt.head_dim, bits = c.fmt.bits;
     DraftArgs a;
     const Plan p = plan_any(bits, d, c.batch, c.fmt.num_kv_heads, max(max_seq_len, 1));
@@ -159,6 +160,9 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     a.ws_o = (float *)ws;
     a.ws_ml = a.ws_o + (size_t)c.batch * hq * p.n_splits * d;
     a.status = status;
+    a.k_new = (const uint16_t *)k_new;
+    a.v_new = (const uint16_t *)v_new;
+    a.slot = slot;
     cudaError_t e;
 #define VC_L(B_, D_) launch<B_, D_>(a, c.batch, st)
     if (d == 64) {

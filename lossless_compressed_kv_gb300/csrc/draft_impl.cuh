@@ -5,6 +5,7 @@
 
 #include <type_traits>
 
+#include "quant_row.cuh"
 #include "vc_internal.cuh"
 
 namespace vc {
@@ -22,6 +23,11 @@ struct DraftArgs {
     float *ws_o;   // [B][Hq][n_splits][D]
     float *ws_ml;  // [B][Hq][n_splits][2]
     int32_t *status;
+    // vc_draft_step: the step's new entry of every request (bf16 K and V
+    // rows, [B][Hkv][D]) is written to KV_comp position slot[b] before the
+    // attention; null for a plain draft call
+    const uint16_t *k_new = nullptr, *v_new = nullptr;
+    const int32_t *slot = nullptr;
 };
 
 template <int BITS, int D, int NW>
@@ -253,6 +259,35 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                                                                                                 : C::COMBINE)) +
                                          NW * C::NSTAGE) +
                  warp * C::NSTAGE;
+
+    if (a.k_new != nullptr) {
+        // vc_draft_step: the CTA whose pages hold slot[b] writes the step's
+        // new entry there before any copy of that page is issued; the other
+        // CTAs never read that page
+        const int s = a.slot[b];
+        if (split == 0 && kvh == 0 && (s < 0 || s >= len) && threadIdx.x == 0) report(a.status, VC_ERR_INVALID_ARG);
+        const int pi = (s >= 0 && s < len) ? s / kPage : -1;
+        if (pi >= p0 && pi < p1) {  // uniform over the CTA
+            if (warp == 0) {
+                __shared__ uint32_t krow[BITS == 16 ? 1 : D * BITS / 32];
+                const int id = pi < a.maxb ? trow[pi] : -1;
+                if (id >= 0 && id < a.n_pages) {
+                    const int64_t off = ((int64_t)id * a.hkv + kvh) * C::HB;
+                    const int64_t row = ((int64_t)b * a.hkv + kvh) * D;
+                    qrow::append_entry<BITS, D>(reinterpret_cast<const uint8_t *>(a.k_new + row),
+                                                reinterpret_cast<const uint8_t *>(a.v_new + row),
+                                                const_cast<uint8_t *>(a.kp) + off, const_cast<uint8_t *>(a.vp) + off,
+                                                s % kPage, lane, krow);
+                    // the generic-proxy writes must be visible to the bulk
+                    // copies (async proxy) issued after the barrier below
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                } else if (lane == 0) {
+                    report(a.status, VC_ERR_BAD_INDEX);
+                }
+            }
+            __syncthreads();
+        }
+    }
 
     // Page ids of this warp's pages, 32 at a time: lane i holds page 32 blk + i
     // (-1: past the warp's pages or not a valid page id).  Two blocks are kept

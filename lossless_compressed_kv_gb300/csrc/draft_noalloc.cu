@@ -22,7 +22,8 @@ namespace vc {
 size_t draft_workspace(const vc_paged_kv &c, int hq, int max_seq_len);
 bool draft_supported(const vc_kv_format &f, int hq);
 cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scale, float *out,
-                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
+                         int max_seq_len, void *ws, int32_t *status, cudaStream_t st,
+                         const void *k_new = nullptr, const void *v_new = nullptr, const int32_t *slot = nullptr);
 
 namespace {
 

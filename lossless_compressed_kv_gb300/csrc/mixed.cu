@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__
         const int rest = bid / m.v.n_splits;
         const int rb = rest % m.rb, bk = rest / m.rb;
         if (m.role[bk / m.v.hkv] != 1) return;
-        vtc::verify_tc_block<D, 1>(m.v, split, rb, bk, smem);
+        vtc::verify_tc_cta<D, 1>(m.v, split, rb, bk, smem);
     } else {
         bid -= m.n_verify_blocks;
         const int split = bid % m.d.n_splits;

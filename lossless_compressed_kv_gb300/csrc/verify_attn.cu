@@ -18,7 +18,7 @@ template <int D, int QT>
 __global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS, vtc::Cfg<D, QT>::MIN_CTAS) verify_kernel(const __grid_constant__ Args a) {
     pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem[];
-    vtc::verify_tc_block<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
+    vtc::verify_tc_cta<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
 }
 
 template <int D>

@@ -184,9 +184,21 @@ __device__ inline void tmem_ld_row(uint32_t taddr, float (&v)[N]) {
             : "memory");
     } else {
         asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+            "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+            "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+            "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63"
+            "}, [%64];\n\t"
             "tcgen05.wait::ld.sync.aligned;"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+              "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+              "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+              "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+              "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
             : "r"(taddr)
             : "memory");
     }
@@ -229,7 +241,10 @@ __device__ inline int sw128(int row, int c, int rows) {
 }
 
 // --- the CTA body ------------------------------------------------------------
-template <int D, int QT>
+// FULL: every tile of this row block holds rows (the tile count is then a
+// compile-time constant and the tile loops fold away); otherwise the last
+// row block skips its empty tiles.
+template <int D, int QT, bool FULL>
 __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb, int bk, uint8_t *smem_raw) {
     using C = Cfg<D, QT>;
     const uint32_t raw = smem_u32(smem_raw);
@@ -259,7 +274,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     const int nrows = a.n_q * a.grp;
     // tiles of this row block holding at least one row (the last row block
     // may fill fewer than QT): the others issue no MMA and run no softmax
-    const int nt = min(QT, ceil_div(max(0, min(a.rows_per_cta, nrows - rb * a.rows_per_cta)), kTileRows));
+    const int nt = FULL ? QT : min(QT, ceil_div(max(0, min(a.rows_per_cta, nrows - rb * a.rows_per_cta)), kTileRows));
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
     // ---- set-up: barriers, TMEM, Q tiles ----
@@ -409,17 +424,25 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 const uint8_t *kt = skv + st * 2 * C::KTILE;
                 if constexpr (C::SB == 2) {
                     // S of every tile for block j, then P V of block j - 1
-                    for (int qt = 0; qt < nt; ++qt) issue_s(j, qt, kt);
+#pragma unroll
+                    for (int qt = 0; qt < QT; ++qt)
+                        if (qt < nt) issue_s(j, qt, kt);
                     if (j >= 1) {
-                        for (int qt = 0; qt < nt; ++qt) wait_p(j - 1, qt);
+#pragma unroll
+                        for (int qt = 0; qt < QT; ++qt)
+                            if (qt < nt) wait_p(j - 1, qt);
                         if (!alive) break;
-                        for (int qt = 0; qt < nt; ++qt) issue_pv_tile(j - 1, qt);
+#pragma unroll
+                        for (int qt = 0; qt < QT; ++qt)
+                            if (qt < nt) issue_pv_tile(j - 1, qt);
                         finish_pv(j - 1);
                     }
                 } else {
                     // one S buffer per tile: a tile's P V of block j - 1 reads
                     // the buffer its S of block j then overwrites (in order)
-                    for (int qt = 0; qt < nt && alive; ++qt) {
+#pragma unroll
+                    for (int qt = 0; qt < QT; ++qt) {
+                        if (qt >= nt || !alive) continue;
                         if (j >= 1) {
                             wait_p(j - 1, qt);
                             if (!alive) break;
@@ -431,9 +454,13 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 }
             }
             if (nb > 0 && alive) {
-                for (int qt = 0; qt < nt; ++qt) wait_p(nb - 1, qt);
+#pragma unroll
+                for (int qt = 0; qt < QT; ++qt)
+                    if (qt < nt) wait_p(nb - 1, qt);
                 if (alive) {
-                    for (int qt = 0; qt < nt; ++qt) issue_pv_tile(nb - 1, qt);
+#pragma unroll
+                    for (int qt = 0; qt < QT; ++qt)
+                        if (qt < nt) issue_pv_tile(nb - 1, qt);
                     finish_pv(nb - 1);
                 }
             }
@@ -572,6 +599,16 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     tc_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+}
+
+// The CTA body, with the tile count folded for full row blocks.
+template <int D, int QT>
+__device__ __forceinline__ void verify_tc_cta(const Args &a, int split, int rb, int bk, uint8_t *smem_raw) {
+    const int rows_here = a.n_q * a.grp - rb * a.rows_per_cta;
+    if (QT == 1 || rows_here > (QT - 1) * kTileRows)  // every tile holds rows
+        verify_tc_block<D, QT, true>(a, split, rb, bk, smem_raw);
+    else
+        verify_tc_block<D, QT, false>(a, split, rb, bk, smem_raw);
 }
 
 // Combine the splits of one row in split order (fixed, so a row's result does
