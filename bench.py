@@ -1071,7 +1071,7 @@ def toy_main(args):
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("draft_attn.cu", "draft_impl.cuh", "vc_internal.cuh"):
+    for f in ("draft_attn.cu", "draft_impl.cuh", "vc_internal.cuh", "quant_row.cuh", "comp_layout.cuh"):
         with open(os.path.join(ROOT, "lossless_compressed_kv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
