@@ -25,6 +25,7 @@ constexpr int kColsT = 4;             // vocabulary columns per thread
 constexpr int kCols = kThreadsL * kColsT;
 constexpr int kRowsT = 16;            // prediction rows per CTA
 constexpr int kKT = 128;              // hidden dims staged per step
+constexpr int kKU = 8;                // hidden dims whose W loads are in flight together
 
 // Order-preserving key: value bits mapped to an unsigned order in the high
 // word (-0 folded onto +0 first), the complement of the id in the low word.
@@ -71,11 +72,12 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
             hs[k][r] = (r0 + r < rows && k < kn) ? h[(int64_t)(r0 + r) * d + k0 + k] : 0.0f;
         }
         __syncthreads();
-        // four hidden dims per step: the W loads of all four issued first
-        for (int kk = 0; kk < kn; kk += 4) {
-            float wv[4][kColsT];
+        // kKU hidden dims per step: the W loads of all of them issued first
+        // (enough loads in flight to cover the L2 latency)
+        for (int kk = 0; kk < kn; kk += kKU) {
+            float wv[kKU][kColsT];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kKU; ++u) {
                 const float *wp = w + (int64_t)(k0 + kk + u) * vocab + v0;
                 if (kk + u < kn && vec && v0 + kColsT <= vocab) {
                     const float4 q4 = *reinterpret_cast<const float4 *>(wp);
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kKU; ++u) {
                 if (kk + u >= kn) break;
                 float hv[kRowsT];
 #pragma unroll
