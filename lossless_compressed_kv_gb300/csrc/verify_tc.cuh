@@ -86,12 +86,17 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
     static_assert(STAGES >= 2, "K/V ring needs two stages");
     static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * KTILE;
-    static constexpr int NBAR = QT * 2 + QT * 2 + 2 + 2 * STAGES;  // s_ready, p_ready, pv_done, full, empty
+    static constexpr int NBAR = QT * 6 + 2 * STAGES;  // s_ready, p_ready, pv_done ([QT][2] each), full, empty
     static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
     static constexpr int TMEM_USED = QT * SB * BK + QT * D + (QTM ? QT * D / 2 : 0);
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= TMEM_LIMIT, "S, O (and Q) columns exceed TMEM");
-    static constexpr int THREADS = QT * 128 + 64;  // softmax warps + producer warp + MMA warp
+    // MMA-issuing warps: one per tile with two S buffers, so each tile's S /
+    // P V chain is issued independently (one thread issuing both tiles'
+    // MMAs in a fixed order stalls on the other tile's waits); one with a
+    // single S buffer
+    static constexpr int NMMA = SB == 2 ? QT : 1;
+    static constexpr int THREADS = QT * 128 + 32 + 32 * NMMA;  // softmax warps + producer + MMA warps
     static constexpr int MIN_CTAS = QT == 1 ? 2 : 1;  // resident CTAs per SM (TMEM: 256 columns each)
     __host__ __device__ static constexpr uint32_t S_COL(int qt, int buf) { return (uint32_t)(qt * SB + buf) * BK; }
     __host__ __device__ static constexpr uint32_t O_COL(int qt) { return (uint32_t)(QT * SB * BK + qt * D); }
@@ -254,14 +259,15 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *s_ready = bars;             // [QT][2]
     uint64_t *p_ready = bars + QT * 2;    // [QT][2]
-    uint64_t *pv_done = bars + QT * 4;    // [2]
-    uint64_t *full = bars + QT * 4 + 2;   // [STAGES]
+    uint64_t *pv_done = bars + QT * 4;    // [QT][2]
+    uint64_t *full = bars + QT * 6;       // [STAGES]
     uint64_t *empty = full + C::STAGES;   // [STAGES]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + C::NBAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp == QT * 4;
-    const bool mma_warp = warp == QT * 4 + 1;
+    const bool mma_warp = warp > QT * 4 && warp <= QT * 4 + C::NMMA;
+    const int mtile = warp - QT * 4 - 1;  // the tile an MMA warp issues for (two S buffers)
     const int b = bk / a.hkv, kvh = bk % a.hkv;
     const int len = a.lens[b];
     const bool len_ok = len >= a.n_q;
@@ -283,11 +289,11 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             mbar_init(&s_ready[i], 1);
             mbar_init(&p_ready[i], kTileRows);
         }
-        mbar_init(&pv_done[0], 1);
-        mbar_init(&pv_done[1], 1);
+        for (int i = 0; i < QT * 2; ++i) mbar_init(&pv_done[i], 1);
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            // a stage is free once every issuing thread's P V of it is done
+            mbar_init(&empty[i], C::SB == 2 ? nt : 1);
         }
         fence_mbar_init();
     }
@@ -380,8 +386,8 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             }
         }
     } else if (mma_warp) {
-        // ================= MMA issue (one thread) =================
-        if (lane == 0) {
+        // ================= MMA issue (one thread per MMA warp) =================
+        if (lane == 0 && (C::SB != 2 || mtile < nt)) {
             auto issue_s = [&](int j, int qt, const uint8_t *kt) {
                 if constexpr (C::QTM) {
 #pragma unroll
@@ -408,8 +414,14 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                     umma_ta(tmem + C::O_COL(qt), tmem + C::S_COL(qt, j % C::SB) + kk * 8,
                             sdesc(smem_u32(vt) + kk * 16 * 128, C::BK * 128, 1024), IPV, (j > 0 || kk > 0));
             };
-            auto finish_pv = [&](int j) {
-                umma_commit(&pv_done[j & 1]);
+            auto finish_pv = [&](int j, int qt) {  // the P V of tile qt (SB == 2) or of every tile
+                if constexpr (C::SB == 2) {
+                    umma_commit(&pv_done[qt * 2 + (j & 1)]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < QT; ++t)
+                        if (t < nt) umma_commit(&pv_done[t * 2 + (j & 1)]);
+                }
                 umma_commit(&empty[j % C::STAGES]);
             };
             auto wait_p = [&](int j, int qt) {
@@ -423,19 +435,13 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 tc_fence_after();
                 const uint8_t *kt = skv + st * 2 * C::KTILE;
                 if constexpr (C::SB == 2) {
-                    // S of every tile for block j, then P V of block j - 1
-#pragma unroll
-                    for (int qt = 0; qt < QT; ++qt)
-                        if (qt < nt) issue_s(j, qt, kt);
+                    // this warp's tile: S of block j, then P V of block j - 1
+                    issue_s(j, mtile, kt);
                     if (j >= 1) {
-#pragma unroll
-                        for (int qt = 0; qt < QT; ++qt)
-                            if (qt < nt) wait_p(j - 1, qt);
+                        wait_p(j - 1, mtile);
                         if (!alive) break;
-#pragma unroll
-                        for (int qt = 0; qt < QT; ++qt)
-                            if (qt < nt) issue_pv_tile(j - 1, qt);
-                        finish_pv(j - 1);
+                        issue_pv_tile(j - 1, mtile);
+                        finish_pv(j - 1, mtile);
                     }
                 } else {
                     // one S buffer per tile: a tile's P V of block j - 1 reads
@@ -450,18 +456,26 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                         }
                         issue_s(j, qt, kt);
                     }
-                    if (j >= 1 && alive) finish_pv(j - 1);
+                    if (j >= 1 && alive) finish_pv(j - 1, 0);
                 }
             }
             if (nb > 0 && alive) {
-#pragma unroll
-                for (int qt = 0; qt < QT; ++qt)
-                    if (qt < nt) wait_p(nb - 1, qt);
-                if (alive) {
+                if constexpr (C::SB == 2) {
+                    wait_p(nb - 1, mtile);
+                    if (alive) {
+                        issue_pv_tile(nb - 1, mtile);
+                        finish_pv(nb - 1, mtile);
+                    }
+                } else {
 #pragma unroll
                     for (int qt = 0; qt < QT; ++qt)
-                        if (qt < nt) issue_pv_tile(nb - 1, qt);
-                    finish_pv(nb - 1);
+                        if (qt < nt) wait_p(nb - 1, qt);
+                    if (alive) {
+#pragma unroll
+                        for (int qt = 0; qt < QT; ++qt)
+                            if (qt < nt) issue_pv_tile(nb - 1, qt);
+                        finish_pv(nb - 1, 0);
+                    }
                 }
             }
         }
@@ -504,7 +518,8 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             const float f = grow ? (m_used == -INFINITY ? 0.0f : ex2(m_used - mb)) : 1.0f;
             if (__any_sync(0xffffffffu, grow) && o_touched) {
                 // the previous block's P V must have landed before O is rescaled
-                alive = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status));
+                alive = __all_sync(0xffffffffu,
+                                   mbar_wait(&pv_done[qt * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1, a.status));
                 if (!alive) break;
                 tc_fence_after();
                 for (int c0 = 0; c0 < D; c0 += 16) {
@@ -521,9 +536,12 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             }
             const float nms = m_used == -INFINITY ? 0.0f : -m_used;
             // slots past the request's end (or of pages past it) may hold any
-            // bytes: zero their V rows so that 0 * NaN never reaches P V
+            // bytes: zero their V rows so that 0 * NaN never reaches P V.
+            // Every tile does it before it signals its P: a tile's P V is
+            // issued independently of the other tile's (zeros written twice
+            // are still zeros)
             const int nvalid = len - key0;
-            if (nvalid < C::BK && qt == 0) {
+            if (nvalid < C::BK) {
                 uint8_t *vt = skv + (j % C::STAGES) * 2 * C::KTILE + C::KTILE;
                 for (int e = r; e < (C::BK - nvalid) * (D / 8); e += kTileRows) {
                     const int kr = nvalid + e / (D / 8), c = e % (D / 8);
@@ -569,7 +587,8 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
         }
         bool have_o = nb > 0 && alive;
         if (have_o) {
-            have_o = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, a.status));
+            have_o = __all_sync(0xffffffffu,
+                                mbar_wait(&pv_done[qt * 2 + ((nb - 1) & 1)], ((nb - 1) >> 1) & 1, a.status));
             alive = have_o;
         }
         if (have_o) {
