@@ -56,11 +56,13 @@ __device__ inline void mbar_arrive(uint64_t *bar) {
 
 __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
-    // suspend-time hint 20 us: a poll returns within that time even if the
-    // phase is still open, so the caller's wall-clock bound holds
+    // no suspend-time hint: the poll returns after the hardware's own short
+    // time limit even if the phase is still open (so the caller's wall-clock
+    // bound holds), and a thread waiting on a phase that completes soon
+    // resumes sooner than with a long hint (measured: verify 3 %, draft 2 %)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)

@@ -295,14 +295,15 @@ def test_mixed_launch_matches_oracle_and_standalone():
             assert np.all(od[b] == 7.0)
 
 
-@pytest.mark.parametrize("bits", [2, 16])
-def test_garbage_past_the_end_never_leaks(bits):
+@pytest.mark.parametrize("bits,n_q", [(2, 9), (16, 9), (2, 40)])
+def test_garbage_past_the_end_never_leaks(bits, n_q):
     """Slots past a request's length may hold any bytes (memory reused from
     earlier work): fill them with NaN bit patterns and check that draft and
-    verification outputs stay finite and match the oracle."""
+    verification outputs stay finite and match the oracle (n_q 40: two
+    128-row tiles, each with its own MMA warp)."""
     rng = np.random.default_rng(77)
-    d, hkv, grp, n_q = 128, 2, 4, 9
-    lens = [37, 100, 16 * 9 + 3]
+    d, hkv, grp = 128, 2, 4
+    lens = [max(37, n_q), 100, 16 * 9 + 3]
     full, hf = H.full_cache(rng, lens, hkv, d)
     # poison every slot of the last page past each request's length
     for b, n in enumerate(lens):
