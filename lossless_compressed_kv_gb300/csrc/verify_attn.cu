@@ -7,7 +7,13 @@
 // and to itself ("KV Cache and Speculative Decoding": causal attention).
 // Launch: one CTA per (split of 4096 keys, row block, request x kv head);
 // a row block holds one 128-row MMA tile of (query, head) rows when there
-// are at most 128 rows, else two (more rows take further row blocks).
+// are at most 128 rows, else two (more rows take further row blocks).  When
+// the last row block would hold a single tile behind full two-tile blocks
+// (e.g. 40 queries x 8 heads = 256 + 64 rows), it runs as a second launch of
+// one-tile CTAs, which fit two to an SM instead of leaving half of a
+// two-tile CTA idle.
+#include <type_traits>
+
 #include "verify_tc.cuh"
 
 namespace vc {
@@ -18,7 +24,7 @@ template <int D, int QT>
 __global__ void __launch_bounds__(vtc::Cfg<D, QT>::THREADS, vtc::Cfg<D, QT>::MIN_CTAS) verify_kernel(const __grid_constant__ Args a) {
     pdl_wait();
     extern __shared__ __align__(1024) uint8_t smem[];
-    vtc::verify_tc_cta<D, QT>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
+    vtc::verify_tc_cta<D, QT>(a, blockIdx.x, blockIdx.y + a.rb0, blockIdx.z, smem);
 }
 
 template <int D>
@@ -27,8 +33,9 @@ __global__ void verify_reduce_kernel(const float *ws_o, const float *ws_ml, int 
     vtc::reduce_row<D>(ws_o, ws_ml, n_splits, blockIdx.x, out, threadIdx.x, blockDim.x);
 }
 
+// Row blocks rb0 .. rb0 + n_rb - 1 of QT tiles each.
 template <int D, int QT>
-cudaError_t launch(Args &a, int batch, cudaStream_t st) {
+cudaError_t launch(Args a, int batch, int rb0, int n_rb, cudaStream_t st) {
     using C = vtc::Cfg<D, QT>;
     static bool attr = false;
     if (!attr) {
@@ -36,7 +43,8 @@ cudaError_t launch(Args &a, int batch, cudaStream_t st) {
         attr = true;
     }
     a.rows_per_cta = QT * vtc::kTileRows;
-    dim3 grid(a.n_splits, ceil_div(a.n_q * a.grp, a.rows_per_cta), batch * a.hkv);
+    a.rb0 = rb0;
+    dim3 grid(a.n_splits, n_rb, batch * a.hkv);
     launch_pdl(verify_kernel<D, QT>, grid, C::THREADS, C::SMEM, st, a);
     return cudaGetLastError();
 }
@@ -117,21 +125,30 @@ cudaError_t verify_launch(const void *q, int n_q, int hq, const vc_paged_kv &f, 
     Args a;
     if (!verify_args(a, q, n_q, hq, f, scale, max(max_seq_len, 1), ws, status)) return cudaErrorInvalidValue;
     const int d = f.fmt.head_dim;
-    // one tile for up to 128 rows, else row blocks of two tiles (the last
-    // one may hold a single used tile): every configuration uses the same
-    // 64-key blocks, so a row's bits do not depend on n_q
-    const int tiles = min(2, ceil_div(n_q * a.grp, vtc::kTileRows));
-    cudaError_t e;
-    if (d == 64)
-        e = tiles == 1 ? launch<64, 1>(a, f.batch, st) : launch<64, 2>(a, f.batch, st);
-    else
-        e = tiles == 1 ? launch<128, 1>(a, f.batch, st) : launch<128, 2>(a, f.batch, st);
+    // one tile for up to 128 rows, else row blocks of two tiles; a last row
+    // block with one tile behind full two-tile blocks runs as one-tile CTAs.
+    // Every configuration uses the same 64-key blocks and rows as its own
+    // unit, so a row's bits do not depend on n_q or on the split
+    const int rows = n_q * a.grp, pair = 2 * vtc::kTileRows;
+    const int full2 = rows / pair, rem = rows % pair;
+    auto go = [&](auto dc) -> cudaError_t {
+        constexpr int D = decltype(dc)::value;
+        if (rows <= vtc::kTileRows) return launch<D, 1>(a, f.batch, 0, 1, st);
+        if (full2 >= 1 && rem > 0 && rem <= vtc::kTileRows) {
+            const cudaError_t e2 = launch<D, 2>(a, f.batch, 0, full2, st);
+            if (e2 != cudaSuccess) return e2;
+            return launch<D, 1>(a, f.batch, 2 * full2, 1, st);
+        }
+        return launch<D, 2>(a, f.batch, 0, ceil_div(rows, pair), st);
+    };
+    const cudaError_t e =
+        d == 64 ? go(std::integral_constant<int, 64>{}) : go(std::integral_constant<int, 128>{});
     if (e != cudaSuccess) return e;
-    const int rows = f.batch * n_q * hq;
+    const int out_rows = f.batch * n_q * hq;
     if (d == 64)
-        launch_pdl(verify_reduce_kernel<64>, rows, 64, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
+        launch_pdl(verify_reduce_kernel<64>, out_rows, 64, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
     else
-        launch_pdl(verify_reduce_kernel<128>, rows, 128, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
+        launch_pdl(verify_reduce_kernel<128>, out_rows, 128, 0, st, a.ws_o, a.ws_ml, a.n_splits, out);
     return cudaGetLastError();
 }
 

@@ -54,6 +54,7 @@ struct Args {
     float scale_log2;
     int n_splits;
     int rows_per_cta;   // QT * 128
+    int rb0 = 0;        // row block of the first CTA row (a launch may cover the last row blocks only)
     float *ws_o;        // [B][n_q][Hq][n_splits][D]
     float *ws_ml;       // [..][2]
     int32_t *status;

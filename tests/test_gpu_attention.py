@@ -179,6 +179,11 @@ VERIFY_CASES = [
     (64, 1, 8, 64, [64, 200]),
     (128, 2, 4, 40, [40, 4200, 8200]),   # 160 rows: two 128-row tiles
     (64, 1, 8, 24, [24, 700]),           # 192 rows: two tiles, head_dim 64
+    # a one-tile last row block behind two-tile blocks runs as a second
+    # launch of one-tile CTAs: 256 + 128, 256 + 94 and (head_dim 64) 256 + 24 rows
+    (128, 1, 8, 48, [48, 4300]),
+    (128, 2, 7, 50, [50, 51, 2000]),
+    (64, 2, 5, 56, [56, 5000]),
 ]
 
 
@@ -205,13 +210,15 @@ def test_verify_short_request_reports_bad_index():
     assert st == 3 and np.all(got[0] == 0) and np.all(np.isfinite(got[1]))
 
 
-@pytest.mark.parametrize("grp,n_q,rows_i", [(4, 33, (0, 7, 32)), (8, 40, (0, 31, 32, 39))])
+@pytest.mark.parametrize("grp,n_q,rows_i", [(4, 33, (0, 7, 32)), (8, 40, (0, 31, 32, 39)),
+                                             (7, 50, (0, 36, 37, 49))])
 def test_verify_rows_invariant_to_block_and_batch(grp, n_q, rows_i):
     """A query's output is the same bits whether it is verified alone (n_q =
     1, batch 1, one 128-row tile) or as row i of a block of n_q in a batch of
     3 (two tiles; with grp 8 and 40 queries 320 rows, so queries 32.. sit in
-    a second row block): split boundaries are fixed by position and rows are
-    independent."""
+    a one-tile row block of a second launch; with grp 7 and 50 queries,
+    query 36 straddles the two launches):
+    split boundaries are fixed by position and rows are independent."""
     rng = np.random.default_rng(11 + grp)
     d, hkv = 128, 2
     lens = [5000, 9000, 333]
