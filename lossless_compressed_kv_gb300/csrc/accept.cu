@@ -49,6 +49,19 @@ __global__ void group_mean_kernel(const float *hidden, int rows, int hg, int d, 
     h[i] = __fdiv_rn(s, (float)hg);
 }
 
+// Two rows' terms of one column in one packed instruction: lane i computes
+// fma(h_i, w, acc_i) rounded to nearest, the same as two scalar fmaf.
+__device__ __forceinline__ void fma_rows2(float &a0, float &a1, float h0, float h1, float w) {
+    asm("{\n\t.reg .b64 ra, rh, rw;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rh, {%2, %3};\n\t"
+        "mov.b64 rw, {%4, %4};\n\t"
+        "fma.rn.f32x2 ra, rh, rw, ra;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(h0), "f"(h1), "f"(w));
+}
+
 // STORE: write the logits [rows][vocab] instead of the argmax keys.
 template <bool STORE>
 __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h, int rows, const float *w, int d,
@@ -97,9 +110,9 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
                     hv[4 * i] = q4.x; hv[4 * i + 1] = q4.y; hv[4 * i + 2] = q4.z; hv[4 * i + 3] = q4.w;
                 }
 #pragma unroll
-                for (int r = 0; r < kRowsT; ++r)
+                for (int r = 0; r < kRowsT; r += 2)
 #pragma unroll
-                    for (int c = 0; c < kColsT; ++c) acc[r][c] = __fmaf_rn(hv[r], wv[u][c], acc[r][c]);
+                    for (int c = 0; c < kColsT; ++c) fma_rows2(acc[r][c], acc[r + 1][c], hv[r], hv[r + 1], wv[u][c]);
             }
         }
     }
