@@ -215,12 +215,13 @@ class Round:
         q = st["q"] if q is None else q
         qv = st["qv"] if qv is None else qv
         full = st["full"] if full is None else full
+        # ev: {call index: (event recorded before it or None, event after it or None)}
         for i in range(self.x):
-            if ev is not None and i in ev:
+            if ev is not None and i in ev and ev[i][0] is not None:
                 ev[i][0].record()
             vc.draft_step(q[i], self.comp_i[i], st["kn"][i], st["vn"][i], self.app_start[i], self.scale, self.dout,
                           self.N + self.x, self.dws, status=self.status)
-            if ev is not None and i in ev:
+            if ev is not None and i in ev and ev[i][1] is not None:
                 ev[i][1].record()
         if verify_wait is not None:
             torch.cuda.current_stream().wait_event(verify_wait)
@@ -409,18 +410,19 @@ def main():
     assert rnd.status.item() == 0, "device status %d" % rnd.status.item()
 
     # the whole round as one CUDA graph: the host launches it once per step.
-    # Event-record nodes around three of the draft calls (a quarter, half and
-    # three quarters into the round) time the draft kernels of the timed
-    # replays themselves (the last replay's values are read after).  Event
-    # nodes split the graph's programmatic launch edges and cost a few us
-    # each, so the other calls carry none.
-    timed_calls = (x // 4, x // 2, (3 * x) // 4)
+    # Two event-record nodes, before draft call x/4 and after call 3x/4 - 1,
+    # time the middle half of the draft calls of the timed replays
+    # themselves (the last replay's values are read after).  An event node
+    # splits the graph's programmatic launch edge and costs a few us, so the
+    # span carries only these two.
+    span = (x // 4, (3 * x) // 4)
     try:
-        pairs = {i: (torch.cuda.Event(enable_timing=True, external=True),
-                     torch.cuda.Event(enable_timing=True, external=True)) for i in timed_calls}
+        span_ev = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True))
+        marks = {span[0]: (span_ev[0], None), span[1] - 1: (None, span_ev[1])}
     except TypeError:
-        pairs = None
-    graph = capture(lambda: rnd.run(ev=pairs))
+        marks = None
+    graph = capture(lambda: rnd.run(ev=marks))
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
@@ -436,11 +438,11 @@ def main():
     ms_step = t_ms / args.steps
     stages = rnd.breakdown()
     # algorithmic bytes of call i: N + i + 1 entries
-    if pairs is not None:
-        draft_src = ("CUDA events around draft calls %s of 0..%d inside the timed graph replays"
-                     % (list(timed_calls), x - 1))
-        bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in timed_calls]))
-        t_draft = float(np.mean([pairs[i][0].elapsed_time(pairs[i][1]) for i in timed_calls])) * 1e-3
+    if marks is not None:
+        draft_src = ("CUDA events before draft call %d and after call %d of 0..%d inside the timed graph "
+                     "replays; per call = span / %d" % (span[0], span[1] - 1, x - 1, span[1] - span[0]))
+        bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in range(*span)]))
+        t_draft = span_ev[0].elapsed_time(span_ev[1]) * 1e-3 / (span[1] - span[0])
     else:
         draft_src = "CUDA events around replays of a graph of the round's draft calls"
         bytes_avg = float(np.mean([draft_bytes(w, N + i + 1) for i in range(x)]))
