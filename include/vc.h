@@ -38,6 +38,11 @@
  *    timed out) are written to the optional device word `dev_status` (first
  *    error wins; the caller zeroes it and reads it after synchronising); the
  *    offending element is skipped, never read or written out of bounds.
+ *  - A call with batch 0 (for vc_compress also one with max_kept 0) checks
+ *    its formats and sizes, launches nothing and returns VC_OK.  Pointers to
+ *    per-request data (queries, outputs, pools, block tables, lengths, kept
+ *    lists, hidden rows, drafts, uniforms) may then be NULL, as the data
+ *    pointer of a zero-size tensor is.
  *  - No C++ exception crosses this interface.
  *
  * Paged KV layout (page = 16 tokens, separate K and V pools)

@@ -37,10 +37,15 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
                          float scale, int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
 
 namespace {
+// The format and batch of a paged cache (all an empty batch needs).
+bool paged_fmt_ok(const vc_paged_kv *p) {
+    return p && p->batch >= 0 && p->fmt.num_kv_heads >= 1 && p->fmt.head_dim >= 32 && p->fmt.head_dim % 32 == 0 &&
+           p->fmt.head_dim <= VC_MAX_HEAD_DIM;
+}
+// ... and its pools, table and lengths, for a batch with requests.
 bool paged_ok(const vc_paged_kv *p) {
-    return p && p->k_pages && p->v_pages && p->block_table && p->seq_lens && p->batch >= 0 &&
-           p->max_blocks >= 1 && p->num_pages >= 1 && p->fmt.num_kv_heads >= 1 && p->fmt.head_dim >= 32 &&
-           p->fmt.head_dim % 32 == 0 && p->fmt.head_dim <= VC_MAX_HEAD_DIM;
+    return paged_fmt_ok(p) && p->k_pages && p->v_pages && p->block_table && p->seq_lens && p->max_blocks >= 1 &&
+           p->num_pages >= 1;
 }
 bool bits_ok(int b) { return b == 2 || b == 3 || b == 4 || b == 16; }
 vc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? VC_OK : VC_ERR_CUDA; }
@@ -65,8 +70,10 @@ size_t vc_page_bytes(const vc_kv_format *f) {
 vc_status vc_compress(const vc_paged_kv *full, const int32_t *kept_offsets, const int32_t *kept_idx,
                       const int32_t *comp_start, int32_t max_kept, const vc_paged_kv *comp,
                       int32_t *dev_status, vc_stream_t stream) {
-    if (!paged_ok(full) || !comp || !comp->k_pages || !comp->v_pages || !comp->block_table ||
-        comp->num_pages < 1 || comp->max_blocks < 1)
+    if (!paged_fmt_ok(full) || !comp) return VC_ERR_INVALID_ARG;
+    if (full->batch > 0 && max_kept > 0 &&
+        (!paged_ok(full) || !comp->k_pages || !comp->v_pages || !comp->block_table || comp->num_pages < 1 ||
+         comp->max_blocks < 1))
         return VC_ERR_INVALID_ARG;
     return compress(full, kept_offsets, kept_idx, comp_start, max_kept, comp, dev_status,
                     (cudaStream_t)stream);
@@ -80,9 +87,9 @@ size_t vc_select_workspace_bytes(int32_t batch, int32_t score_stride) {
 vc_status vc_select_kept(const vc_paged_kv *full, const float *scores, int32_t score_stride,
                          const int32_t *kept_offsets, int32_t sink, int32_t recent, int32_t *kept_idx,
                          void *workspace, size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream) {
-    if (!full || !full->seq_lens || !kept_offsets || !kept_idx || full->batch < 0 || sink < 0 || recent < 0 ||
-        score_stride < 1)
-        return VC_ERR_INVALID_ARG;
+    if (!full || full->batch < 0 || sink < 0 || recent < 0 || score_stride < 1) return VC_ERR_INVALID_ARG;
+    if (full->batch == 0) return VC_OK;
+    if (!full->seq_lens || !kept_offsets || !kept_idx) return VC_ERR_INVALID_ARG;
     if (!scores && (!paged_ok(full) || !full->k_pages)) return VC_ERR_INVALID_ARG;
     return select_kept(full, scores, score_stride, kept_offsets, sink, recent, kept_idx, workspace, workspace_bytes,
                        dev_status, (cudaStream_t)stream);
@@ -96,9 +103,10 @@ size_t vc_draft_workspace_bytes(const vc_paged_kv *comp, int32_t num_q_heads, in
 vc_status vc_draft_attn(const void *q, int32_t num_q_heads, const vc_paged_kv *comp, float softmax_scale,
                         float *out, int32_t max_seq_len, void *workspace, size_t workspace_bytes,
                         int32_t *dev_status, vc_stream_t stream) {
-    if (!q || !out || !paged_ok(comp) || max_seq_len < 0) return VC_ERR_INVALID_ARG;
+    if (!paged_fmt_ok(comp) || max_seq_len < 0) return VC_ERR_INVALID_ARG;
     if (!bits_ok(comp->fmt.bits) || !draft_supported(comp->fmt, num_q_heads)) return VC_ERR_UNSUPPORTED;
     if (comp->batch == 0) return VC_OK;
+    if (!q || !out || !paged_ok(comp)) return VC_ERR_INVALID_ARG;
     const size_t need = draft_workspace(*comp, num_q_heads, max_seq_len > 0 ? max_seq_len : 1);
     if (!workspace || workspace_bytes < need) return VC_ERR_WORKSPACE;
     return from_cuda(draft_launch(q, num_q_heads, *comp, softmax_scale, out, max_seq_len > 0 ? max_seq_len : 1,
@@ -109,9 +117,10 @@ vc_status vc_draft_step(const void *q, int32_t num_q_heads, const vc_paged_kv *c
                         const void *v_new, const int32_t *slot, float softmax_scale, float *out,
                         int32_t max_seq_len, void *workspace, size_t workspace_bytes, int32_t *dev_status,
                         vc_stream_t stream) {
-    if (!q || !out || !k_new || !v_new || !slot || !paged_ok(comp) || max_seq_len < 0) return VC_ERR_INVALID_ARG;
+    if (!paged_fmt_ok(comp) || max_seq_len < 0) return VC_ERR_INVALID_ARG;
     if (!bits_ok(comp->fmt.bits) || !draft_supported(comp->fmt, num_q_heads)) return VC_ERR_UNSUPPORTED;
     if (comp->batch == 0) return VC_OK;
+    if (!q || !out || !k_new || !v_new || !slot || !paged_ok(comp)) return VC_ERR_INVALID_ARG;
     const size_t need = draft_workspace(*comp, num_q_heads, max_seq_len > 0 ? max_seq_len : 1);
     if (!workspace || workspace_bytes < need) return VC_ERR_WORKSPACE;
     return from_cuda(draft_launch(q, num_q_heads, *comp, softmax_scale, out, max_seq_len > 0 ? max_seq_len : 1,
@@ -127,9 +136,10 @@ size_t vc_verify_workspace_bytes(const vc_paged_kv *full, int32_t n_q, int32_t n
 vc_status vc_verify_attn(const void *q, int32_t n_q, int32_t num_q_heads, const vc_paged_kv *full,
                          float softmax_scale, float *out, int32_t max_seq_len, void *workspace,
                          size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream) {
-    if (!q || !out || !paged_ok(full) || max_seq_len < 0 || n_q < 1) return VC_ERR_INVALID_ARG;
+    if (!paged_fmt_ok(full) || max_seq_len < 0 || n_q < 1) return VC_ERR_INVALID_ARG;
     if (!verify_supported(full->fmt, num_q_heads, n_q)) return VC_ERR_UNSUPPORTED;
     if (full->batch == 0) return VC_OK;
+    if (!q || !out || !paged_ok(full)) return VC_ERR_INVALID_ARG;
     const int msl = max_seq_len > 0 ? max_seq_len : 1;
     if (!workspace || workspace_bytes < verify_workspace(*full, n_q, num_q_heads, msl)) return VC_ERR_WORKSPACE;
     return from_cuda(verify_launch(q, n_q, num_q_heads, *full, softmax_scale, out, msl, workspace, dev_status,
@@ -145,11 +155,11 @@ vc_status vc_accept(const float *hidden, int32_t batch, int32_t n_pred, int32_t 
                     const float *lm_head, int32_t d, int32_t vocab, const int32_t *drafts, int32_t x,
                     int32_t *verified, int32_t *accept_len, int32_t *emitted, void *workspace,
                     size_t workspace_bytes, vc_stream_t stream) {
-    if (!hidden || !lm_head || !verified || !accept_len || !emitted || batch < 0 || n_pred < 1 ||
-        hidden_group < 1 || d < 1 || vocab < 1 || x < 0 || (x > 0 && !drafts))
+    if (!lm_head || batch < 0 || n_pred < 1 || hidden_group < 1 || d < 1 || vocab < 1 || x < 0)
         return VC_ERR_INVALID_ARG;
     if (n_pred != x && n_pred != x + 1) return VC_ERR_INVALID_ARG;
     if (batch == 0) return VC_OK;
+    if (!hidden || !verified || !accept_len || !emitted || (x > 0 && !drafts)) return VC_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < accept_workspace(batch, n_pred, vocab, d)) return VC_ERR_WORKSPACE;
     return from_cuda(accept_launch(hidden, batch, n_pred, hidden_group, lm_head, d, vocab, drafts, x, verified,
                                    accept_len, emitted, workspace, (cudaStream_t)stream));
@@ -164,10 +174,11 @@ vc_status vc_accept_sampled(const float *target_hidden, const float *draft_hidde
                             int32_t hidden_group, const float *lm_head, int32_t d, int32_t vocab, float temperature,
                             const int32_t *drafts, const float *u, const float *v, int32_t *accept_len,
                             int32_t *emitted, void *workspace, size_t workspace_bytes, vc_stream_t stream) {
-    if (!target_hidden || !lm_head || !accept_len || !emitted || !v || batch < 0 || x < 0 || hidden_group < 1 ||
-        d < 1 || vocab < 1 || !(temperature > 0.0f) || (x > 0 && (!draft_hidden || !drafts || !u)))
+    if (!lm_head || batch < 0 || x < 0 || hidden_group < 1 || d < 1 || vocab < 1 || !(temperature > 0.0f))
         return VC_ERR_INVALID_ARG;
     if (batch == 0) return VC_OK;
+    if (!target_hidden || !accept_len || !emitted || !v || (x > 0 && (!draft_hidden || !drafts || !u)))
+        return VC_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < accept_sampled_workspace(batch, x, vocab, d)) return VC_ERR_WORKSPACE;
     return from_cuda(accept_sampled_launch(target_hidden, draft_hidden, batch, x, hidden_group, lm_head, d, vocab,
                                            temperature, drafts, u, v, accept_len, emitted, workspace,
@@ -202,14 +213,15 @@ vc_status vc_mixed_attn(const int32_t *role, const void *q_draft, const vc_paged
                         const void *q_verify, int32_t n_q, const vc_paged_kv *full, float *out_verify,
                         int32_t num_q_heads, float softmax_scale, int32_t max_seq_len, void *workspace,
                         size_t workspace_bytes, int32_t *dev_status, vc_stream_t stream) {
-    if (!role || !q_draft || !q_verify || !out_draft || !out_verify || !paged_ok(comp) || !paged_ok(full) ||
-        max_seq_len < 0 || n_q < 1 || comp->batch != full->batch)
+    if (!paged_fmt_ok(comp) || !paged_fmt_ok(full) || max_seq_len < 0 || n_q < 1 || comp->batch != full->batch)
         return VC_ERR_INVALID_ARG;
     if (comp->fmt.num_kv_heads != full->fmt.num_kv_heads || comp->fmt.head_dim != full->fmt.head_dim)
         return VC_ERR_INVALID_ARG;
     if (!draft_supported(comp->fmt, num_q_heads) || !verify_supported(full->fmt, num_q_heads, n_q))
         return VC_ERR_UNSUPPORTED;
     if (comp->batch == 0) return VC_OK;
+    if (!role || !q_draft || !q_verify || !out_draft || !out_verify || !paged_ok(comp) || !paged_ok(full))
+        return VC_ERR_INVALID_ARG;
     const int msl = max_seq_len > 0 ? max_seq_len : 1;
     if (!workspace || workspace_bytes < mixed_workspace(*comp, *full, n_q, num_q_heads, msl))
         return VC_ERR_WORKSPACE;

@@ -240,7 +240,7 @@ cudaError_t launch_b(int d, const CompressArgs &a, int batch, int max_kept, cuda
 vc_status compress(const vc_paged_kv *full, const int32_t *kept_offsets, const int32_t *kept_idx,
                    const int32_t *comp_start, int32_t max_kept, const vc_paged_kv *comp,
                    int32_t *dev_status, cudaStream_t st) {
-    if (!full || !comp || !kept_offsets || !kept_idx || max_kept < 0) return VC_ERR_INVALID_ARG;
+    if (!full || !comp || max_kept < 0 || full->batch < 0) return VC_ERR_INVALID_ARG;
     if (full->fmt.bits != 16) return VC_ERR_UNSUPPORTED;
     const int d = full->fmt.head_dim, hkv = full->fmt.num_kv_heads, bits = comp->fmt.bits;
     if (comp->fmt.head_dim != d || comp->fmt.num_kv_heads != hkv || full->batch != comp->batch)
@@ -248,11 +248,10 @@ vc_status compress(const vc_paged_kv *full, const int32_t *kept_offsets, const i
     if (!(d == 32 || d == 64 || d == 128 || d == 256) || hkv < 1) return VC_ERR_UNSUPPORTED;
     if (!(bits == 2 || bits == 3 || bits == 4 || bits == 16)) return VC_ERR_UNSUPPORTED;
     if (bits != 16 && d % 64) return VC_ERR_UNSUPPORTED;  // quantised formats: head_dim 64, 128, 256
-    if (!full->k_pages || !full->v_pages || !full->block_table || !full->seq_lens || !comp->k_pages ||
-        !comp->v_pages || !comp->block_table || full->batch < 0 || full->max_blocks < 1 ||
-        comp->max_blocks < 1)
+    if (full->batch == 0 || max_kept == 0) return VC_OK;  // nothing is read or written
+    if (!kept_offsets || !kept_idx || !full->k_pages || !full->v_pages || !full->block_table || !full->seq_lens ||
+        !comp->k_pages || !comp->v_pages || !comp->block_table || full->max_blocks < 1 || comp->max_blocks < 1)
         return VC_ERR_INVALID_ARG;
-    if (full->batch == 0 || max_kept == 0) return VC_OK;
     CompressArgs a;
     a.fk = (const uint8_t *)full->k_pages;
     a.fv = (const uint8_t *)full->v_pages;

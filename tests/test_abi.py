@@ -85,6 +85,34 @@ def test_host_side_argument_errors(vc):
     assert L.vc_status_string(7) == b"workspace missing or too small"
 
 
+def test_empty_batch_is_ok_with_null_data(vc):
+    """Batch 0: formats and sizes are checked, nothing is launched, VC_OK;
+    the per-request pointers may be NULL (a zero-size tensor's data pointer).
+    No CUDA call happens on this path, so it runs without a GPU."""
+    L = vc.library()
+    comp = vc.PagedKVStruct(None, None, 0, None, None, 0, 0, vc.KVFormat(8, 128, 2))
+    full = vc.PagedKVStruct(None, None, 0, None, None, 0, 0, vc.KVFormat(8, 128, 16))
+    assert L.vc_draft_attn(None, 32, C.byref(comp), 1.0, None, 0, None, 0, None, None) == 0
+    assert L.vc_draft_step(None, 32, C.byref(comp), None, None, None, 1.0, None, 0, None, 0, None, None) == 0
+    assert L.vc_verify_attn(None, 32, 32, C.byref(full), 1.0, None, 0, None, 0, None, None) == 0
+    assert L.vc_mixed_attn(None, None, C.byref(comp), None, None, 25, C.byref(full), None, 32, 1.0, 0, None, 0,
+                           None, None) == 0
+    assert L.vc_compress(C.byref(full), None, None, None, 0, C.byref(comp), None, None) == 0
+    assert L.vc_select_kept(C.byref(full), None, 1, None, 64, 512, None, None, 0, None, None) == 0
+    fake = C.c_void_p(16)   # never dereferenced
+    assert L.vc_accept(None, 0, 33, 1, fake, 128, 32000, None, 32, None, None, None, None, 0, None) == 0
+    assert L.vc_accept_sampled(None, None, 0, 4, 1, fake, 128, 32000, 1.0, None, None, None, None, None, None, 0,
+                               None) == 0
+    # the formats are still checked: an unsupported width or block length is refused
+    bad = vc.PagedKVStruct(None, None, 0, None, None, 0, 0, vc.KVFormat(8, 128, 5))
+    assert L.vc_draft_attn(None, 32, C.byref(bad), 1.0, None, 0, None, 0, None, None) == 2
+    assert L.vc_verify_attn(None, 65, 32, C.byref(full), 1.0, None, 0, None, 0, None, None) == 2
+    assert L.vc_accept(None, 0, 5, 1, fake, 128, 32000, None, 32, None, None, None, None, 0, None) == 1
+    # ... and with requests, a NULL query is an argument error again
+    one = vc.PagedKVStruct(fake.value, fake.value, 4, fake.value, fake.value, 1, 1, vc.KVFormat(8, 128, 2))
+    assert L.vc_draft_attn(None, 32, C.byref(one), 1.0, fake, 16, fake, 1 << 20, None, None) == 1
+
+
 def test_oracle_and_library_share_no_code():
     """The CUDA sources and the oracle do not include or import each other."""
     csrc = os.path.join(ROOT, "lossless_compressed_kv_gb300", "csrc")

@@ -103,6 +103,36 @@ def test_draft_empty_request_gives_zeros():
     assert np.all(got[1] == 0) and np.all(np.isfinite(got[0]))
 
 
+def test_empty_batch_through_the_binding():
+    """Batch 0 with zero-size tensors (null data pointers): every call is a
+    no-op that returns VC_OK and leaves the status word and the pools alone."""
+    m = vc()
+    rng = np.random.default_rng(9)
+    d, hkv, hq = 128, 2, 8
+    full, _ = H.full_cache(rng, [40], hkv, d)
+    comp, _ = H.comp_cache(rng, 1, 64, hkv, d, 3)
+    k0, v0 = comp.k_pages.clone(), comp.v_pages.clone()
+    bt = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    ln = torch.zeros(0, dtype=torch.int32, device="cuda")
+    c0 = m.PagedKV(comp.k_pages, comp.v_pages, bt, ln, hkv, d, 3)
+    f0 = m.PagedKV(full.k_pages, full.v_pages, bt, ln, hkv, d, 16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e = lambda *shape, dt=torch.float32: torch.empty(shape, dtype=dt, device="cuda")
+    m.draft_attn(e(0, hq, d, dt=torch.bfloat16), c0, 0.1, e(0, hq, d), 64, e(0, dt=torch.uint8), status=st)
+    m.draft_step(e(0, hq, d, dt=torch.bfloat16), c0, e(0, hkv, d, dt=torch.int16), e(0, hkv, d, dt=torch.int16),
+                 e(0, dt=torch.int32), 0.1, e(0, hq, d), 64, e(0, dt=torch.uint8), status=st)
+    m.verify_attn(e(0, 9, hq, d, dt=torch.bfloat16), f0, 0.1, e(0, 9, hq, d), 64, e(0, dt=torch.uint8), status=st)
+    m.compress(f0, torch.zeros(1, dtype=torch.int32, device="cuda"), e(0, dt=torch.int32), c0, 0, status=st)
+    m.mixed_attn(e(0, dt=torch.int32), e(0, hq, d, dt=torch.bfloat16), c0, e(0, hq, d),
+                 e(0, 9, hq, d, dt=torch.bfloat16), f0, e(0, 9, hq, d), 0.1, 64, e(0, dt=torch.uint8), status=st)
+    lm = torch.zeros((d, 1000), dtype=torch.float32, device="cuda")
+    m.accept(e(0, 9, hq, d), lm, e(0, 8, dt=torch.int32), e(0, 9, dt=torch.int32), e(0, dt=torch.int32),
+             e(0, 9, dt=torch.int32), e(0, dt=torch.uint8), hidden_group=hq)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(comp.k_pages, k0) and torch.equal(comp.v_pages, v0)
+
+
 def test_draft_bad_page_id_reported():
     rng = np.random.default_rng(6)
     full, hf = H.full_cache(rng, [64], 1, 64)
