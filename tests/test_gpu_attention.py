@@ -72,6 +72,8 @@ DRAFT_CASES = [
     (3, 64, 1, 2, [129]),
     (4, 64, 2, 4, [1, 2, 3]),
     (16, 64, 1, 4, [513, 31]),
+    (2, 128, 1, 8, [3000, 47]),          # 2-bit with the full 8-head group
+    (3, 128, 4, 3, [1500, 16]),          # an odd group size
 ]
 
 
@@ -214,6 +216,7 @@ VERIFY_CASES = [
     (128, 1, 8, 48, [48, 4300]),
     (128, 2, 7, 50, [50, 51, 2000]),
     (64, 2, 5, 56, [56, 5000]),
+    (128, 1, 8, 64, [64, 3000]),         # the largest block: 64 queries x 8 heads = 512 rows
 ]
 
 
