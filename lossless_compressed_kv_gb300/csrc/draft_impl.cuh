@@ -244,16 +244,35 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     using C = Cfg<BITS, D, NW>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int p0 = split * a.chunk_pages;
+    const int32_t *trow = a.table + (int64_t)b * a.maxb;
+    // The loads that depend on nothing else go out together: the group's
+    // queries, the table entries of the warp's first 64 pages (read before
+    // the length is known: every entry below maxb is in bounds) and the
+    // length, so their latencies overlap at the start of the CTA.
+    constexpr int QW = (8 * D / 2 + NW * 32 - 1) / (NW * 32);  // query words per thread
+    uint32_t qreg[QW];
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.hq + kvh * a.grp) * D);
+#pragma unroll
+        for (int i = 0; i < QW; ++i) {
+            const int e = threadIdx.x + i * NW * 32;
+            qreg[i] = e < a.grp * D / 2 ? src[e] : 0u;
+        }
+    }
+    auto raw_id = [&](int kk) -> int {
+        const int pg = p0 + warp + NW * kk;
+        return pg < a.maxb ? trow[pg] : -1;
+    };
+    const int raw0 = raw_id(lane), raw1 = raw_id(32 + lane);
     const int len = a.lens[b];
     const int npages = ceil_div(len, kPage);
-    const int p0 = split * a.chunk_pages;
     const int p1 = min(p0 + a.chunk_pages, npages);
     uint8_t *ring = smem + warp * C::NSTAGE * C::STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE)) +
                      warp * C::NSTAGE;
     // pages of this warp: p0 + warp + NW k
     const int nw = p1 > p0 + warp ? ceil_div(p1 - (p0 + warp), NW) : 0;
-    const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
     int *sflag = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + (C::RING > C::COMBINE ? C::RING
                                                                                                 : C::COMBINE)) +
@@ -292,14 +311,12 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     // Page ids of this warp's pages, 32 at a time: lane i holds page 32 blk + i
     // (-1: past the warp's pages or not a valid page id).  Two blocks are kept
     // so the table reads run a block ahead of the copies.
+    auto valid_id = [&](int kk, int id) -> int { return (kk < nw && id >= 0 && id < a.n_pages) ? id : -1; };
     auto load_ids = [&](int blk) -> int {
         const int kk = 32 * blk + lane;
-        if (kk >= nw) return -1;
-        const int pg = p0 + warp + NW * kk;
-        const int id = pg < a.maxb ? trow[pg] : -1;
-        return (id >= 0 && id < a.n_pages) ? id : -1;
+        return kk < nw ? valid_id(kk, raw_id(kk)) : -1;
     };
-    int ids_cur = load_ids(0), ids_nxt = load_ids(1), cur_blk = 0;
+    int ids_cur = valid_id(lane, raw0), ids_nxt = valid_id(32 + lane, raw1), cur_blk = 0;
     auto issue = [&](int k) {  // every lane (k is warp-uniform); lane 0 issues the copies
         if ((k >> 5) != cur_blk) {
             ids_cur = ids_nxt;
@@ -334,9 +351,12 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     uint16_t *qs = reinterpret_cast<uint16_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE) + C::BARS);
     float *qsum = reinterpret_cast<float *>(qs + 8 * D);  // [8 heads][NG] group sums, pre-scaled
     {
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.hq + kvh * a.grp) * D);
         uint32_t *dst = reinterpret_cast<uint32_t *>(qs);
-        for (int e = threadIdx.x; e < 8 * D / 2; e += NW * 32) dst[e] = e < a.grp * D / 2 ? src[e] : 0u;
+#pragma unroll
+        for (int i = 0; i < QW; ++i) {
+            const int e = threadIdx.x + i * NW * 32;
+            if (e < 8 * D / 2) dst[e] = qreg[i];
+        }
         __syncthreads();
         if constexpr (BITS != 16) {
             for (int e = threadIdx.x; e < 8 * C::NG; e += NW * 32) {
