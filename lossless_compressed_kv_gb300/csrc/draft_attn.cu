@@ -40,22 +40,41 @@ constexpr int kWarps = 4;
 template <int BITS, int D>
 constexpr int kMinCtas = 4;
 
+// One CTA per (unit = request x kv head, context chunk), numbered units
+// 0 .. hi_units - 1 first (n_hi chunks of chunk_hi pages each), then the rest
+// (n_lo chunks of chunk_pages).
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(DraftArgs a) {
     pdl_begin();
     extern __shared__ __align__(128) uint8_t smem[];
-    draft::draft_block<BITS, D, kWarps>(a, blockIdx.x, blockIdx.y, blockIdx.z, smem);
+    int c = blockIdx.x, unit, split, chunk;
+    if (c < a.hi_units * a.n_hi) {
+        unit = c / a.n_hi;
+        split = c % a.n_hi;
+        chunk = a.chunk_hi;
+    } else {
+        c -= a.hi_units * a.n_hi;
+        unit = a.hi_units + c / a.n_lo;
+        split = c % a.n_lo;
+        chunk = a.chunk_pages;
+    }
+    draft::draft_block<BITS, D, kWarps>(a, split, unit % a.hkv, unit / a.hkv, chunk, smem);
 }
 
 template <int D>
-__global__ void draft_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, float *out) {
+__global__ void draft_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, int grp, int hkv,
+                                    int hi_units, int n_hi, int n_lo, float *out) {
     pdl_begin();
     const int64_t row = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;  // b * Hq + h
-    draft::reduce_row<D>(ws_o, ws_ml, n_splits, row, out, threadIdx.x, blockDim.x);
+    const int unit = blockIdx.y * hkv + blockIdx.x / grp;
+    draft::reduce_row<D>(ws_o, ws_ml, n_splits, unit < hi_units ? n_hi : n_lo, row, out, threadIdx.x,
+                         blockDim.x);
 }
 
+// hi_units units in n_hi chunks of chunk_hi pages, the others in n_lo chunks
+// of chunk_pages; n_splits = the workspace's chunk slots per row.
 struct Plan {
-    int chunk_pages, n_splits;
+    int chunk_pages, n_lo, hi_units, chunk_hi, n_hi, n_splits;
 };
 
 template <int BITS, int D>
@@ -87,17 +106,36 @@ int num_sms() {
 
 template <int BITS, int D>
 Plan plan(int batch, int hkv, int max_seq_len) {
-    // one full wave: at most SMs x resident CTAs work items, equal chunks
+    // One full wave: as many CTAs as SMs x resident CTAs, every one inside
+    // one unit.  When the slots are not a multiple of the units, the first
+    // (slots mod units) units take one chunk more (smaller chunks), so that
+    // every slot holds a CTA and the SMs get nearly equal pages: the block
+    // scheduler fills the SMs breadth first, and the smaller chunks come
+    // first in launch order, so each SM mixes both sizes.
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
     const int64_t slots = (int64_t)num_sms() * occupancy<BITS, D>();
-    int splits = (int)(slots / units);
-    splits = max(1, min(splits, ceil_div(max_pages, kWarps)));
-    int chunk = ceil_div(max_pages, splits);
-    chunk = max(kWarps, ceil_div(chunk, kWarps) * kWarps);
+    const int cap = ceil_div(max_pages, kWarps);  // a warp needs a page
+    const int64_t per_unit = slots / units;
+    const int base = per_unit < 1 ? 1 : (per_unit > cap ? cap : (int)per_unit);
+    auto chunk_for = [&](int splits) { return max(kWarps, ceil_div(ceil_div(max_pages, splits), kWarps) * kWarps); };
     Plan p;
-    p.chunk_pages = chunk;
-    p.n_splits = max(1, ceil_div(max_pages, chunk));
+    p.chunk_pages = chunk_for(base);
+    p.n_lo = max(1, ceil_div(max_pages, p.chunk_pages));
+    p.hi_units = 0;
+    p.chunk_hi = p.chunk_pages;
+    p.n_hi = p.n_lo;
+    const int64_t extra = slots - (int64_t)base * units;
+    if (base + 1 <= cap && extra > 0 && extra < units) {
+        const int ch = chunk_for(base + 1);
+        const int nh = max(1, ceil_div(max_pages, ch));
+        if (nh > p.n_lo) {
+            p.hi_units = (int)extra;
+            p.chunk_hi = ch;
+            p.n_hi = nh;
+        }
+    }
+    p.n_splits = max(p.n_hi, p.n_lo);
     return p;
 }
 
@@ -119,8 +157,9 @@ template <int BITS, int D>
 cudaError_t launch(const DraftArgs &a, int batch, cudaStream_t st) {
     using C = Cfg<BITS, D, kWarps>;
     occupancy<BITS, D>();  // sets the shared-memory attribute once
-    dim3 grid(a.n_splits, a.hkv, batch);
-    launch_pdl(draft_kernel<BITS, D>, grid, kWarps * 32, C::SMEM, st, a);
+    const int64_t units = (int64_t)batch * a.hkv;
+    const int64_t ctas = (int64_t)a.hi_units * a.n_hi + (units - a.hi_units) * a.n_lo;
+    launch_pdl(draft_kernel<BITS, D>, dim3((unsigned)ctas), kWarps * 32, C::SMEM, st, a);
     return cudaGetLastError();
 }
 
@@ -157,6 +196,10 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     a.scale_log2 = scale * 1.4426950408889634f;
     a.chunk_pages = p.chunk_pages;
     a.n_splits = p.n_splits;
+    a.n_lo = p.n_lo;
+    a.hi_units = p.hi_units;
+    a.chunk_hi = p.chunk_hi;
+    a.n_hi = p.n_hi;
     a.ws_o = (float *)ws;
     a.ws_ml = a.ws_o + (size_t)c.batch * hq * p.n_splits * d;
     a.status = status;
@@ -174,9 +217,11 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     if (e != cudaSuccess) return e;
     dim3 rg(hq, c.batch);
     if (d == 64)
-        launch_pdl(draft_reduce_kernel<64>, rg, 64, 0, st, a.ws_o, a.ws_ml, p.n_splits, out);
+        launch_pdl(draft_reduce_kernel<64>, rg, 64, 0, st, a.ws_o, a.ws_ml, p.n_splits, a.grp, a.hkv, p.hi_units,
+                   p.n_hi, p.n_lo, out);
     else
-        launch_pdl(draft_reduce_kernel<128>, rg, 128, 0, st, a.ws_o, a.ws_ml, p.n_splits, out);
+        launch_pdl(draft_reduce_kernel<128>, rg, 128, 0, st, a.ws_o, a.ws_ml, p.n_splits, a.grp, a.hkv,
+                   p.hi_units, p.n_hi, p.n_lo, out);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,10 @@ struct DraftArgs {
     int maxb;
     int hq, hkv, grp;
     float scale_log2;
-    int chunk_pages, n_splits;
+    int chunk_pages, n_splits;  // pages per chunk; chunk slots per row of the workspace
+    // the draft launch's first hi_units units (request x kv head) take n_hi
+    // chunks of chunk_hi pages, the others n_lo chunks of chunk_pages
+    int hi_units = 0, chunk_hi = 0, n_hi = 0, n_lo = 0;
     float *ws_o;   // [B][Hq][n_splits][D]
     float *ws_ml;  // [B][Hq][n_splits][2]
     int32_t *status;
@@ -240,11 +243,12 @@ __device__ inline void load_halves(const __half *p, float (&f)[NG]) {
 }
 
 template <int BITS, int D, int NW>
-__device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int kvh, int b, uint8_t *smem) {
+__device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int kvh, int b, int chunk,
+                                            uint8_t *smem) {
     using C = Cfg<BITS, D, NW>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int p0 = split * a.chunk_pages;
+    const int p0 = split * chunk;
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
     // The loads that depend on nothing else go out together: the group's
     // queries, the table entries of the warp's first 64 pages (read before
@@ -267,7 +271,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     const int raw0 = raw_id(lane), raw1 = raw_id(32 + lane);
     const int len = a.lens[b];
     const int npages = ceil_div(len, kPage);
-    const int p1 = min(p0 + a.chunk_pages, npages);
+    const int p1 = min(p0 + chunk, npages);
     uint8_t *ring = smem + warp * C::NSTAGE * C::STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (C::RING > C::COMBINE ? C::RING : C::COMBINE)) +
                      warp * C::NSTAGE;
@@ -779,17 +783,18 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
     }
 }
 
-// Combine the chunk partials of one (request, head) row.
+// Combine the first `count` chunk partials of one (request, head) row (of
+// n_splits slots), in chunk order.
 template <int D>
-__device__ __forceinline__ void reduce_row(const float *ws_o, const float *ws_ml, int n_splits, int64_t row,
-                                           float *out, int tid, int nthreads) {
+__device__ __forceinline__ void reduce_row(const float *ws_o, const float *ws_ml, int n_splits, int count,
+                                           int64_t row, float *out, int tid, int nthreads) {
     const float *ml = ws_ml + row * n_splits * 2;
     float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ml[2 * s]);
+    for (int s = 0; s < count; ++s) M = fmaxf(M, ml[2 * s]);
     for (int c = tid; c < D; c += nthreads) {
         float acc = 0.0f, L = 0.0f;
         if (M != -INFINITY) {
-            for (int s = 0; s < n_splits; ++s) {
+            for (int s = 0; s < count; ++s) {
                 const float f = ex2(ml[2 * s] - M);
                 acc += f * ws_o[(row * n_splits + s) * D + c];
                 L += f * ml[2 * s + 1];

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__
         const int rest = bid / m.d.n_splits;
         const int kvh = rest % m.d.hkv, b = rest / m.d.hkv;
         if (m.role[b] != 0) return;
-        draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, smem);
+        draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, m.d.chunk_pages, smem);
     }
 }
 
@@ -65,7 +65,8 @@ __global__ void mixed_reduce_kernel(MixedArgs m, float *out_draft, float *out_ve
     const int row = blockIdx.x;
     if (row < draft_rows) {  // row = b * Hq + h
         if (m.role[row / m.d.hq] != 0) return;
-        draft::reduce_row<D>(m.d.ws_o, m.d.ws_ml, m.d.n_splits, row, out_draft, threadIdx.x, blockDim.x);
+        draft::reduce_row<D>(m.d.ws_o, m.d.ws_ml, m.d.n_splits, m.d.n_splits, row, out_draft, threadIdx.x,
+                             blockDim.x);
     } else {  // ((b * n_q + i) * Hq + h)
         const int r = row - draft_rows;
         if (m.role[r / (m.v.n_q * m.v.hq)] != 1) return;
