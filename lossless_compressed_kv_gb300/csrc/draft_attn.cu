@@ -40,41 +40,41 @@ constexpr int kWarps = 4;
 template <int BITS, int D>
 constexpr int kMinCtas = 4;
 
-// One CTA per (unit = request x kv head, context chunk), numbered units
-// 0 .. hi_units - 1 first (n_hi chunks of chunk_hi pages each), then the rest
-// (n_lo chunks of chunk_pages).
+// One CTA per (unit = request x kv head, context chunk): units 0 ..
+// lo_units - 1 first, in n_lo chunks of chunk_pages each, then the others in
+// n_hi (smaller) chunks of chunk_hi.
 template <int BITS, int D>
 __global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(DraftArgs a) {
     pdl_begin();
     extern __shared__ __align__(128) uint8_t smem[];
     int c = blockIdx.x, unit, split, chunk;
-    if (c < a.hi_units * a.n_hi) {
-        unit = c / a.n_hi;
-        split = c % a.n_hi;
-        chunk = a.chunk_hi;
-    } else {
-        c -= a.hi_units * a.n_hi;
-        unit = a.hi_units + c / a.n_lo;
+    if (c < a.lo_units * a.n_lo) {
+        unit = c / a.n_lo;
         split = c % a.n_lo;
         chunk = a.chunk_pages;
+    } else {
+        c -= a.lo_units * a.n_lo;
+        unit = a.lo_units + c / a.n_hi;
+        split = c % a.n_hi;
+        chunk = a.chunk_hi;
     }
     draft::draft_block<BITS, D, kWarps>(a, split, unit % a.hkv, unit / a.hkv, chunk, smem);
 }
 
 template <int D>
 __global__ void draft_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, int grp, int hkv,
-                                    int hi_units, int n_hi, int n_lo, float *out) {
+                                    int lo_units, int n_hi, int n_lo, float *out) {
     pdl_begin();
     const int64_t row = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;  // b * Hq + h
     const int unit = blockIdx.y * hkv + blockIdx.x / grp;
-    draft::reduce_row<D>(ws_o, ws_ml, n_splits, unit < hi_units ? n_hi : n_lo, row, out, threadIdx.x,
+    draft::reduce_row<D>(ws_o, ws_ml, n_splits, unit < lo_units ? n_lo : n_hi, row, out, threadIdx.x,
                          blockDim.x);
 }
 
-// hi_units units in n_hi chunks of chunk_hi pages, the others in n_lo chunks
-// of chunk_pages; n_splits = the workspace's chunk slots per row.
+// lo_units units in n_lo chunks of chunk_pages, the others in n_hi chunks of
+// chunk_hi pages (n_hi >= n_lo); n_splits = the workspace's chunk slots per row.
 struct Plan {
-    int chunk_pages, n_lo, hi_units, chunk_hi, n_hi, n_splits;
+    int chunk_pages, n_lo, lo_units, chunk_hi, n_hi, n_splits;
 };
 
 template <int BITS, int D>
@@ -107,11 +107,12 @@ int num_sms() {
 template <int BITS, int D>
 Plan plan(int batch, int hkv, int max_seq_len) {
     // One full wave: as many CTAs as SMs x resident CTAs, every one inside
-    // one unit.  When the slots are not a multiple of the units, the first
-    // (slots mod units) units take one chunk more (smaller chunks), so that
-    // every slot holds a CTA and the SMs get nearly equal pages: the block
-    // scheduler fills the SMs breadth first, and the smaller chunks come
-    // first in launch order, so each SM mixes both sizes.
+    // one unit.  When the slots are not a multiple of the units, (slots mod
+    // units) units take one chunk more (smaller chunks), so that every slot
+    // holds a CTA.  The block scheduler fills the SMs breadth first, so each
+    // SM gets both sizes; the larger chunks are launched first, because the
+    // warp schedulers favour a CTA's warps by age and the first CTAs on an
+    // SM run faster: that way an SM's CTAs end closer together.
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
     const int64_t slots = (int64_t)num_sms() * occupancy<BITS, D>();
@@ -122,7 +123,7 @@ Plan plan(int batch, int hkv, int max_seq_len) {
     Plan p;
     p.chunk_pages = chunk_for(base);
     p.n_lo = max(1, ceil_div(max_pages, p.chunk_pages));
-    p.hi_units = 0;
+    p.lo_units = (int)units;
     p.chunk_hi = p.chunk_pages;
     p.n_hi = p.n_lo;
     const int64_t extra = slots - (int64_t)base * units;
@@ -130,7 +131,7 @@ Plan plan(int batch, int hkv, int max_seq_len) {
         const int ch = chunk_for(base + 1);
         const int nh = max(1, ceil_div(max_pages, ch));
         if (nh > p.n_lo) {
-            p.hi_units = (int)extra;
+            p.lo_units = (int)(units - extra);
             p.chunk_hi = ch;
             p.n_hi = nh;
         }
@@ -158,7 +159,7 @@ cudaError_t launch(const DraftArgs &a, int batch, cudaStream_t st) {
     using C = Cfg<BITS, D, kWarps>;
     occupancy<BITS, D>();  // sets the shared-memory attribute once
     const int64_t units = (int64_t)batch * a.hkv;
-    const int64_t ctas = (int64_t)a.hi_units * a.n_hi + (units - a.hi_units) * a.n_lo;
+    const int64_t ctas = (int64_t)a.lo_units * a.n_lo + (units - a.lo_units) * a.n_hi;
     launch_pdl(draft_kernel<BITS, D>, dim3((unsigned)ctas), kWarps * 32, C::SMEM, st, a);
     return cudaGetLastError();
 }
@@ -197,7 +198,7 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     a.chunk_pages = p.chunk_pages;
     a.n_splits = p.n_splits;
     a.n_lo = p.n_lo;
-    a.hi_units = p.hi_units;
+    a.lo_units = p.lo_units;
     a.chunk_hi = p.chunk_hi;
     a.n_hi = p.n_hi;
     a.ws_o = (float *)ws;
@@ -217,11 +218,11 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     if (e != cudaSuccess) return e;
     dim3 rg(hq, c.batch);
     if (d == 64)
-        launch_pdl(draft_reduce_kernel<64>, rg, 64, 0, st, a.ws_o, a.ws_ml, p.n_splits, a.grp, a.hkv, p.hi_units,
+        launch_pdl(draft_reduce_kernel<64>, rg, 64, 0, st, a.ws_o, a.ws_ml, p.n_splits, a.grp, a.hkv, p.lo_units,
                    p.n_hi, p.n_lo, out);
     else
         launch_pdl(draft_reduce_kernel<128>, rg, 128, 0, st, a.ws_o, a.ws_ml, p.n_splits, a.grp, a.hkv,
-                   p.hi_units, p.n_hi, p.n_lo, out);
+                   p.lo_units, p.n_hi, p.n_lo, out);
     return cudaGetLastError();
 }
 

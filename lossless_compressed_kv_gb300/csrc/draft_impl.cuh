@@ -20,9 +20,9 @@ struct DraftArgs {
     int hq, hkv, grp;
     float scale_log2;
     int chunk_pages, n_splits;  // pages per chunk; chunk slots per row of the workspace
-    // the draft launch's first hi_units units (request x kv head) take n_hi
-    // chunks of chunk_hi pages, the others n_lo chunks of chunk_pages
-    int hi_units = 0, chunk_hi = 0, n_hi = 0, n_lo = 0;
+    // the draft launch's first lo_units units (request x kv head) take n_lo
+    // chunks of chunk_pages, the others n_hi chunks of chunk_hi pages
+    int lo_units = 0, chunk_hi = 0, n_hi = 0, n_lo = 0;
     float *ws_o;   // [B][Hq][n_splits][D]
     float *ws_ml;  // [B][Hq][n_splits][2]
     int32_t *status;
