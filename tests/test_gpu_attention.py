@@ -198,6 +198,50 @@ def test_draft_full_size_workloads(name):
             assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
 
 
+@pytest.mark.parametrize("name", ["8b_32k_2bit", "70b_128k_drop4"])
+def test_draft_step_full_size_workloads(name):
+    """The call the benchmark's round makes (vc_draft_step: append the step's
+    entry at slot ctx, then attend) at full size, every row against the
+    oracle over the cache with that entry."""
+    from concurrent.futures import ThreadPoolExecutor
+    m = vc()
+    w = synth.WORKLOADS[name]
+    rng = synth.rng_for(name, 5)
+    n = w["ctx"]
+    lens = [n + 1] * w["batch"]
+    full, hf = H.full_cache(rng, lens, w["hkv"], w["d"])
+    if w["bits"] == 16:
+        kept = [synth.kept_sink_recent_topk(rng, n, w["sink"], w["recent"], w["kept_total"]) for _ in lens]
+    else:
+        kept = [np.arange(n, dtype=np.int32)] * w["batch"]
+    cap = len(kept[0]) + 1
+    comp, _ = H.comp_cache(rng, w["batch"], cap, w["hkv"], w["d"], w["bits"])
+    compress_all(full, comp, kept)
+    slot = np.full(w["batch"], len(kept[0]), np.int32)
+    kvn = [H.logical_full(hf, b) for b in range(w["batch"])]
+    kn = np.stack([k[n] for k, _ in kvn])
+    vn = np.stack([v[n] for _, v in kvn])
+    lens_c = H.to_dev(slot + 1)
+    c = m.PagedKV(comp.k_pages, comp.v_pages, comp.block_table, lens_c, w["hkv"], w["d"], w["bits"])
+    qn, qd = q_bf16(rng, (w["batch"], w["hq"], w["d"]))
+    scale = 1.0 / math.sqrt(w["d"])
+    out = torch.empty((w["batch"], w["hq"], w["d"]), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.draft_workspace_bytes(c, w["hq"], cap), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.draft_step(qd, c, H.to_dev(kn.view(np.int16)), H.to_dev(vn.view(np.int16)), H.to_dev(slot), scale, out, cap,
+                 ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got = out.cpu().numpy()
+    del full, comp
+    with ThreadPoolExecutor(oracle.threads()) as pool:
+        for b in range(w["batch"]):
+            k, v = kvn[b]
+            kb = np.concatenate([kept[b], np.array([n], np.int32)])
+            ref = oracle.draft_attn(qn[b], oracle.compress(k, v, kb, w["bits"]), float(np.float32(scale)), pool=pool)
+            assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
+
+
 # --------------------------------------------------------------- verify
 
 VERIFY_CASES = [
