@@ -379,7 +379,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging", "70b_128k_drop4",
-                             "stagger_32req_3bit", "remote_prefix_8req_3bit"])
+                             "stagger_32req_3bit", "remote_prefix_8req_3bit", "verify_40k"])
     ap.add_argument("--cycles", type=int, default=2, help="measured cycles of the staggering workload")
     args = ap.parse_args()
     rank, ws = dist_init()
@@ -391,7 +391,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         {"mixed_32req_3bit": mixed_main, "toy_e2e": toy_main, "staging": staging_main,
          "70b_128k_drop4": big_main, "stagger_32req_3bit": stagger_main,
-         "remote_prefix_8req_3bit": remote_main}[args.workload](args)
+         "remote_prefix_8req_3bit": remote_main, "verify_40k": verify40k_main}[args.workload](args)
         return
     import torch
     import synth
@@ -565,6 +565,74 @@ def e2e_measure(w, st, rnd, args, ws, device):
 # host -> device staging bandwidth
 # ---------------------------------------------------------------------------
 
+def _bf16_pools(vc, torch, g, device, b, n_tok, nkv, d):
+    """Random bf16 KV_full of b requests x n_tok tokens, pages in a seeded
+    permuted order."""
+    npg = (n_tok + 15) // 16
+    perm = torch.randperm(b * npg, generator=g, device=device).to(torch.int32)
+    kp = torch.empty((b * npg, nkv, 16, d), dtype=torch.bfloat16, device=device)
+    vp = torch.empty_like(kp)
+    for s0 in range(0, b * npg, 1024):
+        e = min(b * npg, s0 + 1024)
+        kp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
+        vp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
+    return vc.PagedKV(kp.view(torch.uint8).view(b * npg, -1), vp.view(torch.uint8).view(b * npg, -1),
+                      perm.view(b, npg).contiguous(), torch.full((b,), n_tok, dtype=torch.int32, device=device),
+                      nkv, d, 16)
+
+
+def _graph_us(torch, fn, reps):
+    """Mean device time of fn over replays of a CUDA graph of it (us)."""
+    gr = capture(fn)
+    a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gr.replay()
+    a.record()
+    for _ in range(reps):
+        gr.replay()
+    b2.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b2) / reps * 1e3
+
+
+def _verify_40k(vc, torch, g, device, d, hkv, peak, tpeak, reps):
+    """The 40k-context verify point: batch 8, 32q/8kv, context 40960, a block
+    of 40 queries (160 rows per kv head: one two-tile row block)."""
+    B2, hq2, N2, x2 = 8, 32, 40960, 40
+    L2 = N2 + x2
+    scale = 1.0 / math.sqrt(d)
+    full2 = _bf16_pools(vc, torch, g, device, B2, L2, hkv, d)
+    qv2 = torch.randn((B2, x2, hq2, d), generator=g, device=device).to(torch.bfloat16)
+    vout2 = torch.empty((B2, x2, hq2, d), dtype=torch.float32, device=device)
+    vws2 = torch.empty(vc.verify_workspace_bytes(full2, x2, hq2, L2), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    t_ver2 = _graph_us(torch, lambda: vc.verify_attn(qv2, full2, scale, vout2, L2, vws2, status=status), reps)
+    torch.cuda.synchronize()
+    assert status.item() == 0, "device status %d" % status.item()
+    v2_bytes = B2 * L2 * hkv * 2 * d * 2
+    v2_flops = 2 * 2 * B2 * x2 * hq2 * L2 * d
+    return {"config": {"batch": B2, "q_heads": hq2, "kv_heads": hkv, "ctx": N2, "n_q": x2},
+            "us_per_call": t_ver2, "GBps": v2_bytes / t_ver2 / 1e3,
+            "frac_hbm_measured": v2_bytes / t_ver2 / 1e3 / peak, "TFLOPs": v2_flops / t_ver2 / 1e6,
+            "frac_bf16_measured": v2_flops / t_ver2 / 1e6 / tpeak}
+
+
+def verify40k_main(args):
+    """Only the 40k-context verify point (for profiling it alone)."""
+    import torch
+    import lossless_compressed_kv_gb300 as vc
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    g = torch.Generator(device=device)
+    g.manual_seed(78)
+    peak, _ = peaks()
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        tpeak = float(json.load(f)["bf16_tflops"])
+    r = _verify_40k(vc, torch, g, device, 128, 8, peak, tpeak, max(1, args.steps))
+    print(json.dumps({"metric": "40k-context verify: 8 requests x 40 queries, 32q/8kv, D 128, bf16 KV_full",
+                      "workload": "verify_40k", "verify_40k": r,
+                      "timing": "CUDA events around replays of a CUDA graph of the call; flops count the causal "
+                                "block as full"}), flush=True)
+
+
 def big_main(args):
     """70B-shaped layer (batch 4, 64q/8kv, D 128, 131072-token context,
     32768 kept in bf16: 64 sink + 512 recent + top by a seeded score): the
@@ -584,28 +652,10 @@ def big_main(args):
         tpeak = float(json.load(f)["bf16_tflops"])
 
     def pools(b, n_tok, nkv):
-        npg = (n_tok + 15) // 16
-        perm = torch.randperm(b * npg, generator=g, device=device).to(torch.int32)
-        kp = torch.empty((b * npg, nkv, 16, d), dtype=torch.bfloat16, device=device)
-        vp = torch.empty_like(kp)
-        for s0 in range(0, b * npg, 1024):
-            e = min(b * npg, s0 + 1024)
-            kp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
-            vp[s0:e] = torch.randn((e - s0, nkv, 16, d), generator=g, device=device).to(torch.bfloat16)
-        return vc.PagedKV(kp.view(torch.uint8).view(b * npg, -1), vp.view(torch.uint8).view(b * npg, -1),
-                          perm.view(b, npg).contiguous(), torch.full((b,), n_tok, dtype=torch.int32, device=device),
-                          nkv, d, 16)
+        return _bf16_pools(vc, torch, g, device, b, n_tok, nkv, d)
 
     def timed(fn, reps):
-        gr = capture(fn)
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        gr.replay()
-        a.record()
-        for _ in range(reps):
-            gr.replay()
-        b2.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b2) / reps * 1e3  # us
+        return _graph_us(torch, fn, reps)
 
     scale = 1.0 / math.sqrt(d)
     L = N + x
@@ -650,17 +700,9 @@ def big_main(args):
     del full, comp, dws, vws
     torch.cuda.empty_cache()
     # the 40k-context verify point
-    B2, hq2, N2, x2 = 8, 32, 40960, 40
-    L2 = N2 + x2
-    full2 = pools(B2, L2, hkv)
-    qv2 = torch.randn((B2, x2, hq2, d), generator=g, device=device).to(torch.bfloat16)
-    vout2 = torch.empty((B2, x2, hq2, d), dtype=torch.float32, device=device)
-    vws2 = torch.empty(vc.verify_workspace_bytes(full2, x2, hq2, L2), dtype=torch.uint8, device=device)
-    t_ver2 = timed(lambda: vc.verify_attn(qv2, full2, scale, vout2, L2, vws2, status=status), 10)
+    v40 = _verify_40k(vc, torch, g, device, d, hkv, peak, tpeak, 10)
     torch.cuda.synchronize()
     assert status.item() == 0, "device status %d" % status.item()
-    v2_bytes = B2 * L2 * hkv * 2 * d * 2
-    v2_flops = 2 * 2 * B2 * x2 * hq2 * L2 * d
     print(json.dumps({
         "metric": "70B-shaped layer: draft over bf16 token-drop KV_comp and 40-query verify; 40k-context verify",
         "workload": "70b_128k_drop4",
@@ -675,10 +717,7 @@ def big_main(args):
         "verify": {"us_per_call": t_ver, "bytes": ver_bytes, "GBps": ver_bytes / t_ver / 1e3,
                    "frac_hbm_measured": ver_bytes / t_ver / 1e3 / peak, "TFLOPs": ver_flops / t_ver / 1e6,
                    "frac_bf16_measured": ver_flops / t_ver / 1e6 / tpeak},
-        "verify_40k": {"config": {"batch": B2, "q_heads": hq2, "kv_heads": hkv, "ctx": N2, "n_q": x2},
-                       "us_per_call": t_ver2, "GBps": v2_bytes / t_ver2 / 1e3,
-                       "frac_hbm_measured": v2_bytes / t_ver2 / 1e3 / peak, "TFLOPs": v2_flops / t_ver2 / 1e6,
-                       "frac_bf16_measured": v2_flops / t_ver2 / 1e6 / tpeak},
+        "verify_40k": v40,
         "timing": "CUDA events around replays of a CUDA graph of the call; flops count the causal block as full",
     }), flush=True)
 
