@@ -5,7 +5,7 @@
 // items 3-5: one pass over KV_full checks all drafted positions in
 // parallel; query i of the block attends causally to every earlier position
 // and to itself ("KV Cache and Speculative Decoding": causal attention).
-// Launch: one CTA per (split of 4096 keys, row block, request x kv head);
+// Launch: one CTA per (split of 3648 keys, row block, request x kv head);
 // a row block holds one 128-row MMA tile of (query, head) rows when there
 // are at most 128 rows, else two (more rows take further row blocks).  When
 // the last row block would hold a single tile behind full two-tile blocks
