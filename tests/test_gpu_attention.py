@@ -250,7 +250,7 @@ VERIFY_CASES = [
     (128, 1, 8, 40, [40, 41, 1300]),
     (128, 2, 4, 25, [25, 8193]),
     (64, 1, 4, 9, [512, 9, 16]),
-    (64, 2, 2, 1, [1, 17, 4096, 4097]),
+    (64, 2, 2, 1, [1, 17, 3648, 3649, 4097]),   # a split ends after 3648 keys
     (128, 3, 1, 33, [700]),
     (64, 1, 8, 64, [64, 200]),
     (128, 2, 4, 40, [40, 4200, 8200]),   # 160 rows: two 128-row tiles
