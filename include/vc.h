@@ -254,7 +254,7 @@ VC_API size_t vc_static_scratch_bytes(void);
  * 1 <= n_q <= 64, num_q_heads / num_kv_heads <= 8, head_dim in {64, 128},
  * full->fmt.bits == 16, L >= n_q (a request with L < n_q gets
  * VC_ERR_BAD_INDEX in dev_status and zero output).  The split over context
- * chunks is fixed by position (1024 keys), so a query's result does not
+ * chunks is fixed by position (3648 keys), so a query's result does not
  * depend on n_q, its place in the block, or the batch.
  */
 VC_API size_t vc_verify_workspace_bytes(const vc_paged_kv *full, int32_t n_q, int32_t num_q_heads,
