@@ -369,6 +369,23 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 for (int i = 0; i < kGroup; ++i) sum += bf16_bits_to_f32(qs[n * D + gr * kGroup + i]);
                 qsum[e] = sum * a.scale_log2;
             }
+            // Q fragments: B of S^T = K Q^T, column n = head g, k-slot pair of
+            // register r pre-scaled by 2^-kpos(r) so every product is c q
+            // 2^-24.  The same for every warp: packed once into shared memory
+            // as [group][lane][k-step 2gr lo, hi, k-step 2gr+1 lo, hi], the
+            // k-steps spread over the warps.
+            uint32_t *qf = reinterpret_cast<uint32_t *>(qsum + 8 * C::NG);
+#pragma unroll
+            for (int ks = 0; ks < C::NT; ++ks) {
+                if (ks % NW != warp) continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c0 = 16 * ks + 4 * t + 2 * h;
+                    const float f = __uint_as_float((uint32_t)(127 - kpos<BITS>(2 * ks + h)) << 23);
+                    qf[((ks >> 1) * 32 + lane) * 4 + 2 * (ks & 1) + h] =
+                        pack_f16(bf16_bits_to_f32(qs[g * D + c0]) * f, bf16_bits_to_f32(qs[g * D + c0 + 1]) * f);
+                }
+            }
             __syncthreads();
         }
     }
@@ -474,24 +491,8 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         }
     } else {
         // ---- quantised cache ----
-        // Q fragments: B of S^T = K Q^T, column n = head g, k-slot pair of
-        // register r pre-scaled by 2^-kpos(r) so every product is c q 2^-24.
-        // The same for every warp: warp 0 packs them once into shared memory
-        // as [group][lane][k-step 2gr lo, hi, k-step 2gr+1 lo, hi].
-        uint32_t *qfrag = reinterpret_cast<uint32_t *>(qsum + 8 * C::NG);
-        if (warp == 0) {
-#pragma unroll
-            for (int ks = 0; ks < C::NT; ++ks) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c0 = 16 * ks + 4 * t + 2 * h;
-                    const float f = __uint_as_float((uint32_t)(127 - kpos<BITS>(2 * ks + h)) << 23);
-                    qfrag[((ks >> 1) * 32 + lane) * 4 + 2 * (ks & 1) + h] =
-                        pack_f16(bf16_bits_to_f32(qs[g * D + c0]) * f, bf16_bits_to_f32(qs[g * D + c0 + 1]) * f);
-                }
-            }
-        }
-        __syncthreads();
+        // (query fragments packed in the prologue above)
+        const uint32_t *qfrag = reinterpret_cast<const uint32_t *>(qsum + 8 * C::NG);
         // Zero-point term of the scores as one more MMA: k-slots (2t, 2t+1)
         // carry groups (2P, 2P+1), P = t & 1, as the hi (t < 2) or lo (t >= 2)
         // f16 part of the pre-scaled query group sums.
