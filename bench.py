@@ -57,12 +57,16 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples during the timed region: the sampler is started and
+    its first line awaited before the region begins (nvidia-smi takes longer
+    to start than a short timed region lasts), that line is dropped, and the
+    GPU is polled every 10 ms."""
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.lines = []
+        self.skip = 0
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -70,10 +74,14 @@ class Clocks:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.005)
+            self.skip = len(self.lines)
         except Exception:
             self.proc = None
         return self
@@ -93,7 +101,7 @@ class Clocks:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.skip:]:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
