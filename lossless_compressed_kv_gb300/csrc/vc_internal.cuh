@@ -181,6 +181,51 @@ __device__ inline float ex2(float x) {
     return y;
 }
 
+// Combine the first `count` split partials (m, l, o) of one output row
+// (`stride` slots per row; m in log2 units), in split order:
+//   out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s
+// (0 when no split saw a key).  The loads go out eight splits at a time --
+// the partials come from L2, and one round trip per split would add up --
+// while the arithmetic keeps split order.
+template <int D>
+__device__ __forceinline__ void combine_partials(const float *ws_o, const float *ws_ml, int stride, int count,
+                                                 int64_t row, float *out, int tid, int nthreads) {
+    constexpr int U = 8;
+    const float *ml = ws_ml + row * stride * 2;
+    float M = -INFINITY;
+    for (int s0 = 0; s0 < count; s0 += U) {
+        float m[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) m[j] = s0 + j < count ? ml[2 * (s0 + j)] : -INFINITY;
+#pragma unroll
+        for (int j = 0; j < U; ++j) M = fmaxf(M, m[j]);
+    }
+    for (int c = tid; c < D; c += nthreads) {
+        float acc = 0.0f, L = 0.0f;
+        if (M != -INFINITY) {
+            for (int s0 = 0; s0 < count; s0 += U) {
+                float mm[U], ll[U], oo[U];
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    const bool in = s0 + j < count;
+                    mm[j] = in ? ml[2 * (s0 + j)] : 0.0f;
+                    ll[j] = in ? ml[2 * (s0 + j) + 1] : 0.0f;
+                    oo[j] = in ? ws_o[(row * stride + s0 + j) * D + c] : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    if (s0 + j < count) {
+                        const float f = ex2(mm[j] - M);
+                        acc += f * oo[j];
+                        L += f * ll[j];
+                    }
+                }
+            }
+        }
+        out[row * D + c] = L > 0.0f ? acc / L : 0.0f;
+    }
+}
+
 __device__ inline float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

@@ -641,20 +641,7 @@ __device__ __forceinline__ void verify_tc_cta(const Args &a, int split, int rb, 
 template <int D>
 __device__ __forceinline__ void reduce_row(const float *ws_o, const float *ws_ml, int n_splits, int64_t row,
                                            float *out, int tid, int nthreads) {
-    const float *ml = ws_ml + row * n_splits * 2;
-    float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ml[2 * s]);
-    for (int c = tid; c < D; c += nthreads) {
-        float acc = 0.0f, L = 0.0f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < n_splits; ++s) {
-                const float f = ex2(ml[2 * s] - M);
-                acc += f * ws_o[(row * n_splits + s) * D + c];
-                L += f * ml[2 * s + 1];
-            }
-        }
-        out[row * D + c] = L > 0.0f ? acc / L : 0.0f;
-    }
+    combine_partials<D>(ws_o, ws_ml, n_splits, n_splits, row, out, tid, nthreads);
 }
 
 }  // namespace vtc
