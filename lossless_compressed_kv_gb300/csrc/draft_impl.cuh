@@ -497,7 +497,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         // carry groups (2P, 2P+1), P = t & 1, as the hi (t < 2) or lo (t >= 2)
         // f16 part of the pre-scaled query group sums.
         const int zp = t & 1;
-        const bool zuse = 2 * zp + 1 < C::NG;
+        const bool zuse = C::NG >= 4 || 2 * zp + 1 < C::NG;  // always with four or more groups
         uint32_t bz = 0u;
         if (zuse) {
             const float s0 = qsum[g * C::NG + 2 * zp], s1 = qsum[g * C::NG + 2 * zp + 1];
@@ -651,14 +651,13 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 // A of the V zero-point MMA: rows 0..G-1 the group's zero
                 // points of tokens (2t, 2t+1) / (2t+8, 2t+9); row G ones, so
                 // the MMA also sums P over the page (the softmax denominator)
-                uint32_t vza0 = 0u, vza2 = 0u;
-                if (g < C::NG) {
-                    const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + g) * 8);
-                    vza0 = u.x;
-                    vza2 = u.y;
-                } else if (g == C::NG) {
-                    vza0 = vza2 = 0x3C003C00u;
-                }
+                // (every lane loads -- the rows past the groups read group 0's
+                // words and drop them -- so the warp does not diverge)
+                const int gz = g < C::NG ? g : 0;
+                const uint2 u = *reinterpret_cast<const uint2 *>(vpar + kPage * C::NG * 2 + (t * C::NG + gz) * 8);
+                const uint32_t vone = g == C::NG ? 0x3C003C00u : 0u;
+                uint32_t vza0 = g < C::NG ? u.x : vone;
+                uint32_t vza2 = g < C::NG ? u.y : vone;
                 if (nvalid[i] < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
                     const int nv = nvalid[i];
                     const uint32_t mlo = (2 * t < nv ? 0x0000FFFFu : 0u) | (2 * t + 1 < nv ? 0xFFFF0000u : 0u);
