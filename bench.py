@@ -293,6 +293,19 @@ def draft_bytes(w, n_entries):
     return w["batch"] * n_entries * hkv * per_tok_head
 
 
+def headline_config(w):
+    """The `config` object of the headline line, the same for both arms."""
+    N, x = w["ctx"], w["x"]
+    span = (x // 4, (3 * x) // 4)
+    comp_mb = float(np.mean([draft_bytes(w, N + i + 1) for i in range(*span)])) / 1e6
+    full_mb = w["batch"] * ((N + x + 15) // 16) * 16 * w["hkv"] * w["d"] * 2 * 2 / 1e6
+    return {"workload": WORKLOAD, "batch": w["batch"], "ctx": N, "q_heads": w["hq"], "kv_heads": w["hkv"],
+            "head_dim": w["d"], "bits": w["bits"], "group": 32, "page": 16, "x": x, "verify_n_q": x,
+            "lm_head": [w["d"], w["vocab"]], "parallelism": "replicas",
+            "l2": "inputs larger than L2: KV_comp %.0f MB per draft call, KV_full %.0f MB per verify"
+                  % (comp_mb, full_mb)}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
@@ -364,8 +377,7 @@ def reference_main(args, rank, ws):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "batch": w["batch"], "ctx": N, "q_heads": hq,
-                                            "kv_heads": hkv, "head_dim": d, "bits": w["bits"]},
+            "data": "synthetic", "config": headline_config(w),
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
                              "sample": "1 request x 1 draft step per step (32 query heads over 32768 2-bit "
                                        "KV_comp entries)"},
@@ -477,11 +489,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f16 mma / fp32 accumulate on 2-bit codes", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "batch": B, "ctx": N, "q_heads": w["hq"], "kv_heads": w["hkv"],
-                           "head_dim": w["d"], "bits": w["bits"], "group": 32, "page": 16, "x": x,
-                           "verify_n_q": x, "lm_head": [w["d"], w["vocab"]], "parallelism": "replicas",
-                           "l2": "inputs larger than L2: KV_comp %.0f MB per draft call, KV_full %.0f MB per "
-                                 "verify" % (bytes_avg / 1e6, st["full"].k_pages.numel() * 2 / 1e6)},
+                "config": headline_config(w),
                 "draft_attn": {"tokens_per_s": ws * B / t_draft, "us_per_call": t_draft * 1e6,
                                "bytes_per_call": bytes_avg, "timing": draft_src},
                 "stages": stages,
@@ -865,62 +873,6 @@ def mixed_main(args):
     print(json.dumps(line), flush=True)
 
 
-def stagger_rig(w, device):
-    """The staggering workload: per layer, KV_full of every request (bf16,
-    N(0,1), room for blocks of up to max_x tokens, a request's pages
-    contiguous) in page-locked host memory and KV_comp of its context (every
-    token, w["bits"]) resident on the device; per-layer queries.  Returns
-    (engine, q_draft per layer [B][Hq][D], q_verify per layer [B][max_x][Hq][D])."""
-    import torch
-    import synth
-    import lossless_compressed_kv_gb300 as vc
-    from lossless_compressed_kv_gb300.stagger import StaggerEngine
-    B, hq, hkv, d, bits, L, mx = w["batch"], w["hq"], w["hkv"], w["d"], w["bits"], w["layers"], w["max_x"]
-    rng = np.random.default_rng(w["seed"])
-    ctx = rng.integers(w["ctx_lo"], w["ctx_hi"] + 1, size=B).astype(np.int64)
-    npg = (ctx + mx + 15) // 16
-    first = np.concatenate([[0], np.cumsum(npg)[:-1]]).astype(np.int64)
-    P = int(npg.sum())
-    pb = vc.page_bytes(hkv, d, 16)
-    tab = np.full((B, int(npg.max())), -1, np.int32)
-    for b in range(B):
-        tab[b, :npg[b]] = np.arange(first[b], first[b] + npg[b], dtype=np.int32)
-    cpg = (ctx + 15) // 16
-    ctab = np.full((B, int(cpg.max())), -1, np.int32)
-    c0 = np.concatenate([[0], np.cumsum(cpg)[:-1]])
-    for b in range(B):
-        ctab[b, :cpg[b]] = np.arange(c0[b], c0[b] + cpg[b], dtype=np.int32)
-    tabd, ctabd = torch.from_numpy(tab).to(device), torch.from_numpy(ctab).to(device)
-    lens_full = torch.from_numpy((ctx + mx).astype(np.int32)).to(device)
-    lens_comp = torch.from_numpy(ctx.astype(np.int32)).to(device)
-    offs, idx = synth.csr([np.arange(n, dtype=np.int32) for n in ctx])
-    offs, idx = torch.from_numpy(offs).to(device), torch.from_numpy(idx).to(device)
-    g = torch.Generator(device=device)
-    g.manual_seed(w["seed"])
-    comps, hk, hv = [], [], []
-    for _ in range(L):
-        kp = torch.empty((P, pb // 2), dtype=torch.bfloat16, device=device)
-        vp = torch.empty_like(kp)
-        for s0 in range(0, P, 4096):
-            e = min(P, s0 + 4096)
-            kp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
-            vp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
-        full = vc.PagedKV(kp.view(torch.uint8), vp.view(torch.uint8), tabd, lens_full, hkv, d, 16)
-        comp = vc.PagedKV.allocate(int(cpg.sum()), hkv, d, bits, ctabd, lens_comp, device=device)
-        vc.compress(full, offs, idx, comp, int(ctx.max()))
-        comps.append(comp)
-        for src, dst in ((kp, hk), (vp, hv)):
-            h = torch.empty((P, pb), dtype=torch.uint8, pin_memory=True)
-            h.copy_(src.view(torch.uint8))
-            dst.append(h)
-        del kp, vp, full
-    torch.cuda.synchronize()
-    qd = [torch.randn((B, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
-    qv = [torch.randn((B, mx, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
-    eng = StaggerEngine(comps, hk, hv, first, ctx, hkv, d, hq, mx, device=device)
-    return eng, qd, qv
-
-
 def stagger_main(args):
     """Staggering scheduler on the 32-request, 2-layer workload: lock step
     (every request drafts x tokens, then all verify; one staging buffer for
@@ -937,6 +889,7 @@ def stagger_main(args):
     w = dict(synth.WORKLOADS["stagger_32req_3bit"])
     dev = torch.device("cuda")
     t0 = time.perf_counter()
+    from synth.rigs import stagger_rig
     eng, qd, qv = stagger_rig(w, dev)
     t_build = time.perf_counter() - t0
     B, L, x, mx = w["batch"], w["layers"], w["x"], w["max_x"]
@@ -1012,59 +965,6 @@ def stagger_main(args):
     print(json.dumps(line), flush=True)
 
 
-def remote_rig(w, device):
-    """Remote prefix caching workload: per layer bf16 KV_full (prefix + x
-    tokens, N(0,1)) and its KV_comp (every prefix token, w["bits"]) on the
-    device, and their bytes in page-locked host memory (the store).  Returns
-    (engine, q_draft, q_verify [B][x], q_one [B][1], KV_full views with
-    seq_lens = prefix + 1 for the one-token baseline), all per layer."""
-    import torch
-    import synth
-    import lossless_compressed_kv_gb300 as vc
-    from lossless_compressed_kv_gb300.remote import RemotePrefixEngine
-    B, hq, hkv, d, bits, L, n, x = (w["batch"], w["hq"], w["hkv"], w["d"], w["bits"], w["layers"], w["ctx"],
-                                    w["x"])
-    npg, cpg = (n + x + 15) // 16, (n + 15) // 16
-    pb = vc.page_bytes(hkv, d, 16)
-    tabd = torch.arange(B * npg, dtype=torch.int32, device=device).view(B, npg).contiguous()
-    ctabd = torch.arange(B * cpg, dtype=torch.int32, device=device).view(B, cpg).contiguous()
-    full_lens = torch.full((B,), n + x, dtype=torch.int32, device=device)
-    one_lens = torch.full((B,), n + 1, dtype=torch.int32, device=device)
-    comp_lens = torch.full((B,), n, dtype=torch.int32, device=device)
-    offs, idx = synth.csr([np.arange(n, dtype=np.int32)] * B)
-    offs, idx = torch.from_numpy(offs).to(device), torch.from_numpy(idx).to(device)
-    g = torch.Generator(device=device)
-    g.manual_seed(w["seed"])
-    fulls, comps, ones, fh, ch = [], [], [], [], []
-
-    def pinned(t):
-        h = torch.empty(t.numel(), dtype=torch.uint8, pin_memory=True)
-        h.copy_(t.view(-1))
-        return h
-
-    for _ in range(L):
-        kp = torch.empty((B * npg, pb // 2), dtype=torch.bfloat16, device=device)
-        vp = torch.empty_like(kp)
-        for s0 in range(0, B * npg, 4096):
-            e = min(B * npg, s0 + 4096)
-            kp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
-            vp[s0:e] = torch.randn((e - s0, pb // 2), generator=g, device=device).to(torch.bfloat16)
-        full = vc.PagedKV(kp.view(torch.uint8), vp.view(torch.uint8), tabd, full_lens, hkv, d, 16)
-        comp = vc.PagedKV.allocate(B * cpg, hkv, d, bits, ctabd, comp_lens, device=device)
-        vc.compress(full, offs, idx, comp, n)
-        torch.cuda.synchronize()
-        fulls.append(full)
-        comps.append(comp)
-        ones.append(vc.PagedKV(full.k_pages, full.v_pages, tabd, one_lens, hkv, d, 16))
-        fh.append((pinned(full.k_pages), pinned(full.v_pages)))
-        ch.append((pinned(comp.k_pages), pinned(comp.v_pages)))
-    qd = [torch.randn((B, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
-    qv = [torch.randn((B, x, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
-    q1 = [torch.randn((B, 1, hq, d), generator=g, device=device).to(torch.bfloat16) for _ in range(L)]
-    eng = RemotePrefixEngine(comps, fulls, ch, fh, hq, n + x)
-    return eng, qd, qv, q1, ones
-
-
 def remote_main(args):
     """Remote prefix caching: time to the first drafted token and to the
     first verified block when only KV_comp crosses the slow link (KV_full on
@@ -1074,6 +974,7 @@ def remote_main(args):
     import synth
     w = dict(synth.WORKLOADS["remote_prefix_8req_3bit"])
     dev = torch.device("cuda")
+    from synth.rigs import remote_rig
     eng, qd, qv, q1, ones = remote_rig(w, dev)
     rate, chunk = w["slow_GBps"], int(w["chunk_MB"]) << 20
     # warm-up (module loading, first launches) on an unthrottled link

@@ -231,7 +231,11 @@ VC_API vc_status vc_draft_step(const void *q, int32_t num_q_heads, const vc_page
  * inside the library, held on every GPU that loads the library until the
  * process exits.  The first call on a device looks up that array's device
  * address (a one-time set-up per device); make that first call before any
- * stream capture.  All calls share the array and it keeps the last call's
+ * stream capture.  The address is cached per device together with the
+ * device's current context: after cudaDeviceReset the next call looks it up
+ * again (make that call before any capture too).  A call with batch 0 checks
+ * the format and returns VC_OK before looking at any pointer, as
+ * vc_draft_attn does.  All calls share the array and it keeps the last call's
  * contents: calls that overlap on the GPU (several streams or threads) race,
  * so the caller must serialise them.  Nothing in it needs clearing: a call
  * writes every partial before it reads it.  A call that would need more
@@ -475,6 +479,21 @@ VC_API vc_status vc_swiglu(const float *gu, int32_t m, int32_t f, float *out, vc
 VC_API vc_status vc_rope_kv_write(const float *qkv, int32_t m, const int32_t *row_req, const int32_t *row_pos,
                                   int32_t num_q_heads, float rope_theta, void *q_out, const vc_paged_kv *full,
                                   int32_t *dev_status, vc_stream_t stream);
+
+/*
+ * vc_debug_set_wait_fault -- fault injection for tests of the bounded device
+ * waits (host-side switch, process-wide, off by default; not for production
+ * use).  Every wait of a kernel on a copy or on another warp gives up after
+ * a time limit, reports VC_ERR_TIMEOUT in dev_status and lets the block
+ * drain and exit (no GPU hang on a lost copy).  This sets that limit for the
+ * draft, draft-step, verification and mixed launches made after the call:
+ * wait_limit_ns in (0, 2e9], or 0 for the default of 2 s.  skip_copies != 0
+ * makes those kernels issue none of their KV page copies (and signal none),
+ * so every wait on a copy runs into the limit: outputs are then zeros and
+ * nothing of the cache is read.  Calls racing with launches on other threads
+ * see either setting.  VC_ERR_INVALID_ARG for a limit out of range.
+ */
+VC_API vc_status vc_debug_set_wait_fault(int64_t wait_limit_ns, int32_t skip_copies);
 
 VC_API const char *vc_status_string(vc_status s);
 VC_API const char *vc_version(void);

@@ -98,6 +98,7 @@ _SIG = {
     "vc_stagger_simulate": (C.c_int, [C.POINTER(StaggerModel), C.c_int32, _P, C.c_int32, C.POINTER(StaggerResult)]),
     "vc_stagger_horizon": (C.c_int, [C.POINTER(StaggerModel), C.c_int32, C.c_int32, C.c_int32,
                                      C.POINTER(C.c_int32), _P, C.POINTER(StaggerResult)]),
+    "vc_debug_set_wait_fault": (C.c_int, [C.c_int64, C.c_int32]),
     "vc_status_string": (C.c_char_p, [C.c_int]),
     "vc_version": (C.c_char_p, []),
 }
@@ -139,6 +140,11 @@ def version() -> str:
 def library():
     """The loaded ctypes handle (for ABI tests)."""
     return _lib
+
+
+def debug_set_wait_fault(wait_limit_ns: int = 0, skip_copies: bool = False):
+    """vc_debug_set_wait_fault (tests of the bounded device waits only)."""
+    _check(_lib.vc_debug_set_wait_fault(int(wait_limit_ns), int(bool(skip_copies))), "vc_debug_set_wait_fault")
 
 
 def head_block_bytes(head_dim: int, bits: int) -> int:

@@ -37,6 +37,11 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
                          float scale, int max_seq_len, void *ws, int32_t *status, cudaStream_t st);
 
 namespace {
+WaitFault g_wait_fault;
+}  // namespace
+WaitFault wait_fault() { return g_wait_fault; }
+
+namespace {
 // The format and batch of a paged cache (all an empty batch needs).
 bool paged_fmt_ok(const vc_paged_kv *p) {
     return p && p->batch >= 0 && p->fmt.num_kv_heads >= 1 && p->fmt.head_dim >= 32 && p->fmt.head_dim % 32 == 0 &&
@@ -227,6 +232,13 @@ vc_status vc_mixed_attn(const int32_t *role, const void *q_draft, const vc_paged
         return VC_ERR_WORKSPACE;
     return from_cuda(mixed_launch(role, q_draft, *comp, out_draft, q_verify, n_q, *full, out_verify, num_q_heads,
                                   softmax_scale, msl, workspace, dev_status, (cudaStream_t)stream));
+}
+
+vc_status vc_debug_set_wait_fault(int64_t wait_limit_ns, int32_t skip_copies) {
+    if (wait_limit_ns < 0 || wait_limit_ns > (int64_t)kWaitNs) return VC_ERR_INVALID_ARG;
+    g_wait_fault.wait_ns = wait_limit_ns == 0 ? kWaitNs : (uint64_t)wait_limit_ns;
+    g_wait_fault.skip_copies = skip_copies != 0;
+    return VC_OK;
 }
 
 const char *vc_status_string(vc_status s) {

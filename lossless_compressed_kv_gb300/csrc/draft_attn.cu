@@ -204,6 +204,8 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     a.ws_o = (float *)ws;
     a.ws_ml = a.ws_o + (size_t)c.batch * hq * p.n_splits * d;
     a.status = status;
+    a.wait_ns = wait_fault().wait_ns;
+    a.skip_copies = wait_fault().skip_copies;
     a.k_new = (const uint16_t *)k_new;
     a.v_new = (const uint16_t *)v_new;
     a.slot = slot;

@@ -26,6 +26,8 @@ struct DraftArgs {
     float *ws_o;   // [B][Hq][n_splits][D]
     float *ws_ml;  // [B][Hq][n_splits][2]
     int32_t *status;
+    uint64_t wait_ns = kWaitNs;  // bounded-wait limit
+    int skip_copies = 0;         // fault injection: issue no copy (every wait then times out)
     // vc_draft_step: the step's new entry of every request (bf16 K and V
     // rows, [B][Hkv][D]) is written to KV_comp position slot[b] before the
     // attention; null for a plain draft call
@@ -328,7 +330,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             cur_blk = k >> 5;
         }
         const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
-        if (lane == 0) {
+        if (lane == 0 && !a.skip_copies) {
             const int st = k % C::NSTAGE;
             sflag[st] = id >= 0;
             if (id < 0) {
@@ -411,7 +413,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         }
         for (int k = 0; k < nw; ++k) {
             const int st = k % C::NSTAGE;
-            if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status)) break;
+            if (!mbar_wait(&bars[st], (k / C::NSTAGE) & 1, a.status, a.wait_ns)) break;
             const uint8_t *kb = ring + st * C::STAGE;
             uint8_t *vb = ring + st * C::STAGE + C::HB;
             const int pg = p0 + warp + NW * k;
@@ -527,7 +529,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             int nvalid[NPG];
 #pragma unroll
             for (int i = 0; i < NPG; ++i) {
-                if (!mbar_wait(&bars[S0 + i], parity, a.status)) return false;
+                if (!mbar_wait(&bars[S0 + i], parity, a.status, a.wait_ns)) return false;
                 // slots >= nvalid are past the end; a bad page id (reported
                 // at issue time, nothing copied) masks the whole stage
                 const int pg = p0 + warp + NW * (k + i);

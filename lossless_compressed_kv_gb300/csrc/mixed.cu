@@ -155,6 +155,8 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
     m.d.ws_o = (float *)ws;
     m.d.ws_ml = m.d.ws_o + (size_t)batch * hq * splits * d;
     m.d.status = status;
+    m.d.wait_ns = wait_fault().wait_ns;
+    m.d.skip_copies = wait_fault().skip_copies;
     void *vws = (uint8_t *)ws + draft_part(comp, hq, max_seq_len);
     if (!verify_args(m.v, q_verify, n_q, hq, full, scale, max_seq_len, vws, status)) return cudaErrorInvalidValue;
     m.role = role;

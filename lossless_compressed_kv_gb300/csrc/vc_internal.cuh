@@ -76,21 +76,31 @@ __device__ inline uint64_t global_ns() {
     return t;
 }
 
-// Bounded wait: gives up after about 2 seconds of wall-clock time, reports
-// VC_ERR_TIMEOUT and returns false (the caller then drains and exits).
+// Bounded wait: gives up after limit_ns of wall-clock time (2 s unless a
+// test lowered it with vc_debug_set_wait_fault), reports VC_ERR_TIMEOUT and
+// returns false (the caller then drains and exits).
 constexpr uint64_t kWaitNs = 2000000000ull;
-__device__ inline bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *st) {
+__device__ inline bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *st, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitNs) {
+        if (global_ns() - t0 > limit_ns) {
             report(st, VC_ERR_TIMEOUT);
             return false;
         }
     }
 }
+
+// Host-side fault injection for the tests of the bounded waits
+// (vc_debug_set_wait_fault): the wait limit and whether the draft and
+// verification kernels skip their KV copies, read by every launch.
+struct WaitFault {
+    uint64_t wait_ns = kWaitNs;
+    int skip_copies = 0;
+};
+WaitFault wait_fault();
 
 // One bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).
 __device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

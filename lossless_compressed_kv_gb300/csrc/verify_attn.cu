@@ -116,6 +116,8 @@ bool verify_args(Args &a, const void *q, int n_q, int hq, const vc_paged_kv &f, 
     a.ws_o = (float *)ws;
     a.ws_ml = a.ws_o + (size_t)f.batch * n_q * hq * a.n_splits * f.fmt.head_dim;
     a.status = status;
+    a.wait_ns = wait_fault().wait_ns;
+    a.skip_copies = wait_fault().skip_copies;
     return encode_pool(&a.kmap, f.k_pages, f.num_pages, a.hkv, f.fmt.head_dim) &&
            encode_pool(&a.vmap, f.v_pages, f.num_pages, a.hkv, f.fmt.head_dim);
 }

@@ -63,6 +63,8 @@ struct Args {
     float *ws_o;        // [B][n_q][Hq][n_splits][D]
     float *ws_ml;       // [..][2]
     int32_t *status;
+    uint64_t wait_ns = kWaitNs;  // bounded-wait limit
+    int skip_copies = 0;         // fault injection: the producer issues no copy
 };
 
 template <int D, int QT>
@@ -364,10 +366,10 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     constexpr uint32_t IPV = idesc_bf16(128, D, true);
     if (producer) {
         // ================= producer: TMA tensor copies into the stage ring =================
-        if (lane == 0) {
+        if (lane == 0 && !a.skip_copies) {
             for (int j = 0; j < nb && alive; ++j) {
                 const int st = j % C::STAGES;
-                if (j >= C::STAGES) alive = mbar_wait(&empty[st], ((j / C::STAGES) - 1) & 1, a.status);
+                if (j >= C::STAGES) alive = mbar_wait(&empty[st], ((j / C::STAGES) - 1) & 1, a.status, a.wait_ns);
                 if (!alive) break;
                 uint8_t *kt = skv + st * 2 * C::KTILE;
                 mbar_arrive_expect_tx(&full[st], 2 * C::KTILE);
@@ -431,12 +433,12 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 umma_commit(&empty[j % C::STAGES]);
             };
             auto wait_p = [&](int j, int qt) {
-                alive = alive && mbar_wait(&p_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status);
+                alive = alive && mbar_wait(&p_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status, a.wait_ns);
                 tc_fence_after();
             };
             for (int j = 0; j < nb && alive; ++j) {
                 const int st = j % C::STAGES;
-                alive = mbar_wait(&full[st], (j / C::STAGES) & 1, a.status);
+                alive = mbar_wait(&full[st], (j / C::STAGES) & 1, a.status, a.wait_ns);
                 if (!alive) break;
                 tc_fence_after();
                 const uint8_t *kt = skv + st * 2 * C::KTILE;
@@ -500,7 +502,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
         // tcgen05.ld / st are warp-collective: every lane of a softmax warp runs
         // them together (row validity and rescale decisions only pick values)
         for (int j = 0; j < nb && alive; ++j) {
-            alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status));
+            alive = __all_sync(0xffffffffu, mbar_wait(&s_ready[qt * 2 + j % C::SB], (j / C::SB) & 1, a.status, a.wait_ns));
             if (!alive) break;
             tc_fence_after();
             float s[C::BK];
@@ -525,7 +527,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
             if (__any_sync(0xffffffffu, grow) && o_touched) {
                 // the previous block's P V must have landed before O is rescaled
                 alive = __all_sync(0xffffffffu,
-                                   mbar_wait(&pv_done[qt * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1, a.status));
+                                   mbar_wait(&pv_done[qt * 2 + ((j - 1) & 1)], ((j - 1) >> 1) & 1, a.status, a.wait_ns));
                 if (!alive) break;
                 tc_fence_after();
                 for (int c0 = 0; c0 < D; c0 += 16) {
@@ -594,7 +596,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
         bool have_o = nb > 0 && alive;
         if (have_o) {
             have_o = __all_sync(0xffffffffu,
-                                mbar_wait(&pv_done[qt * 2 + ((nb - 1) & 1)], ((nb - 1) >> 1) & 1, a.status));
+                                mbar_wait(&pv_done[qt * 2 + ((nb - 1) & 1)], ((nb - 1) >> 1) & 1, a.status, a.wait_ns));
             alive = have_o;
         }
         if (have_o) {

@@ -95,6 +95,33 @@ def test_draft_matches_oracle(bits, d, hkv, grp, lens):
         assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4, 16])
+@pytest.mark.parametrize("qstd", [1.0 / 64, 64.0, 1024.0])
+def test_draft_query_range(bits, qstd):
+    """Queries far from N(0, 1): rotary-embedded queries of real models reach
+    tens to hundreds, and small ones lose bits in narrow formats.  q ~
+    N(0, qstd^2) with 4 K outlier channels x10 against the oracle: the
+    quantised path carries q in f16 operands pre-scaled per register, so the
+    small end tests its subnormal range and the large end its overflow
+    headroom (|q| up to several thousand at qstd 1024)."""
+    rng = np.random.default_rng(int(qstd * 64) + bits)
+    d, hkv, grp = 128, 2, 4
+    lens = [3000, 17, 700]
+    full, hf = H.full_cache(rng, lens, hkv, d, synth.outlier_channels(rng, d, 4), 10.0)
+    kept = [np.arange(n, dtype=np.int32) for n in lens]
+    comp, _ = H.comp_cache(rng, len(lens), lens, hkv, d, bits)
+    compress_all(full, comp, kept)
+    qn = synth.normal_bf16(rng, (len(lens), hkv * grp, d), std=qstd)
+    qd = H.to_dev(qn.view(np.int16)).view(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    got = gpu_draft(comp, qd, scale, max(lens))
+    assert np.isfinite(got).all()
+    for b in range(len(lens)):
+        k, v = H.logical_full(hf, b)
+        ref = oracle.draft_attn(qn[b], oracle.compress(k, v, kept[b], bits), float(np.float32(scale)))
+        assert H.row_err(got[b], ref) <= H.TOL, (b, H.row_err(got[b], ref))
+
+
 def test_draft_empty_request_gives_zeros():
     rng = np.random.default_rng(5)
     full, hf = H.full_cache(rng, [40, 40], 1, 64)
@@ -344,8 +371,9 @@ def test_verify_full_size_sampled(name, n_q):
 
 def test_mixed_launch_matches_oracle_and_standalone():
     """Staggered batch: even requests draft over 3-bit KV_comp, odd requests
-    verify x = 25 over KV_full, in one launch.  Draft rows match the oracle;
-    verify rows are bit-identical to the standalone verification kernel."""
+    verify x = 25 over KV_full, in one launch.  Draft and verify rows match
+    the oracle; verify rows are also bit-identical to the standalone
+    verification kernel."""
     rng = np.random.default_rng(44)
     d, hkv, grp, n_q, bits = 128, 2, 4, 25, 3
     lens = [3000, 2100, 700, 4500, 1234, 90]
@@ -375,8 +403,66 @@ def test_mixed_launch_matches_oracle_and_standalone():
             assert H.row_err(od[b], ref) <= H.TOL
             assert np.all(ov[b] == 7.0)           # other role's buffer untouched
         else:
+            k, v = H.logical_full(hf, b)
+            ref = oracle.verify_attn_block(qvn[b], k, v, float(np.float32(scale)))
+            assert H.row_err(ov[b], ref) <= H.TOL
             assert np.array_equal(ov[b], alone[b])
             assert np.all(od[b] == 7.0)
+
+
+def test_mixed_launch_full_size_workload():
+    """The staggered mixed workload at its stated size, in one vc_mixed_attn
+    call: 32 requests with contexts drawn uniformly from [8192, 65536], 32
+    query / 8 kv heads, head_dim 128, 3-bit group-32 KV_comp; even requests
+    draft, odd requests verify a block of x = 25 over KV_full.  Every draft
+    row is checked against the oracle over the same KV_comp, and 4 seeded
+    (query, head) rows of each verifying request (64 rows) against the
+    oracle's causal attention over KV_full."""
+    from concurrent.futures import ThreadPoolExecutor
+    w = synth.WORKLOADS["mixed_32req_3bit"]
+    B, hq, hkv, d, x, bits = w["batch"], w["hq"], w["hkv"], w["d"], w["x"], w["bits"]
+    rng = synth.rng_for("mixed_32req_3bit", 1)
+    ctx = rng.integers(w["ctx_lo"], w["ctx_hi"] + 1, size=B).astype(np.int64)
+    role = np.array([b % 2 for b in range(B)], np.int32)
+    full_lens = [int(n) + x for n in ctx]            # a verifying request holds its block too
+    full, hf = H.full_cache(rng, full_lens, hkv, d)
+    kept = [np.arange(int(n), dtype=np.int32) for n in ctx]
+    comp, _ = H.comp_cache(rng, B, [len(k) for k in kept], hkv, d, bits)
+    compress_all(full, comp, kept)
+    qdn, qdd = q_bf16(rng, (B, hq, d))
+    qvn, qvd = q_bf16(rng, (B, x, hq, d))
+    scale = 1.0 / math.sqrt(d)
+    m = vc()
+    msl = max(full_lens)
+    od = torch.full((B, hq, d), 7.0, device="cuda")
+    ov = torch.full((B, x, hq, d), 7.0, device="cuda")
+    ws = torch.empty(m.mixed_workspace_bytes(comp, full, x, hq, msl), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.mixed_attn(H.to_dev(role), qdd, comp, od, qvd, full, ov, scale, msl, ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    od, ov = od.cpu().numpy(), ov.cpu().numpy()
+    del full, comp, ws
+    samp = np.random.default_rng(2)
+    sc = float(np.float32(scale))
+    with ThreadPoolExecutor(oracle.threads()) as pool:
+        for b in range(B):
+            k, v = H.logical_full(hf, b)
+            if role[b] == 0:
+                ref = oracle.draft_attn(qdn[b], oracle.compress(k[:ctx[b]], v[:ctx[b]], kept[b], bits), sc,
+                                        pool=pool)
+                assert H.row_err(od[b], ref) <= H.TOL, (b, H.row_err(od[b], ref))
+                assert np.all(ov[b] == 7.0)
+            else:
+                qs = [0, x - 1] + [int(i) for i in samp.integers(1, x - 1, 2)]
+                hs = [int(h) for h in samp.integers(0, hq, 4)]
+                rows = list(zip(qs, hs))
+                ref = oracle.verify_attn(qvn[b], k, v, sc, heads=sorted(set(hs)), queries=sorted(set(qs)),
+                                         pool=pool)
+                for i, h in rows:
+                    e = H.row_err(ov[b, i, h], ref[i, h])
+                    assert e <= H.TOL, (b, i, h, e)
+                assert np.all(od[b] == 7.0)
 
 
 @pytest.mark.parametrize("bits,n_q", [(2, 9), (16, 9), (2, 40)])

@@ -53,9 +53,9 @@ def test_paced_copy_argument_errors():
 
 
 def test_remote_prefix_engine_outputs_and_pacing():
-    import bench
+    from synth.rigs import remote_rig
     import lossless_compressed_kv_gb300 as vc
-    eng, qd, qv, q1, ones = bench.remote_rig(SPEC, torch.device("cuda"))
+    eng, qd, qv, q1, ones = remote_rig(SPEC, torch.device("cuda"))
     rate, chunk = 2.0, 64 << 10
     outs = []
     vr = eng.run_vericache(qd, qv, SPEC["rounds"], rate, chunk, outputs=outs)

@@ -22,8 +22,8 @@ SPEC = dict(batch=6, hq=8, hkv=2, d=128, ctx_lo=600, ctx_hi=3000, layers=2, bits
 
 @pytest.fixture(scope="module")
 def rig():
-    import bench
-    eng, qd, qv = bench.stagger_rig(SPEC, torch.device("cuda"))
+    from synth.rigs import stagger_rig
+    eng, qd, qv = stagger_rig(SPEC, torch.device("cuda"))
     return eng, qd, qv
 
 

@@ -57,20 +57,46 @@ def test_static_scratch_draft_matches_workspace_draft_twice():
     assert lib.vc_static_scratch_bytes() == 8 << 20
     # two calls in a row with different shapes / data: the second must not see
     # anything left over from the first in the shared array
-    for seed, lens in ((1, [3000, 17, 900]), (2, [40, 5000, 2047, 1, 600])):
+    for i, (seed, lens) in enumerate(((1, [3000, 17, 900]), (2, [40, 5000, 2047, 1, 600]))):
         comp, q = _setup(seed, lens)
         scale = 1.0 / math.sqrt(128)
-        assert vc.draft_workspace_bytes(comp, q.shape[1], max(lens)) <= lib.vc_static_scratch_bytes()
+        need = vc.draft_workspace_bytes(comp, q.shape[1], max(lens))
+        assert need <= lib.vc_static_scratch_bytes()
+        # the partials of more than one context chunk per row go through the
+        # array, so the combine pass reads what this call wrote there
+        assert need // (len(lens) * q.shape[1] * (128 + 2) * 4) > 1
         out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         rc = _static_call(lib, q, comp, scale, out, max(lens), st)
         assert rc == 0, vc.STATUS.get(rc, rc)
+        torch.cuda.synchronize()
+        if i == 1:   # device set up by the first call: the second allocates nothing
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == alloc0
         ref = _reference(comp, q, scale, max(lens))
         torch.cuda.synchronize()
         assert st.item() == 0
         got, want = out.cpu().numpy(), ref.cpu().numpy()
         assert np.isfinite(got).all()
         assert H.row_err(got, want) <= H.TOL
+
+
+def test_static_scratch_empty_batch_with_null_pointers():
+    """Batch 0: the format is checked and VC_OK returned before any pointer
+    is looked at, as vc_draft_attn does (zero-size tensors carry null data
+    pointers)."""
+    import lossless_compressed_kv_gb300 as vc
+    lib = vc.library()
+    lib.vc_draft_attn_static.restype = C.c_int
+    lib.vc_draft_attn_static.argtypes = [C.c_void_p, C.c_int32, C.POINTER(vc.PagedKVStruct), C.c_float,
+                                         C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]
+    s = vc.PagedKVStruct(None, None, 0, None, None, 0, 0, vc.KVFormat(2, 128, 2))
+    assert lib.vc_draft_attn_static(None, 8, C.byref(s), C.c_float(0.1), None, 64, None, None) == 0
+    s.fmt = vc.KVFormat(2, 96, 2)         # an unsupported head_dim is still refused
+    assert vc.STATUS[lib.vc_draft_attn_static(None, 8, C.byref(s), C.c_float(0.1), None, 64, None,
+                                              None)] == "VC_ERR_UNSUPPORTED"
 
 
 def test_static_scratch_rejects_oversized_calls():
