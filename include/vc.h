@@ -51,13 +51,42 @@
  *    bytes starting at h * vc_head_block_bytes(); token slot s = position % 16.
  *  - bits == 16 (bf16, KV_full or token-drop KV_comp):
  *      block = bf16 [16][head_dim]                              (32 * D bytes)
- *  - bits in {2, 3, 4} (quantised KV_comp), D = head_dim, G = D / 32 groups:
- *      codes  uint8 [16][D * bits / 8]   token slot s, channel i uses bits
+ *  - bits in {2, 3, 4} (quantised KV_comp), D = head_dim (64, 128 or 256),
+ *    G = D / 32 groups.  A head block holds, per token slot s (0..15) and
+ *    32-channel group, the codes of the slot's D channels and an fp16 scale
+ *    and zero (2 * D * (bits + 1) bytes in all).
+ *    Logical content (what vc_comp_block_decode returns and the quantiser
+ *    defines):
+ *      codes  uint8 [16][D * bits / 8]   slot s, channel i at bits
  *                                        [bits*i, bits*i + bits) of the slot's
  *                                        little-endian byte string
- *      scales fp16  [16][G]              per token and 32-channel group
+ *      scales fp16  [16][G]              per slot and 32-channel group
  *      zeros  fp16  [16][G]
- *                                        (2 * D * (bits + 1) bytes in all)
+ *    Stored order (what the pools hold; chosen so that the draft kernel turns
+ *    packed words into tensor-core operands with one mask per register):
+ *      bytes [0, 16 D bits / 8)       the code region; K and V blocks place
+ *                                     codes differently (below)
+ *      then fp16 scales, then fp16 zeros, each [16 slots][G], as in the
+ *      logical content
+ *    Code bit offsets from the start of the code region (channel c, slot s;
+ *    for bits 3 "low" = the code's low two bits, "high" = its top bit; every
+ *    field lies inside one little-endian 32-bit word):
+ *      K: ks = c / 16, t = (c / 4) % 4, e = c % 4, r = 2 ks + e / 2, h = e % 2
+ *        bits 2: s 2D + t D/2 + 32 (r / 8) + 16 h + 2 (r % 8)
+ *        bits 4: s 4D + t D   + 32 (r / 4) + 16 h + 4 (r % 4)
+ *        bits 3 low:  s 3D + t D/2 + 32 (r / 8) + 16 h + 2 (r % 8)
+ *        bits 3 high: with u = r / 8, j = r % 8, S = 2 (u % 2) + j / 4,
+ *          beta = 2 (j % 4) + {0, 1, 8, 9}[S]:
+ *          D = 64: s 3D + 2D + 16 t + 8 h + beta;
+ *          else:   s 3D + 2D + t D/4 + 32 (u / 2) + 16 h + beta
+ *      V (channel-major, so that one thread reads one channel's codes of a
+ *      page in one or two words):
+ *        bits 2: 32 c + 16 (s % 2) + 2 (s / 2)
+ *        bits 3 low:  32 c + 16 (s % 2) + 2 (s / 2)
+ *        bits 3 high: 32 D + 32 (c / 2) + 16 (s % 2) + 2 (s / 2) + c % 2
+ *        bits 4: 32 (2 c + s / 8) + 16 (s % 2) + 4 ((s % 8) / 2)
+ *    vc_comp_block_decode / vc_comp_block_encode (host functions, below)
+ *    convert one stored head block to and from the logical content.
  *    Quantisation of one group x[0..31] (bf16 values, fp32 arithmetic, every
  *    operation rounded to nearest even, no contraction):
  *      mn = min x (a -0 minimum is stored as +0), mx = max x
@@ -125,6 +154,23 @@ typedef struct {
 /* Bytes of one page (all kv heads) and of one kv head's block in a page. */
 VC_API size_t vc_page_bytes(const vc_kv_format *fmt);
 VC_API size_t vc_head_block_bytes(const vc_kv_format *fmt);
+
+/*
+ * vc_comp_block_decode / vc_comp_block_encode -- host conversions of one
+ * quantised KV_comp head block (vc_head_block_bytes(fmt) bytes, bits 2, 3 or
+ * 4) between its stored order and the logical content described in the
+ * layout notes above.  kind: 0 = a block of the K pool, 1 = of the V pool
+ * (they order codes and parameters differently).  All pointers are host
+ * memory owned by the caller: codes uint8 [16][D * bits / 8] (little-endian
+ * bit string per slot), scales and zeros fp16 bits [16][D / 32].  encode
+ * writes every byte of the block; bytes of a code's unused bit positions
+ * are 0.  VC_ERR_INVALID_ARG for a null pointer, another kind or a format
+ * other than bits 2 / 3 / 4 with head_dim 64, 128 or 256.  No CUDA call.
+ */
+VC_API vc_status vc_comp_block_decode(const vc_kv_format *fmt, int32_t kind, const void *block, uint8_t *codes,
+                                      uint16_t *scales, uint16_t *zeros);
+VC_API vc_status vc_comp_block_encode(const vc_kv_format *fmt, int32_t kind, const uint8_t *codes,
+                                      const uint16_t *scales, const uint16_t *zeros, void *block);
 
 /*
  * vc_select_kept -- the kept-index list of a token-drop KV_comp ("VeriCache

@@ -99,6 +99,8 @@ _SIG = {
     "vc_stagger_horizon": (C.c_int, [C.POINTER(StaggerModel), C.c_int32, C.c_int32, C.c_int32,
                                      C.POINTER(C.c_int32), _P, C.POINTER(StaggerResult)]),
     "vc_debug_set_wait_fault": (C.c_int, [C.c_int64, C.c_int32]),
+    "vc_comp_block_decode": (C.c_int, [C.POINTER(KVFormat), C.c_int32, _P, _P, _P, _P]),
+    "vc_comp_block_encode": (C.c_int, [C.POINTER(KVFormat), C.c_int32, _P, _P, _P, _P]),
     "vc_status_string": (C.c_char_p, [C.c_int]),
     "vc_version": (C.c_char_p, []),
 }
@@ -140,6 +142,35 @@ def version() -> str:
 def library():
     """The loaded ctypes handle (for ABI tests)."""
     return _lib
+
+
+def comp_block_decode(block, head_dim: int, bits: int, kind: str):
+    """vc_comp_block_decode of one stored head block (host bytes, numpy
+    uint8 [vc_head_block_bytes]); kind "k" or "v".  Returns (codes uint8
+    [16][head_dim * bits / 8] little-endian per slot, scales, zeros fp16 bits
+    [16][head_dim / 32])."""
+    import numpy as np
+    blk = np.ascontiguousarray(block, dtype=np.uint8)
+    codes = np.empty((PAGE, head_dim * bits // 8), np.uint8)
+    sc = np.empty((PAGE, head_dim // GROUP), np.uint16)
+    ze = np.empty_like(sc)
+    f = KVFormat(1, head_dim, bits)
+    _check(_lib.vc_comp_block_decode(C.byref(f), 0 if kind == "k" else 1, blk.ctypes.data, codes.ctypes.data,
+                                     sc.ctypes.data, ze.ctypes.data), "vc_comp_block_decode")
+    return codes, sc, ze
+
+
+def comp_block_encode(codes, scales, zeros, head_dim: int, bits: int, kind: str):
+    """vc_comp_block_encode: logical content -> one stored head block (numpy uint8)."""
+    import numpy as np
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint16)
+    ze = np.ascontiguousarray(zeros, dtype=np.uint16)
+    f = KVFormat(1, head_dim, bits)
+    blk = np.empty(2 * head_dim * (bits + 1), np.uint8)
+    _check(_lib.vc_comp_block_encode(C.byref(f), 0 if kind == "k" else 1, codes.ctypes.data, sc.ctypes.data,
+                                     ze.ctypes.data, blk.ctypes.data), "vc_comp_block_encode")
+    return blk
 
 
 def debug_set_wait_fault(wait_limit_ns: int = 0, skip_copies: bool = False):

@@ -124,3 +124,92 @@ def test_oracle_and_library_share_no_code():
         assert "#include \"vc" not in txt and "libvc.so" not in txt
     pkg = open(os.path.join(ROOT, "lossless_compressed_kv_gb300", "__init__.py")).read()
     assert "import oracle" not in pkg and "from oracle" not in pkg
+
+
+# ---------------------------------------------------------------------------
+# KV_comp head blocks: stored order <-> logical content (host helpers)
+# ---------------------------------------------------------------------------
+
+def _header_k_bit(bits, d, s, c, plane):
+    """The K code placement exactly as the layout notes of include/vc.h
+    write it (bit offset of the code's low bit; plane 1 = top bit of a 3-bit
+    code)."""
+    ks, t, e = c // 16, (c // 4) % 4, c % 4
+    r, h = 2 * ks + e // 2, e % 2
+    if bits == 2:
+        return s * 2 * d + t * d // 2 + 32 * (r // 8) + 16 * h + 2 * (r % 8)
+    if bits == 4:
+        return s * 4 * d + t * d + 32 * (r // 4) + 16 * h + 4 * (r % 4)
+    if plane == 0:
+        return s * 3 * d + t * d // 2 + 32 * (r // 8) + 16 * h + 2 * (r % 8)
+    u, j = r // 8, r % 8
+    beta = 2 * (j % 4) + [0, 1, 8, 9][2 * (u % 2) + j // 4]
+    if d == 64:
+        return s * 3 * d + 2 * d + 16 * t + 8 * h + beta
+    return s * 3 * d + 2 * d + t * d // 4 + 32 * (u // 2) + 16 * h + beta
+
+
+def _header_v_bit(bits, d, s, c, plane):
+    if bits == 4:
+        return 32 * (2 * c + s // 8) + 16 * (s % 2) + 4 * ((s % 8) // 2)
+    if bits == 2 or plane == 0:
+        return 32 * c + 16 * (s % 2) + 2 * (s // 2)
+    return 32 * d + 32 * (c // 2) + 16 * (s % 2) + 2 * (s // 2) + c % 2
+
+
+def _header_param(kind, g, s, gr, bits):
+    return s * g + gr
+
+
+@pytest.mark.parametrize("bits,d", [(2, 64), (2, 128), (3, 64), (3, 128), (3, 256), (4, 64), (4, 128)])
+@pytest.mark.parametrize("kind", ["k", "v"])
+def test_comp_block_helpers_follow_the_header(vc, bits, d, kind):
+    """One code of value 2^b - 1 (or, for 3 bits, each plane's bit) at a time:
+    the stored block vc_comp_block_encode writes has exactly those bits set,
+    at the offsets the header's formulas give; scales and zeros land at the
+    header's parameter indices; decode inverts encode."""
+    import numpy as np
+    rng = np.random.default_rng(bits * 100 + d + (kind == "v"))
+    g = d // 32
+    row, cr = d * bits // 8, 16 * d * bits // 8
+    f = _header_k_bit if kind == "k" else _header_v_bit
+    z16 = np.zeros((16, g), np.uint16)
+    for s, c in [(0, 0), (15, d - 1)] + [tuple(x) for x in rng.integers(0, [16, d], (12, 2))]:
+        codes = np.zeros((16, row), np.uint8)
+        for j in range(bits):           # code 2^b - 1: all its bits
+            bit = bits * c + j
+            codes[s, bit // 8] |= 1 << (bit % 8)
+        blk = vc.comp_block_encode(codes, z16, z16, d, bits, kind)
+        want = set()
+        for j in range(bits):
+            want.add(f(bits, d, s, c, 1) if bits == 3 and j == 2 else f(bits, d, s, c, 0) + j)
+        got = set(np.nonzero(np.unpackbits(blk[:cr], bitorder="little"))[0].tolist())
+        assert got == want, (s, c)
+        assert not blk[cr:].any()
+        back = vc.comp_block_decode(blk, d, bits, kind)
+        assert np.array_equal(back[0], codes)
+    sc = rng.integers(0, 1 << 16, (16, g)).astype(np.uint16)
+    ze = rng.integers(0, 1 << 16, (16, g)).astype(np.uint16)
+    blk = vc.comp_block_encode(np.zeros((16, row), np.uint8), sc, ze, d, bits, kind)
+    par = blk[cr:].view(np.uint16)
+    for s in range(16):
+        for gr in range(g):
+            i = _header_param(kind, g, s, gr, bits)
+            assert par[i] == sc[s, gr] and par[16 * g + i] == ze[s, gr]
+    # every bit of a random stored block is used: decode then encode is the identity
+    rand = rng.integers(0, 256, 2 * d * (bits + 1)).astype(np.uint8)
+    assert np.array_equal(vc.comp_block_encode(*vc.comp_block_decode(rand, d, bits, kind), d, bits, kind), rand)
+
+
+def test_comp_block_helpers_reject_bad_arguments(vc):
+    import numpy as np
+    blk = np.zeros(768, np.uint8)
+    for d, bits in ((128, 16), (96, 2), (32, 2), (128, 5)):
+        with pytest.raises(vc.VCError):
+            vc.comp_block_decode(blk, d, bits, "k")
+    f = vc.KVFormat(1, 128, 2)
+    lib = vc.library()
+    z = np.zeros(4096, np.uint8)
+    assert lib.vc_comp_block_decode(C.byref(f), 2, z.ctypes.data, z.ctypes.data, z.ctypes.data,
+                                    z.ctypes.data) == 1
+    assert lib.vc_comp_block_encode(C.byref(f), 0, None, z.ctypes.data, z.ctypes.data, z.ctypes.data) == 1

@@ -126,3 +126,31 @@ def test_compress_8b_32k_full_size():
     comp, ctable = H.comp_cache(rng, w["batch"], w["ctx"], w["hkv"], w["d"], w["bits"])
     assert run_compress(full, comp, kept) == 0
     check(comp, ctable, hf, kept, w["bits"])
+
+
+@pytest.mark.parametrize("bits,d", [(2, 128), (3, 128), (4, 128), (3, 64), (2, 256)])
+def test_gpu_page_read_through_the_exported_helpers(bits, d):
+    """A C caller's view of KV_comp: head blocks written by vc_compress on
+    the GPU, copied to the host and converted by vc_comp_block_decode (no
+    test-side layout code), equal the oracle's packed little-endian codes,
+    scales and zeros byte for byte."""
+    import lossless_compressed_kv_gb300 as vc
+    rng = np.random.default_rng(900 + bits + d)
+    hkv, n = 2, 16 * 5 + 7
+    full, hf = H.full_cache(rng, [n], hkv, d, outliers=synth.outlier_channels(rng, d, 2), oscale=10.0)
+    kept = [np.arange(n, dtype=np.int32)]
+    comp, ctable = H.comp_cache(rng, 1, n, hkv, d, bits)
+    assert run_compress(full, comp, kept) == 0
+    k, v = H.logical_full(hf, 0)
+    ref = oracle.compress(k, v, kept[0], bits)
+    hb = vc.head_block_bytes(d, bits)
+    pools = {"k": comp.k_pages.cpu().numpy().reshape(-1, hkv, hb), "v": comp.v_pages.cpu().numpy().reshape(-1, hkv, hb)}
+    for kind in ("k", "v"):
+        for p in range((n + 15) // 16):
+            for h in range(hkv):
+                codes, sc, ze = vc.comp_block_decode(pools[kind][ctable[0][p], h], d, bits, kind)
+                s = np.arange(16 * p, min(n, 16 * p + 16))
+                m = len(s)
+                assert np.array_equal(codes[:m], ref[kind + "_packed"][s, h]), (kind, p, h)
+                assert np.array_equal(sc[:m], ref[kind + "_scales"][s, h]), (kind, p, h)
+                assert np.array_equal(ze[:m], ref[kind + "_zeros"][s, h]), (kind, p, h)

@@ -68,20 +68,24 @@ def test_waits_time_out_and_the_next_call_is_clean(fault):
     with pytest.raises(m.VCError):
         fault(-1, True)                                     # out of range: refused
     fault(LIMIT_NS, True)
-    calls = [
-        lambda st: m.draft_attn(qd, comp, scale, od, msl, dws, status=st),
-        lambda st: m.verify_attn(qv, full, scale, ov, msl, vws, status=st),          # two 128-row tiles
-        lambda st: m.verify_attn(qv[:, :25].contiguous(), full, scale, om, msl, vws, status=st),   # one tile
-        lambda st: m.mixed_attn(role, qd, comp, od, qv[:, :25].contiguous(), full, om, scale, msl, mws,
-                                status=st),
+    roles = np.array([0, 1, 0])
+    calls = [   # (call, outputs it writes and the rows written)
+        (lambda st: m.draft_attn(qd, comp, scale, od, msl, dws, status=st), [(od, [0, 1, 2])]),
+        (lambda st: m.verify_attn(qv, full, scale, ov, msl, vws, status=st), [(ov, [0, 1, 2])]),   # two 128-row tiles
+        (lambda st: m.verify_attn(qv[:, :25].contiguous(), full, scale, om, msl, vws, status=st),
+         [(om, [0, 1, 2])]),                                                                        # one tile
+        (lambda st: m.mixed_attn(role, qd, comp, od, qv[:, :25].contiguous(), full, om, scale, msl, mws, status=st),
+         [(od, list(np.nonzero(roles == 0)[0])), (om, list(np.nonzero(roles == 1)[0]))]),
     ]
-    for call in calls:
+    for call, outs in calls:
+        for t in (od, ov, om):
+            t.fill_(float("nan"))
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         call(st)
         torch.cuda.synchronize()
         assert st.item() == TIMEOUT
-        assert torch.isfinite(od).all() and torch.isfinite(ov).all() and torch.isfinite(om).all()
-    assert bool((ov == 0).all()) and bool((od == 0).all())
+        for t, rows in outs:                                # every row the call owns: written, zero
+            assert bool((t[rows] == 0).all())
 
     fault(0, False)                                         # back to normal: exact again
     st = torch.zeros(1, dtype=torch.int32, device="cuda")

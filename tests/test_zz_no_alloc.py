@@ -7,6 +7,7 @@ the attention tolerance used by the other tests, on two calls in a row that
 share the library's fixed scratch array.  Collected last so that a failure
 here does not hide the others."""
 import ctypes as C
+import gc
 import math
 
 import numpy as np
@@ -67,14 +68,22 @@ def test_static_scratch_draft_matches_workspace_draft_twice():
         assert need // (len(lens) * q.shape[1] * (128 + 2) * 4) > 1
         out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        torch.cuda.synchronize()
-        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-        rc = _static_call(lib, q, comp, scale, out, max(lens), st)
+        # no garbage collection inside the measured window: freed tensors of
+        # earlier calls must not show up as a change
+        gc.collect()
+        gc.disable()
+        try:
+            torch.cuda.synchronize()
+            free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+            rc = _static_call(lib, q, comp, scale, out, max(lens), st)
+            torch.cuda.synchronize()
+            free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
         assert rc == 0, vc.STATUS.get(rc, rc)
-        torch.cuda.synchronize()
         if i == 1:   # device set up by the first call: the second allocates nothing
-            assert torch.cuda.mem_get_info()[0] == free0
-            assert torch.cuda.memory_allocated() == alloc0
+            assert free1 == free0
+            assert alloc1 == alloc0
         ref = _reference(comp, q, scale, max(lens))
         torch.cuda.synchronize()
         assert st.item() == 0
