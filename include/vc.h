@@ -63,11 +63,13 @@
  *      scales fp16  [16][G]              per slot and 32-channel group
  *      zeros  fp16  [16][G]
  *    Stored order (what the pools hold; chosen so that the draft kernel turns
- *    packed words into tensor-core operands with one mask per register):
+ *    packed words into mma.sync fragments with one mask, sometimes one
+ *    shift, per operand register):
  *      bytes [0, 16 D bits / 8)       the code region; K and V blocks place
  *                                     codes differently (below)
- *      then fp16 scales, then fp16 zeros, each [16 slots][G], as in the
- *      logical content
+ *      then fp16 scales, then fp16 zeros, 16 G values each:
+ *        K block: [16 slots][G], as in the logical content
+ *        V block: [4][G][4], entry [t][g][i] = slot 2t + (i & 1) + 8 (i >> 1)
  *    Code bit offsets from the start of the code region (channel c, slot s;
  *    for bits 3 "low" = the code's low two bits, "high" = its top bit; every
  *    field lies inside one little-endian 32-bit word):
@@ -79,12 +81,13 @@
  *          beta = 2 (j % 4) + {0, 1, 8, 9}[S]:
  *          D = 64: s 3D + 2D + 16 t + 8 h + beta;
  *          else:   s 3D + 2D + t D/4 + 32 (u / 2) + 16 h + beta
- *      V (channel-major, so that one thread reads one channel's codes of a
- *      page in one or two words):
- *        bits 2: 32 c + 16 (s % 2) + 2 (s / 2)
- *        bits 3 low:  32 c + 16 (s % 2) + 2 (s / 2)
- *        bits 3 high: 32 D + 32 (c / 2) + 16 (s % 2) + 2 (s / 2) + c % 2
- *        bits 4: 32 (2 c + s / 8) + 16 (s % 2) + 4 ((s % 8) / 2)
+ *      V: g = c % 8, w = (c / 8) % 2, m = c / 16, t = (s / 2) % 4,
+ *         hi = s / 8, h = s % 2, R = 4 g + t
+ *        bits 4: 32 (R D/16 + m) + 16 h + 8 w + 4 hi
+ *        bits 2 and bits 3 low, with u = m / 2, n = m % 2:
+ *                32 (R D/32 + u) + 16 h + 8 n + 4 w + 2 hi
+ *        bits 3 high: j = 2 w + hi, S = 2 (u % 2) + n,
+ *                32 D + 32 (R D/64 + u / 2) + 16 h + 2 j + {0, 1, 8, 9}[S]
  *    vc_comp_block_decode / vc_comp_block_encode (host functions, below)
  *    convert one stored head block to and from the logical content.
  *    Quantisation of one group x[0..31] (bf16 values, fp32 arithmetic, every

@@ -38,8 +38,8 @@ int stored_bit(int kind, int bits, int d, int s, int c, int j) {
 
 // index (in fp16 units from the start of the scale array) of the parameter
 // of (slot s, group gr)
-int stored_param(int kind, int bits, int groups, int s, int gr) {
-    return kind == 0 ? s * groups + gr : vc::layout::v_param(bits, groups, s, gr);
+int stored_param(int kind, int groups, int s, int gr) {
+    return kind == 0 ? s * groups + gr : vc::layout::v_param(groups, s, gr);
 }
 
 }  // namespace
@@ -61,7 +61,7 @@ vc_status vc_comp_block_decode(const vc_kv_format *fmt, int32_t kind, const void
     const uint8_t *par = blk + cr;
     for (int s = 0; s < VC_PAGE_TOKENS; ++s)
         for (int gr = 0; gr < g; ++gr) {
-            const int i = stored_param(kind, b, g, s, gr);
+            const int i = stored_param(kind, g, s, gr);
             std::memcpy(scales + s * g + gr, par + 2 * i, 2);
             std::memcpy(zeros + s * g + gr, par + 2 * (VC_PAGE_TOKENS * g + i), 2);
         }
@@ -83,7 +83,7 @@ vc_status vc_comp_block_encode(const vc_kv_format *fmt, int32_t kind, const uint
     uint8_t *par = blk + cr;
     for (int s = 0; s < VC_PAGE_TOKENS; ++s)
         for (int gr = 0; gr < g; ++gr) {
-            const int i = stored_param(kind, b, g, s, gr);
+            const int i = stored_param(kind, g, s, gr);
             std::memcpy(par + 2 * i, scales + s * g + gr, 2);
             std::memcpy(par + 2 * (VC_PAGE_TOKENS * g + i), zeros + s * g + gr, 2);
         }

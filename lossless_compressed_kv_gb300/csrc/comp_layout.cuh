@@ -11,15 +11,21 @@
 //    is operand register r = 2 ks + (e >> 1), half e & 1: the two codes of a
 //    register sit at the same bit position of the two 16-bit halves of one
 //    word, so a mask leaves two f16 subnormals that are exactly code * 2^(p-24).
-//  * V codes: channel-major (see v_bit), so that a thread holding one channel
-//    reads that channel's codes of a page in one or two words.
-//  * 3 bits (K): the low two bits of each code use the 2-bit placement, the
-//    high bit a separate plane placed so that one shift and mask put it right
+//  * V codes, regions per fragment thread (g, t) of the V^T P^T product:
+//    thread (g, t) owns the codes of channels {16 mt + g, 16 mt + 8 + g}
+//    (all m-tiles mt) for tokens {2t, 2t+1, 2t+8, 2t+9}.  An operand
+//    register holds one channel of tokens (2t, 2t+1) or (2t+8, 2t+9); the
+//    four registers of an m-tile sit at positions p, p+VHI (second token
+//    pair) and, for the row g+8 channel, 4 higher (2- and 3-bit) or one
+//    byte higher (4-bit).
+//  * 3 bits: the low two bits of each code use the 2-bit placement, the high
+//    bit a separate plane placed so that one shift and mask put it right
 //    above the low bits of its register.
 //
 // Offsets are in bits from the start of the head block's code region (K) or
 // the V block's code region; every code of a plane lies inside one 32-bit
-// word.  Scales and zeros: fp16 [16 tokens][G] for K and V.
+// word.  Scales and zeros: K as fp16 [16 tokens][G], V as fp16
+// [4][G][4] with entry [t][group][i] for token 2t + (i & 1) + 8 (i >> 1).
 #pragma once
 
 namespace vc {
@@ -41,27 +47,27 @@ __host__ __device__ inline int k_bit(int bits, int D, int s, int c, int plane) {
 }
 
 // V code of token tau of channel c; plane 1 = high bit of a 3-bit code.
-// Channel-major: the tensor-memory operand of the tcgen05 draft kernel (lane
-// = channel, column = token pair) comes out of a channel's words with one
-// mask (or one shift and a mask, plus for 3 bits one merge) per column.
-//  * bits 2: one 32-bit word per channel, token tau at bit 16 (tau & 1) +
-//    2 (tau >> 1).
-//  * bits 3: the low two bits as bits 2 (words 0 .. D-1), then one 32-bit
-//    high-bit word per channel pair, bit 16 (tau & 1) + 2 (tau >> 1) + (c & 1).
-//  * bits 4: two words per channel (tokens 0-7, 8-15), token tau at bit
-//    16 (tau & 1) + 4 ((tau & 7) >> 1) of word 2 c + (tau >> 3).
 __host__ __device__ inline int v_bit(int bits, int D, int tau, int c, int plane) {
-    if (bits == 4) return 32 * (2 * c + (tau >> 3)) + 16 * (tau & 1) + 4 * ((tau & 7) >> 1);
-    if (bits == 2 || plane == 0) return 32 * c + 16 * (tau & 1) + 2 * (tau >> 1);
-    return 32 * D + 32 * (c >> 1) + 16 * (tau & 1) + 2 * (tau >> 1) + (c & 1);
+    const int g = c & 7, row8 = (c >> 3) & 1, mt = c >> 4;
+    const int t = (tau >> 1) & 3, hi = tau >> 3, half = tau & 1;
+    const int region = g * 4 + t;
+    if (bits == 4) return 32 * (region * (D / 16) + mt) + 16 * half + 8 * row8 + 4 * hi;
+    const int u = mt >> 1, m = mt & 1;  // word of the region: one 32-channel group
+    if (plane == 0) return 32 * (region * (D / 32) + u) + 16 * half + 8 * m + 4 * row8 + 2 * hi;
+    // 3 bits, high bit of the register at low-plane position p = 2 j (j < 4)
+    // of word u, shift 8 m: placed in a high-plane word so that one of four
+    // shifts lines it up at p + 2
+    const int j = 2 * row8 + hi;
+    const int set = 2 * (u & 1) + m;
+    const int beta = 2 * j + (set == 0 ? 0 : set == 1 ? 1 : set == 2 ? 8 : 9);
+    return 32 * D + 32 * (region * (D / 64) + (u >> 1)) + 16 * half + beta;
 }
 
 // Element index (in fp16 units from the start of the V scale array) of the
-// scale / zero of token tau, group gr; G = D / 32 groups: [16][G], a token's
-// parameters together (as for K).
-__host__ __device__ inline int v_param(int bits, int G, int tau, int gr) {
-    (void)bits;
-    return tau * G + gr;
+// scale / zero of token tau, group gr; G = D / 32 groups.
+__host__ __device__ inline int v_param(int G, int tau, int gr) {
+    const int t = (tau >> 1) & 3, i = 2 * (tau >> 3) + (tau & 1);
+    return (t * G + gr) * 4 + i;
 }
 
 }  // namespace layout

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kPageWarps * 32) compress_page_kernel(Compress
             }
             if (lane % LPG == 0) {
                 const int gr = lane / LPG;
-                const int e = kv ? layout::v_param(BITS, G, slot, gr) : slot * G + gr;
+                const int e = kv ? layout::v_param(G, slot, gr) : slot * G + gr;
                 uint16_t *par = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(blk[kv]) + CR);
                 par[e] = sh;
                 par[kPage * G + e] = zh;

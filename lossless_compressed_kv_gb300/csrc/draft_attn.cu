@@ -25,7 +25,6 @@
 //  - Online softmax in fp32 (log2 domain), partial (m, l, o) per chunk in the
 //    workspace, combined by draft_reduce_kernel.
 #include "draft_impl.cuh"
-#include "draft_tc.cuh"
 
 namespace vc {
 namespace {
@@ -62,26 +61,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinCtas<BITS, D>) draft_kernel(D
     draft::draft_block<BITS, D, kWarps>(a, split, unit % a.hkv, unit / a.hkv, chunk, smem);
 }
 
-// Quantised KV_comp: the tcgen05 body (draft_tc.cuh), same grid and chunk plan.
-template <int BITS, int D, int GP>
-__global__ void __launch_bounds__(dtc::Cfg<BITS, D, GP>::THREADS, 2)
-    draft_tc_kernel(const __grid_constant__ DraftArgs a) {
-    pdl_begin();
-    extern __shared__ __align__(1024) uint8_t smem[];
-    int c = blockIdx.x, unit, split, chunk;
-    if (c < a.lo_units * a.n_lo) {
-        unit = c / a.n_lo;
-        split = c % a.n_lo;
-        chunk = a.chunk_pages;
-    } else {
-        c -= a.lo_units * a.n_lo;
-        unit = a.lo_units + c / a.n_hi;
-        split = c % a.n_hi;
-        chunk = a.chunk_hi;
-    }
-    dtc::draft_tc_block<BITS, D, GP>(a, split, unit % a.hkv, unit / a.hkv, chunk, smem);
-}
-
 template <int D>
 __global__ void draft_reduce_kernel(const float *ws_o, const float *ws_ml, int n_splits, int grp, int hkv,
                                     int lo_units, int n_hi, int n_lo, float *out) {
@@ -114,24 +93,6 @@ int occupancy() {
     return occ;
 }
 
-// Resident CTAs per SM of the tcgen05 body: two.  Each CTA holds 256 of the
-// SM's 512 TMEM columns, and its shared memory request (at least 80 KB, with
-// the carveout set to the maximum) keeps a third one off the SM.  (The
-// occupancy query reports one here, but two run side by side: measured with
-// per-CTA SM ids and time stamps.)
-template <int BITS, int D, int GP>
-int occupancy_tc() {
-    static int occ = -1;
-    if (occ < 0) {
-        using C = dtc::Cfg<BITS, D, GP>;
-        cudaFuncSetAttribute(draft_tc_kernel<BITS, D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_ALLOC);
-        cudaFuncSetAttribute(draft_tc_kernel<BITS, D, GP>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        occ = 2;
-    }
-    return occ;
-}
-
 int num_sms() {
     static int n = 0;
     if (!n) {
@@ -144,7 +105,7 @@ int num_sms() {
 }
 
 template <int BITS, int D>
-Plan plan(int batch, int hkv, int max_seq_len, int occ, int gran) {
+Plan plan(int batch, int hkv, int max_seq_len) {
     // One full wave: as many CTAs as SMs x resident CTAs, every one inside
     // one unit.  When the slots are not a multiple of the units, (slots mod
     // units) units take one chunk more (smaller chunks), so that every slot
@@ -154,11 +115,11 @@ Plan plan(int batch, int hkv, int max_seq_len, int occ, int gran) {
     // SM run faster: that way an SM's CTAs end closer together.
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
-    const int64_t slots = (int64_t)num_sms() * occ;
-    const int cap = ceil_div(max_pages, gran);  // chunks are multiples of `gran` pages
+    const int64_t slots = (int64_t)num_sms() * occupancy<BITS, D>();
+    const int cap = ceil_div(max_pages, kWarps);  // a warp needs a page
     const int64_t per_unit = slots / units;
     const int base = per_unit < 1 ? 1 : (per_unit > cap ? cap : (int)per_unit);
-    auto chunk_for = [&](int splits) { return max(gran, ceil_div(ceil_div(max_pages, splits), gran) * gran); };
+    auto chunk_for = [&](int splits) { return max(kWarps, ceil_div(ceil_div(max_pages, splits), kWarps) * kWarps); };
     Plan p;
     p.chunk_pages = chunk_for(base);
     p.n_lo = max(1, ceil_div(max_pages, p.chunk_pages));
@@ -181,42 +142,16 @@ Plan plan(int batch, int hkv, int max_seq_len, int occ, int gran) {
 
 template <int BITS>
 Plan plan_b(int d, int batch, int hkv, int max_seq_len) {
-    return d == 64 ? plan<BITS, 64>(batch, hkv, max_seq_len, occupancy<BITS, 64>(), kWarps)
-                   : plan<BITS, 128>(batch, hkv, max_seq_len, occupancy<BITS, 128>(), kWarps);
+    return d == 64 ? plan<BITS, 64>(batch, hkv, max_seq_len) : plan<BITS, 128>(batch, hkv, max_seq_len);
 }
 
-// quantised formats: the tcgen05 body, chunks of whole 8-page tiles
-template <int BITS>
-Plan plan_tc(int d, int grp, int batch, int hkv, int max_seq_len) {
-    constexpr int T = dtc::Cfg<BITS, 128, 4>::TP;
-    const int occ = d == 64 ? (grp <= 4 ? occupancy_tc<BITS, 64, 4>() : occupancy_tc<BITS, 64, 8>())
-                            : (grp <= 4 ? occupancy_tc<BITS, 128, 4>() : occupancy_tc<BITS, 128, 8>());
-    return plan<BITS, 128>(batch, hkv, max_seq_len, occ, T);
-}
-
-Plan plan_any(int bits, int d, int grp, int batch, int hkv, int max_seq_len) {
+Plan plan_any(int bits, int d, int batch, int hkv, int max_seq_len) {
     switch (bits) {
-        case 2: return plan_tc<2>(d, grp, batch, hkv, max_seq_len);
-        case 3: return plan_tc<3>(d, grp, batch, hkv, max_seq_len);
-        case 4: return plan_tc<4>(d, grp, batch, hkv, max_seq_len);
+        case 2: return plan_b<2>(d, batch, hkv, max_seq_len);
+        case 3: return plan_b<3>(d, batch, hkv, max_seq_len);
+        case 4: return plan_b<4>(d, batch, hkv, max_seq_len);
         default: return plan_b<16>(d, batch, hkv, max_seq_len);
     }
-}
-
-template <int BITS, int D, int GP>
-cudaError_t launch_tc(const DraftArgs &a, int batch, cudaStream_t st) {
-    using C = dtc::Cfg<BITS, D, GP>;
-    occupancy_tc<BITS, D, GP>();  // sets the shared-memory attribute once
-    const int64_t units = (int64_t)batch * a.hkv;
-    const int64_t ctas = (int64_t)a.lo_units * a.n_lo + (units - a.lo_units) * a.n_hi;
-    launch_pdl(draft_tc_kernel<BITS, D, GP>, dim3((unsigned)ctas), C::THREADS, C::SMEM_ALLOC, st, a);
-    return cudaGetLastError();
-}
-
-template <int BITS>
-cudaError_t launch_tc_any(const DraftArgs &a, int d, int batch, cudaStream_t st) {
-    if (d == 64) return a.grp <= 4 ? launch_tc<BITS, 64, 4>(a, batch, st) : launch_tc<BITS, 64, 8>(a, batch, st);
-    return a.grp <= 4 ? launch_tc<BITS, 128, 4>(a, batch, st) : launch_tc<BITS, 128, 8>(a, batch, st);
 }
 
 template <int BITS, int D>
@@ -239,8 +174,7 @@ bool draft_supported(const vc_kv_format &f, int hq) {
 
 size_t draft_workspace(const vc_paged_kv &c, int hq, int max_seq_len) {
     if (max_seq_len <= 0) return 0;
-    const Plan p = plan_any(c.fmt.bits, c.fmt.head_dim, hq / c.fmt.num_kv_heads, c.batch, c.fmt.num_kv_heads,
-                            max_seq_len);
+    const Plan p = plan_any(c.fmt.bits, c.fmt.head_dim, c.batch, c.fmt.num_kv_heads, max_seq_len);
     return (size_t)c.batch * hq * p.n_splits * (c.fmt.head_dim + 2) * sizeof(float);
 }
 
@@ -249,7 +183,7 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
                          const void *v_new, const int32_t *slot) {
     const int d = c.fmt.head_dim, bits = c.fmt.bits;
     DraftArgs a;
-    const Plan p = plan_any(bits, d, hq / c.fmt.num_kv_heads, c.batch, c.fmt.num_kv_heads, max(max_seq_len, 1));
+    const Plan p = plan_any(bits, d, c.batch, c.fmt.num_kv_heads, max(max_seq_len, 1));
     a.q = (const uint16_t *)q;
     a.kp = (const uint8_t *)c.k_pages;
     a.vp = (const uint8_t *)c.v_pages;
@@ -277,14 +211,11 @@ cudaError_t draft_launch(const void *q, int hq, const vc_paged_kv &c, float scal
     a.slot = slot;
     cudaError_t e;
 #define VC_L(B_, D_) launch<B_, D_>(a, c.batch, st)
-    if (bits == 2)
-        e = launch_tc_any<2>(a, d, c.batch, st);
-    else if (bits == 3)
-        e = launch_tc_any<3>(a, d, c.batch, st);
-    else if (bits == 4)
-        e = launch_tc_any<4>(a, d, c.batch, st);
-    else
-        e = d == 64 ? VC_L(16, 64) : VC_L(16, 128);
+    if (d == 64) {
+        e = bits == 2 ? VC_L(2, 64) : bits == 3 ? VC_L(3, 64) : bits == 4 ? VC_L(4, 64) : VC_L(16, 64);
+    } else {
+        e = bits == 2 ? VC_L(2, 128) : bits == 3 ? VC_L(3, 128) : bits == 4 ? VC_L(4, 128) : VC_L(16, 128);
+    }
 #undef VC_L
     if (e != cudaSuccess) return e;
     dim3 rg(hq, c.batch);

@@ -10,7 +10,6 @@
 // draft body (6 warps) for requests with role 0; a block whose request has
 // the other role exits at once.  One combine launch finishes both.
 #include "draft_impl.cuh"
-#include "draft_tc.cuh"
 #include "verify_tc.cuh"
 
 namespace vc {
@@ -20,12 +19,10 @@ bool verify_args(vtc::Args &a, const void *q, int n_q, int hq, const vc_paged_kv
 
 namespace {
 
-// the tcgen05 draft body needs 7 warps (4 compute, a producer, two MMA
-// issuers); the verification body of one 128-row tile uses the first 6 (4
-// softmax, a producer, an MMA warp) and leaves the seventh idle
-constexpr int kThreads = 224;
+// the verification body of one 128-row tile needs 4 softmax warps, a
+// producer warp and an MMA warp; draft blocks use the same 6 warps
+constexpr int kThreads = vtc::Cfg<128, 1>::THREADS;
 constexpr int kDraftWarps = kThreads / 32;
-static_assert(vtc::Cfg<128, 1>::THREADS <= kThreads && vtc::Cfg<64, 1>::THREADS <= kThreads, "verify body fits");
 
 struct MixedArgs {
     draft::DraftArgs d;
@@ -36,18 +33,13 @@ struct MixedArgs {
 
 template <int BITS, int D>
 struct MCfg {
-    // quantised: the tcgen05 draft body (either head-slot width); bf16: the
-    // mma.sync body
-    static constexpr int B = BITS == 16 ? 2 : BITS;
-    static constexpr int T4 = dtc::Cfg<B, D, 4>::SMEM, T8 = dtc::Cfg<B, D, 8>::SMEM;
-    static constexpr int DS = BITS != 16 ? (T4 > T8 ? T4 : T8) : draft::Cfg<BITS, D, kDraftWarps>::SMEM;
+    static constexpr int DS = draft::Cfg<BITS, D, kDraftWarps>::SMEM;
     static constexpr int VS = vtc::Cfg<D, 1>::SMEM;
     static constexpr int SMEM = DS > VS ? DS : VS;
 };
-static_assert(dtc::Cfg<2, 128, 4>::THREADS == kThreads, "the draft body takes the whole block");
 
 template <int BITS, int D>
-__global__ void __launch_bounds__(kThreads, 2) mixed_kernel(const __grid_constant__ MixedArgs m) {
+__global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ MixedArgs m) {
     pdl_begin();
     extern __shared__ __align__(1024) uint8_t smem[];
     int bid = blockIdx.x;
@@ -63,14 +55,7 @@ __global__ void __launch_bounds__(kThreads, 2) mixed_kernel(const __grid_constan
         const int rest = bid / m.d.n_splits;
         const int kvh = rest % m.d.hkv, b = rest / m.d.hkv;
         if (m.role[b] != 0) return;
-        if constexpr (BITS != 16) {
-            if (m.d.grp <= 4)
-                dtc::draft_tc_block<BITS, D, 4>(m.d, split, kvh, b, m.d.chunk_pages, smem);
-            else
-                dtc::draft_tc_block<BITS, D, 8>(m.d, split, kvh, b, m.d.chunk_pages, smem);
-        } else {
-            draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, m.d.chunk_pages, smem);
-        }
+        draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, m.d.chunk_pages, smem);
     }
 }
 
@@ -104,22 +89,20 @@ int sms() {
 // the whole batch, and at most 258 pages (43 per warp) per block, so that
 // requests of very different lengths (blocks past a request's end exit at
 // once, as do blocks of verifying requests) still spread evenly over the SMs.
-// (Quantised formats: chunks of whole 8-page tiles of the tcgen05 body.)
-void draft_plan(int bits, int batch, int hkv, int max_seq_len, int &chunk, int &splits) {
+void draft_plan(int batch, int hkv, int max_seq_len, int &chunk, int &splits) {
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
-    const int gran = bits != 16 ? dtc::Cfg<2, 128, 4>::TP : kDraftWarps;
     int s = (int)((2LL * sms() + units - 1) / units);
     s = max(s, ceil_div(max_pages, 43 * kDraftWarps));
-    s = max(1, min(s, ceil_div(max_pages, gran)));
+    s = max(1, min(s, ceil_div(max_pages, kDraftWarps)));
     chunk = ceil_div(max_pages, s);
-    chunk = max(gran, ceil_div(chunk, gran) * gran);
+    chunk = max(kDraftWarps, ceil_div(chunk, kDraftWarps) * kDraftWarps);
     splits = max(1, ceil_div(max_pages, chunk));
 }
 
 size_t draft_part(const vc_paged_kv &comp, int hq, int max_seq_len) {
     int chunk, splits;
-    draft_plan(comp.fmt.bits, comp.batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
+    draft_plan(comp.batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
     return (size_t)comp.batch * hq * splits * (comp.fmt.head_dim + 2) * sizeof(float);
 }
 
@@ -155,7 +138,7 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
     MixedArgs m;
     const int d = comp.fmt.head_dim, bits = comp.fmt.bits, batch = comp.batch;
     int chunk, splits;
-    draft_plan(bits, batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
+    draft_plan(batch, comp.fmt.num_kv_heads, max_seq_len, chunk, splits);
     m.d.q = (const uint16_t *)q_draft;
     m.d.kp = (const uint8_t *)comp.k_pages;
     m.d.vp = (const uint8_t *)comp.v_pages;

@@ -131,7 +131,7 @@ __device__ void append_entry(const uint8_t *k_row, const uint8_t *v_row, uint8_t
             }
             if (lane % LPG == 0) {
                 const int gr = lane / LPG;
-                const int e = kv ? layout::v_param(BITS, G, slot, gr) : slot * G + gr;
+                const int e = kv ? layout::v_param(G, slot, gr) : slot * G + gr;
                 uint16_t *par = reinterpret_cast<uint16_t *>((kv ? gv : gk) + CR);
                 par[e] = sh;
                 par[kPage * G + e] = zh;

@@ -150,15 +150,22 @@ def _header_k_bit(bits, d, s, c, plane):
 
 
 def _header_v_bit(bits, d, s, c, plane):
+    g, w, m = c % 8, (c // 8) % 2, c // 16
+    t, hi, h = (s // 2) % 4, s // 8, s % 2
+    R = 4 * g + t
     if bits == 4:
-        return 32 * (2 * c + s // 8) + 16 * (s % 2) + 4 * ((s % 8) // 2)
+        return 32 * (R * d // 16 + m) + 16 * h + 8 * w + 4 * hi
+    u, n = m // 2, m % 2
     if bits == 2 or plane == 0:
-        return 32 * c + 16 * (s % 2) + 2 * (s // 2)
-    return 32 * d + 32 * (c // 2) + 16 * (s % 2) + 2 * (s // 2) + c % 2
+        return 32 * (R * d // 32 + u) + 16 * h + 8 * n + 4 * w + 2 * hi
+    j = 2 * w + hi
+    return 32 * d + 32 * (R * d // 64 + u // 2) + 16 * h + 2 * j + [0, 1, 8, 9][2 * (u % 2) + n]
 
 
 def _header_param(kind, g, s, gr, bits):
-    return s * g + gr
+    if kind == "k":
+        return s * g + gr
+    return (((s // 2) % 4) * g + gr) * 4 + 2 * (s // 8) + (s % 2)
 
 
 @pytest.mark.parametrize("bits,d", [(2, 64), (2, 128), (3, 64), (3, 128), (3, 256), (4, 64), (4, 128)])

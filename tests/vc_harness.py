@@ -75,20 +75,23 @@ def k_bit(bits: int, d: int, s, c, plane: int = 0):
 
 
 def v_bit(bits: int, d: int, tau, c, plane: int = 0):
-    """Channel-major V placement: bits 2 one word per channel (token tau at
-    16 (tau % 2) + 2 (tau // 2)); bits 3 the same for the low two bits plus a
-    high-bit word per channel pair (+ c % 2); bits 4 two words per channel."""
     tau, c = np.asarray(tau), np.asarray(c)
+    g, row8, mt = c & 7, (c >> 3) & 1, c >> 4
+    t, hi, half = (tau >> 1) & 3, tau >> 3, tau & 1
+    region = g * 4 + t
     if bits == 4:
-        return 32 * (2 * c + (tau >> 3)) + 16 * (tau & 1) + 4 * ((tau & 7) >> 1)
+        return 32 * (region * (d // 16) + mt) + 16 * half + 8 * row8 + 4 * hi
+    u, m = mt >> 1, mt & 1
     if bits == 2 or plane == 0:
-        return 32 * c + 16 * (tau & 1) + 2 * (tau >> 1)
-    return 32 * d + 32 * (c >> 1) + 16 * (tau & 1) + 2 * (tau >> 1) + (c & 1)
+        return 32 * (region * (d // 32) + u) + 16 * half + 8 * m + 4 * row8 + 2 * hi
+    j = 2 * row8 + hi
+    beta = 2 * j + np.array([0, 1, 8, 9])[2 * (u & 1) + m]
+    return 32 * d + 32 * (region * (d // 64) + (u >> 1)) + 16 * half + beta
 
 
-def v_param(g: int, tau, gr, bits: int = 3):
+def v_param(g: int, tau, gr):
     tau, gr = np.asarray(tau), np.asarray(gr)
-    return tau * g + gr
+    return (((tau >> 1) & 3) * g + gr) * 4 + 2 * (tau >> 3) + (tau & 1)
 
 
 def _bits_at(region: np.ndarray, off: np.ndarray, width: int) -> np.ndarray:
@@ -139,7 +142,7 @@ def read_comp(pool: torch.Tensor, table_row: np.ndarray, n: int, hkv: int, d: in
     if kind == "k":
         sc, ze = par[:, 0].reshape(npg * hkv, PAGE, ng), par[:, 1].reshape(npg * hkv, PAGE, ng)
     else:
-        idx = v_param(ng, np.arange(PAGE)[:, None], np.arange(ng)[None, :], bits)
+        idx = v_param(ng, np.arange(PAGE)[:, None], np.arange(ng)[None, :])
         sc, ze = par[:, 0][:, idx], par[:, 1][:, idx]
     sc = sc.reshape(npg, hkv, PAGE, ng).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
     ze = ze.reshape(npg, hkv, PAGE, ng).transpose(0, 2, 1, 3).reshape(npg * PAGE, hkv, ng)
