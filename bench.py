@@ -22,6 +22,12 @@ the queries are copied from pinned host memory, KV_full (the page's
 "full KV in CPU memory") is staged host->device on a side stream while the
 drafting runs, and the verified / emitted tokens are copied back.
 
+other_workloads: after the headline's timed region, rank 0 times the other
+workloads of the path on the device (CUDA events): the 70B-shaped layer
+(draft over bf16 token-drop KV_comp, 40-query verify over a 131072-token
+KV_full, GPU token selection) with the 40k-context verify point, and one
+staggered mixed launch of the 32-request 3-bit workload.
+
 --impl reference: the CPU oracle on this machine's cores, a bounded sample
 of the same workload per step (draft attention of one request).
 Multi-GPU (torchrun): independent replicas, weak scaling, no data-path
@@ -397,6 +403,8 @@ def main():
     ap.add_argument("--impl", default="vc", choices=["vc", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads' device timings (70B-shaped layer, 40k verify, mixed launch)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "mixed_32req_3bit", "toy_e2e", "staging", "70b_128k_drop4",
                              "stagger_32req_3bit", "remote_prefix_8req_3bit", "verify_40k"])
@@ -477,6 +485,12 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_sample(w, st)
+    extras = None
+    if rank == 0 and not args.no_extras:
+        # the other workloads of the path, timed on the device (CUDA events
+        # around graph replays / launches), after the headline's timed region
+        extras = {"70b_128k_drop4": big_measure(),
+                  "mixed_32req_3bit": mixed_measure(args.steps, args.warmup, staging=False)}
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "draft_attn_traffic.txt")) as f:
@@ -497,7 +511,7 @@ def main():
                              "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                              "kernel": "draft_kernel<2,128> (incl. the step's append) + draft_reduce_kernel"},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": rnd.launches * args.steps,
-                "clocks": clk.summary()}
+                "clocks": clk.summary(), "other_workloads": extras}
         print(json.dumps(line), flush=True)
 
 
@@ -656,6 +670,11 @@ def big_main(args):
     draft call over KV_comp and the 40-query verify over KV_full, plus the
     40k-context verify point (batch 8, 32q/8kv, context 40960, 40 queries).
     Each call is captured in a CUDA graph and timed over replays."""
+    print(json.dumps(big_measure()), flush=True)
+
+
+def big_measure():
+    """The measurements of big_main as one JSON-ready dict."""
     import torch
     import synth
     import lossless_compressed_kv_gb300 as vc
@@ -720,7 +739,7 @@ def big_main(args):
     v40 = _verify_40k(vc, torch, g, device, d, hkv, peak, tpeak, 10)
     torch.cuda.synchronize()
     assert status.item() == 0, "device status %d" % status.item()
-    print(json.dumps({
+    return {
         "metric": "70B-shaped layer: draft over bf16 token-drop KV_comp and 40-query verify; 40k-context verify",
         "workload": "70b_128k_drop4",
         "config": {"batch": B, "q_heads": hq, "kv_heads": hkv, "head_dim": d, "ctx": N, "kept": nk, "x": x},
@@ -736,7 +755,7 @@ def big_main(args):
                    "frac_bf16_measured": ver_flops / t_ver / 1e6 / tpeak},
         "verify_40k": v40,
         "timing": "CUDA events around replays of a CUDA graph of the call; flops count the causal block as full",
-    }), flush=True)
+    }
 
 
 def staging_main(args):
@@ -763,6 +782,10 @@ def staging_main(args):
 
 
 def mixed_main(args):
+    print(json.dumps(mixed_measure(args.steps, args.warmup, staging=True)), flush=True)
+
+
+def mixed_measure(steps, warmup, staging):
     """Staggered mixed batch: 32 requests, contexts U[8192, 65536], 32q/8kv,
     D 128, 3-bit KV_comp; even requests draft, odd ones verify x = 25 in one
     launch, while the NEXT round's verifying requests' KV_full (odd requests
@@ -813,13 +836,14 @@ def mixed_main(args):
     # staging: the verifying requests' KV_full for the next round, pinned host -> device
     ver_pages = sum(npg[b] for b in range(B) if role[b] == 1)
     stage_bytes = ver_pages * pb
-    hk = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
-    hv = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
-    hk.fill_(0)
-    hv.fill_(0)
-    sk = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
-    sv = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
-    side = torch.cuda.Stream()
+    if staging:
+        hk = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
+        hv = torch.empty(stage_bytes, dtype=torch.uint8, pin_memory=True)
+        hk.fill_(0)
+        hv.fill_(0)
+        sk = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+        sv = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
+        side = torch.cuda.Stream()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def mixed():
@@ -840,21 +864,23 @@ def mixed_main(args):
         torch.cuda.synchronize()
         return ev[0].elapsed_time(ev[1]) / n
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         mixed()
-    t_mixed = timed(mixed, args.steps)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        stage()
-    torch.cuda.synchronize()
-    t_stage = (time.perf_counter() - t0) * 1e3 / args.steps
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        stage()
-        mixed()
-    torch.cuda.synchronize()
-    t_wall = (time.perf_counter() - t0) * 1e3 / args.steps
+    t_mixed = timed(mixed, max(steps, 3))
+    t_stage = t_wall = None
+    if staging:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            stage()
+        torch.cuda.synchronize()
+        t_stage = (time.perf_counter() - t0) * 1e3 / steps
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            stage()
+            mixed()
+        torch.cuda.synchronize()
+        t_wall = (time.perf_counter() - t0) * 1e3 / steps
     assert status.item() == 0
     nd = int((role == 0).sum())
     nv = int((role == 1).sum())
@@ -865,12 +891,14 @@ def mixed_main(args):
             "config": {"batch": B, "ctx": "U[%d,%d]" % (w["ctx_lo"], w["ctx_hi"]), "q_heads": hq, "kv_heads": hkv,
                        "head_dim": d, "bits": bits, "x": x, "drafting": nd, "verifying": nv},
             "ms_mixed_launch": t_mixed, "ms_stage": t_stage, "ms_wall_stage_and_mixed": t_wall,
-            "overlap_efficiency": (t_mixed + t_stage) / t_wall,
+            "overlap_efficiency": (t_mixed + t_stage) / t_wall if staging else None,
             "draft_tokens_per_s": nd / (t_mixed * 1e-3), "verify_tokens_per_s": nv * x / (t_mixed * 1e-3),
             "algorithmic_GBps": (comp_bytes + full_bytes) / (t_mixed * 1e-3) / 1e9,
-            "verify_tflops": flops / (t_mixed * 1e-3) / 1e12, "stage_GBps": 2 * stage_bytes / (t_stage * 1e-3) / 1e9,
-            "stage_bytes": 2 * stage_bytes}
-    print(json.dumps(line), flush=True)
+            "verify_tflops": flops / (t_mixed * 1e-3) / 1e12,
+            "stage_GBps": 2 * stage_bytes / (t_stage * 1e-3) / 1e9 if staging else None,
+            "stage_bytes": 2 * stage_bytes,
+            "timing": "CUDA events around %d mixed launches" % max(steps, 3)}
+    return line
 
 
 def stagger_main(args):
