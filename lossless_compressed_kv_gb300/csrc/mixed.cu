@@ -5,10 +5,12 @@
 // all requests drafting and then all verifying, some requests verify against
 // their full cache while the others keep drafting from the compressed one.
 // Drafting is HBM-bandwidth bound, verification brings dense tensor work, so
-// one grid holding both keeps both busy.  Blocks [0, Nv) run the
-// verification body for requests with role 1, blocks [Nv, Nv + Nd) the
-// draft body (6 warps) for requests with role 0; a block whose request has
-// the other role exits at once.  One combine launch finishes both.
+// one grid holding both keeps both busy.  The first blocks run the
+// verification body for the items of the requests with role 1, the next
+// ones the draft body (6 warps) for the items of the requests with role 0,
+// both over each request's own length (the grid is sized for the longest
+// request and the worst split of roles; blocks past the two lists exit).
+// One combine launch finishes both.
 #include "draft_impl.cuh"
 #include "verify_tc.cuh"
 
@@ -28,7 +30,7 @@ struct MixedArgs {
     draft::DraftArgs d;
     vtc::Args v;
     const int32_t *role;
-    int n_verify_blocks, rb;
+    int n_verify_blocks, rb, batch;
 };
 
 template <int BITS, int D>
@@ -38,24 +40,75 @@ struct MCfg {
     static constexpr int SMEM = DS > VS ? DS : VS;
 };
 
+// Splits of request b's verification (fixed 3648-key pieces of its length;
+// one for a request shorter than its block, whose single block reports the
+// error and writes zeros) and chunks of its KV_comp (0 for an empty one).
+__device__ inline int verify_splits_of(const MixedArgs &m, int b) {
+    const int len = m.v.lens[b];
+    return len >= m.v.n_q ? ceil_div(ceil_div(len, kPage), vtc::kSplitPages) : 1;
+}
+__device__ inline int draft_chunks_of(const MixedArgs &m, int b) {
+    return ceil_div(ceil_div(max(m.d.lens[b], 0), kPage), m.d.chunk_pages);
+}
+__device__ inline int verify_items(const MixedArgs &m, int b) { return m.v.hkv * m.rb * verify_splits_of(m, b); }
+__device__ inline int draft_items(const MixedArgs &m, int b) { return m.d.hkv * draft_chunks_of(m, b); }
+
 template <int BITS, int D>
 __global__ void __launch_bounds__(kThreads) mixed_kernel(const __grid_constant__ MixedArgs m) {
     pdl_begin();
     extern __shared__ __align__(1024) uint8_t smem[];
-    int bid = blockIdx.x;
-    if (bid < m.n_verify_blocks) {
-        const int split = bid % m.v.n_splits;
-        const int rest = bid / m.v.n_splits;
-        const int rb = rest % m.rb, bk = rest / m.rb;
-        if (m.role[bk / m.v.hkv] != 1) return;
-        vtc::verify_tc_cta<D, 1>(m.v, split, rb, bk, smem);
-    } else {
-        bid -= m.n_verify_blocks;
-        const int split = bid % m.d.n_splits;
-        const int rest = bid / m.d.n_splits;
-        const int kvh = rest % m.d.hkv, b = rest / m.d.hkv;
-        if (m.role[b] != 0) return;
-        draft::draft_block<BITS, D, kDraftWarps>(m.d, split, kvh, b, m.d.chunk_pages, smem);
+    // The grid's blocks cover, in this order, the verification items of the
+    // requests with role 1 (kv head x row block x split over the request's
+    // own length), then the draft items of the requests with role 0 (kv
+    // head x chunk over its own KV_comp length); blocks past both lists
+    // exit.  Each block finds its item from the roles and lengths, so no
+    // block is spent on a request of the other role or past a request's end.
+    __shared__ int item[4];  // kind (1 verify, 2 draft, 0 none), request, index within the request
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int k = blockIdx.x, kind = 0, req = 0, local = 0;
+        for (int pass = 1; pass <= 2 && kind == 0; ++pass) {
+            int base = 0;
+            for (int b0 = 0; b0 < m.batch; b0 += 32) {
+                const int b = b0 + lane;
+                int cnt = 0;
+                if (b < m.batch && m.role[b] == (pass == 1 ? 1 : 0))
+                    cnt = pass == 1 ? verify_items(m, b) : draft_items(m, b);
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int excl = incl - cnt;
+                const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && k >= base + excl && k < base + incl);
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    kind = pass;
+                    req = b0 + src;
+                    local = k - base - __shfl_sync(0xffffffffu, excl, src);
+                    break;
+                }
+                base += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (kind == 0) k -= base;  // the draft items follow the verification items
+        }
+        if (lane == 0) {
+            item[0] = kind;
+            item[1] = req;
+            item[2] = local;
+        }
+    }
+    __syncthreads();
+    const int kind = item[0], b = item[1], local = item[2];
+    if (kind == 1) {
+        const int ns = verify_splits_of(m, b);
+        const int split = local % ns, rest = local / ns;
+        const int rb = rest % m.rb, kvh = rest / m.rb;
+        vtc::verify_tc_cta<D, 1>(m.v, split, rb, b * m.v.hkv + kvh, smem);
+    } else if (kind == 2) {
+        const int nc = draft_chunks_of(m, b);
+        draft::draft_block<BITS, D, kDraftWarps>(m.d, local % nc, local / nc, b, m.d.chunk_pages, smem);
     }
 }
 
@@ -64,13 +117,16 @@ __global__ void mixed_reduce_kernel(MixedArgs m, float *out_draft, float *out_ve
     pdl_begin();
     const int row = blockIdx.x;
     if (row < draft_rows) {  // row = b * Hq + h
-        if (m.role[row / m.d.hq] != 0) return;
-        draft::reduce_row<D>(m.d.ws_o, m.d.ws_ml, m.d.n_splits, m.d.n_splits, row, out_draft, threadIdx.x,
-                             blockDim.x);
+        const int b = row / m.d.hq;
+        if (m.role[b] != 0) return;
+        combine_partials<D>(m.d.ws_o, m.d.ws_ml, m.d.n_splits, draft_chunks_of(m, b), row, out_draft, threadIdx.x,
+                            blockDim.x);
     } else {  // ((b * n_q + i) * Hq + h)
         const int r = row - draft_rows;
-        if (m.role[r / (m.v.n_q * m.v.hq)] != 1) return;
-        vtc::reduce_row<D>(m.v.ws_o, m.v.ws_ml, m.v.n_splits, r, out_verify, threadIdx.x, blockDim.x);
+        const int b = r / (m.v.n_q * m.v.hq);
+        if (m.role[b] != 1) return;
+        combine_partials<D>(m.v.ws_o, m.v.ws_ml, m.v.n_splits, verify_splits_of(m, b), r, out_verify, threadIdx.x,
+                            blockDim.x);
     }
 }
 
@@ -160,6 +216,7 @@ cudaError_t mixed_launch(const int32_t *role, const void *q_draft, const vc_page
     void *vws = (uint8_t *)ws + draft_part(comp, hq, max_seq_len);
     if (!verify_args(m.v, q_verify, n_q, hq, full, scale, max_seq_len, vws, status)) return cudaErrorInvalidValue;
     m.role = role;
+    m.batch = batch;
     m.rb = ceil_div(n_q * m.v.grp, vtc::kTileRows);
     m.n_verify_blocks = m.v.n_splits * m.rb * batch * m.v.hkv;
 #define VC_L(B_, D_) launch<B_, D_>(m, batch, out_draft, out_verify, st)
