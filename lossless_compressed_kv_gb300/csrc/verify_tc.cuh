@@ -95,7 +95,10 @@ struct Cfg {
     static_assert(STAGES >= 2, "K/V ring needs two stages");
     static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * KTILE;
     static constexpr int NBAR = QT * 6 + 2 * STAGES;  // s_ready, p_ready, pv_done ([QT][2] each), full, empty
-    static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+    // page ids of the split (read once at set-up, so that the producer
+    // issues a block's copies without waiting on table loads)
+    static constexpr int OFF_PID = OFF_BAR + NBAR * 8 + 16;
+    static constexpr int SMEM = OFF_PID + kSplitPages * 4 + 1024;
     static constexpr int TMEM_USED = QT * SB * BK + QT * D + (QTM ? QT * D / 2 : 0);
     static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= TMEM_LIMIT, "S, O (and Q) columns exceed TMEM");
@@ -271,6 +274,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     uint64_t *full = bars + QT * 6;       // [STAGES]
     uint64_t *empty = full + C::STAGES;   // [STAGES]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + C::NBAR);
+    int32_t *spid = reinterpret_cast<int32_t *>(smem + C::OFF_PID);  // [nb * BK / 16] page ids
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp == QT * 4;
@@ -291,7 +295,23 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     const int nt = FULL ? QT : min(QT, ceil_div(max(0, min(a.rows_per_cta, nrows - rb * a.rows_per_cta)), kTileRows));
     const int32_t *trow = a.table + (int64_t)b * a.maxb;
 
-    // ---- set-up: barriers, TMEM, Q tiles ----
+    // ---- set-up: barriers, TMEM, page ids, Q tiles ----
+    // Page ids of the split's blocks, checked once (pages past the request's
+    // end within its last block: any valid page, masked / zeroed later).
+    // One dependent table load per page inside the producer loop would cap
+    // the copy issue rate at a block per few table-load latencies.
+    for (int i = tid; i < nb * (C::BK / kPage); i += C::THREADS) {
+        const int pidx = p0 + i;
+        int id = 0;
+        if (pidx < npages) {
+            id = pidx < a.maxb ? trow[pidx] : -1;
+            if (id < 0 || id >= a.n_pages) {
+                report(a.status, VC_ERR_BAD_INDEX);
+                id = 0;
+            }
+        }
+        spid[i] = id;
+    }
     if (tid == 0) {
         for (int i = 0; i < QT * 2; ++i) {
             mbar_init(&s_ready[i], 1);
@@ -373,17 +393,9 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 if (!alive) break;
                 uint8_t *kt = skv + st * 2 * C::KTILE;
                 mbar_arrive_expect_tx(&full[st], 2 * C::KTILE);
+#pragma unroll
                 for (int pg = 0; pg < C::BK / kPage; ++pg) {
-                    const int pidx = p0 + j * (C::BK / kPage) + pg;
-                    int id = 0;
-                    if (pidx < npages) {  // pages past the request's end: any valid page (masked / zeroed)
-                        id = pidx < a.maxb ? trow[pidx] : -1;
-                        if (id < 0 || id >= a.n_pages) {
-                            report(a.status, VC_ERR_BAD_INDEX);
-                            id = 0;
-                        }
-                    }
-                    const int y = (id * a.hkv + kvh) * kPage;
+                    const int y = (spid[j * (C::BK / kPage) + pg] * a.hkv + kvh) * kPage;
 #pragma unroll
                     for (int c = 0; c < C::NC; ++c) {
                         tma2d(kt + c * (C::BK * 128) + pg * (kPage * 128), &a.kmap, c * 64, y, &full[st]);
