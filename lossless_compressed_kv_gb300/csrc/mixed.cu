@@ -7,10 +7,16 @@
 // Drafting is HBM-bandwidth bound, verification brings dense tensor work, so
 // one grid holding both keeps both busy.  The first blocks run the
 // verification body for the items of the requests with role 1, the next
-// ones the draft body (6 warps) for the items of the requests with role 0,
+// ones the draft body (8 warps) for the items of the requests with role 0,
 // both over each request's own length (the grid is sized for the longest
 // request and the worst split of roles; blocks past the two lists exit).
-// One combine launch finishes both.
+// One combine launch finishes both.  Blocks have 8 warps: the draft body
+// uses all of them (16 draft warps per SM at two blocks per SM, as many as
+// the standalone draft kernel keeps), the verification body 6 (the other two
+// only join its CTA barriers).  Measured on the 32-request 3-bit workload
+// against 6-warp blocks: the launch 871 -> 768 us, its drafting half alone
+// 428 -> 329 us.  Interleaving verification and draft blocks in the grid
+// (so that an SM holds one of each) was tried and not kept (766 us).
 #include "draft_impl.cuh"
 #include "verify_tc.cuh"
 
@@ -22,8 +28,10 @@ bool verify_args(vtc::Args &a, const void *q, int n_q, int hq, const vc_paged_kv
 namespace {
 
 // the verification body of one 128-row tile needs 4 softmax warps, a
-// producer warp and an MMA warp; draft blocks use the same 6 warps
-constexpr int kThreads = vtc::Cfg<128, 1>::THREADS;
+// producer warp and an MMA warp; draft blocks use all 8
+constexpr int kThreads = 256;
+static_assert(kThreads >= vtc::Cfg<128, 1>::THREADS && kThreads >= vtc::Cfg<64, 1>::THREADS,
+              "the verification body's roles fit in a block");
 constexpr int kDraftWarps = kThreads / 32;
 
 struct MixedArgs {
@@ -142,7 +150,7 @@ int sms() {
 }
 
 // Draft chunking of the mixed launch: at least two draft blocks per SM over
-// the whole batch, and at most 258 pages (43 per warp) per block, so that
+// the whole batch, and at most 43 pages per warp (344 per block), so that
 // requests of very different lengths (blocks past a request's end exit at
 // once, as do blocks of verifying requests) still spread evenly over the SMs.
 void draft_plan(int batch, int hkv, int max_seq_len, int &chunk, int &splits) {

@@ -300,7 +300,7 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
     // end within its last block: any valid page, masked / zeroed later).
     // One dependent table load per page inside the producer loop would cap
     // the copy issue rate at a block per few table-load latencies.
-    for (int i = tid; i < nb * (C::BK / kPage); i += C::THREADS) {
+    for (int i = tid; i < nb * (C::BK / kPage) && tid < C::THREADS; i += C::THREADS) {
         const int pidx = p0 + i;
         int id = 0;
         if (pidx < npages) {
@@ -330,36 +330,56 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                      "r"(C::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    if constexpr (!C::QTM) {
-        for (int e = tid; e < QT * kTileRows * (D / 8); e += C::THREADS) {
-            const int r = e / (D / 8), c = e % (D / 8);     // r: row within the CTA, c: 16-byte chunk
-            const int rg = rb * a.rows_per_cta + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (rg < nrows) {
-                const int i = rg / a.grp, n = rg % a.grp;
-                v = *reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) *
-                                                               D +
-                                                     c * 8);
-            }
-            *reinterpret_cast<uint4 *>(sq + (r >> 7) * C::QTILE + sw128(r & 127, c, kTileRows)) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if constexpr (C::QTM) {
-        // each softmax thread writes its own row (= TMEM lane) of its tile's
-        // Q as bf16 pairs (element 2c in the low half of column c)
-        if (warp < QT * 4) {
+    // The producer starts its copies now; the other warps stage the Q tiles
+    // meanwhile (every load issued before any store) and meet at their own
+    // barrier, so the first blocks' copy latency overlaps the Q loads.
+    // (a launch with more threads than the roles need -- the mixed grid --
+    // leaves the extra warps out of the staging and its barrier)
+    if (!producer && warp < C::THREADS / 32) {
+        if constexpr (!C::QTM) {
+            constexpr int QE = QT * kTileRows * (D / 8);  // 16-byte chunks of the CTA's Q tiles
+            constexpr int NQ = C::THREADS - 32;           // every thread but the producer warp's
+            constexpr int QPT = (QE + NQ - 1) / NQ;
+            const int qi = tid < QT * 128 ? tid : tid - 32;
+            uint4 v[QPT];
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                const int e = qi + u * NQ;
+                const int r = e / (D / 8), c = e % (D / 8);  // r: row within the CTA, c: 16-byte chunk
+                const int rg = rb * a.rows_per_cta + r;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (e < QE && rg < nrows) {
+                    const int i = rg / a.grp, n = rg % a.grp;
+                    v[u] = *reinterpret_cast<const uint4 *>(
+                        a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D + c * 8);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                const int e = qi + u * NQ;
+                const int r = e / (D / 8), c = e % (D / 8);
+                if (e < QE) *reinterpret_cast<uint4 *>(sq + (r >> 7) * C::QTILE + sw128(r & 127, c, kTileRows)) = v[u];
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else if (warp < QT * 4) {
+            // each softmax thread writes its own row (= TMEM lane) of its
+            // tile's Q as bf16 pairs (element 2c in the low half of column c)
             const int qt = warp >> 2;
             const int r = (warp & 3) * 32 + lane;
             const int rg = rb * a.rows_per_cta + qt * kTileRows + r;
-            const uint4 *src = nullptr;
+            uint4 u[D / 8];
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) u[j] = make_uint4(0, 0, 0, 0);
             if (rg < nrows) {
                 const int i = rg / a.grp, n = rg % a.grp;
-                src = reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D);
+                const uint4 *src =
+                    reinterpret_cast<const uint4 *>(a.q + (((int64_t)b * a.n_q + i) * a.hq + kvh * a.grp + n) * D);
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) u[j] = src[j];
             }
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll
@@ -367,17 +387,16 @@ __device__ __forceinline__ void verify_tc_block(const Args &a, int split, int rb
                 float v[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint4 u = src ? src[c0 / 4 + j] : make_uint4(0, 0, 0, 0);
-                    v[4 * j] = __uint_as_float(u.x);
-                    v[4 * j + 1] = __uint_as_float(u.y);
-                    v[4 * j + 2] = __uint_as_float(u.z);
-                    v[4 * j + 3] = __uint_as_float(u.w);
+                    v[4 * j] = __uint_as_float(u[c0 / 4 + j].x);
+                    v[4 * j + 1] = __uint_as_float(u[c0 / 4 + j].y);
+                    v[4 * j + 2] = __uint_as_float(u[c0 / 4 + j].z);
+                    v[4 * j + 3] = __uint_as_float(u[c0 / 4 + j].w);
                 }
                 tmem_st16(tmem + lane_base + C::Q_COL(qt) + c0, v);
             }
         }
         tc_fence_before();
-        __syncthreads();
+        asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS - 32) : "memory");
         tc_fence_after();
     }
     bool alive = true;
