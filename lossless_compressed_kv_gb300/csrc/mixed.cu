@@ -150,14 +150,16 @@ int sms() {
 }
 
 // Draft chunking of the mixed launch: at least two draft blocks per SM over
-// the whole batch, and at most 43 pages per warp (344 per block), so that
+// the whole batch, and at most 64 pages per warp (512 per block), so that
 // requests of very different lengths (blocks past a request's end exit at
 // once, as do blocks of verifying requests) still spread evenly over the SMs.
+// (Caps of 24 / 32 / 43 / 64 / 96 / 128 pages per warp measured 808 / 783 /
+// 770 / 755 / 755 / 770 us on the 32-request 3-bit workload.)
 void draft_plan(int batch, int hkv, int max_seq_len, int &chunk, int &splits) {
     const int max_pages = ceil_div(max_seq_len, kPage);
     const int64_t units = (int64_t)batch * hkv;
     int s = (int)((2LL * sms() + units - 1) / units);
-    s = max(s, ceil_div(max_pages, 43 * kDraftWarps));
+    s = max(s, ceil_div(max_pages, 64 * kDraftWarps));
     s = max(1, min(s, ceil_div(max_pages, kDraftWarps)));
     chunk = ceil_div(max_pages, s);
     chunk = max(kDraftWarps, ceil_div(chunk, kDraftWarps) * kDraftWarps);
