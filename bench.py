@@ -790,8 +790,9 @@ def mixed_measure(steps, warmup, staging):
     D 128, 3-bit KV_comp; even requests draft, odd ones verify x = 25 in one
     launch, while the NEXT round's verifying requests' KV_full (odd requests
     of the other parity set) is staged from pinned host memory on a side
-    stream.  Reports tokens/s of both halves, the staging bandwidth and the
-    overlap efficiency (t_mixed + t_stage) / t_wall."""
+    stream.  Reports tokens/s of both halves, each half timed alone in the
+    same launch (the other role's requests idle), the staging bandwidth and
+    the overlap efficiency (t_mixed + t_stage) / t_wall."""
     import torch
     import synth
     import lossless_compressed_kv_gb300 as vc
@@ -867,6 +868,12 @@ def mixed_measure(steps, warmup, staging):
     for _ in range(max(3, warmup)):
         mixed()
     t_mixed = timed(mixed, max(steps, 3))
+    # each half alone in the same launch (the other role's requests idle)
+    halves = {}
+    for name, keep in (("draft", 0), ("verify", 1)):
+        rh = torch.from_numpy(np.where(role == keep, role, 2).astype(np.int32)).to(dev)
+        halves[name] = timed(lambda: vc.mixed_attn(rh, qd, comp, od, qv, full, ov, 1.0 / math.sqrt(d), msl, wsb,
+                                                   status=status), max(steps, 3))
     t_stage = t_wall = None
     if staging:
         t0 = time.perf_counter()
@@ -894,6 +901,9 @@ def mixed_measure(steps, warmup, staging):
             "overlap_efficiency": (t_mixed + t_stage) / t_wall if staging else None,
             "draft_tokens_per_s": nd / (t_mixed * 1e-3), "verify_tokens_per_s": nv * x / (t_mixed * 1e-3),
             "algorithmic_GBps": (comp_bytes + full_bytes) / (t_mixed * 1e-3) / 1e9,
+            "ms_draft_half_alone": halves["draft"], "draft_half_GBps": comp_bytes / (halves["draft"] * 1e-3) / 1e9,
+            "ms_verify_half_alone": halves["verify"],
+            "verify_half_GBps": full_bytes / (halves["verify"] * 1e-3) / 1e9,
             "verify_tflops": flops / (t_mixed * 1e-3) / 1e12,
             "stage_GBps": 2 * stage_bytes / (t_stage * 1e-3) / 1e9 if staging else None,
             "stage_bytes": 2 * stage_bytes,
