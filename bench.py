@@ -25,8 +25,9 @@ drafting runs, and the verified / emitted tokens are copied back.
 other_workloads: after the headline's timed region, rank 0 times the other
 workloads of the path on the device (CUDA events): the 70B-shaped layer
 (draft over bf16 token-drop KV_comp, 40-query verify over a 131072-token
-KV_full, GPU token selection) with the 40k-context verify point, and one
-staggered mixed launch of the 32-request 3-bit workload.
+KV_full, GPU token selection) with the 40k-context verify point, one
+staggered mixed launch of the 32-request 3-bit workload, and the headline's
+draft step at 3 and 4 bits.
 
 --impl reference: the CPU oracle on this machine's cores, a bounded sample
 of the same workload per step (draft attention of one request).
@@ -299,6 +300,28 @@ def draft_bytes(w, n_entries):
     return w["batch"] * n_entries * hkv * per_tok_head
 
 
+def bits_measure(w, device, bit_widths=(3, 4)):
+    """The draft step (vc_draft_step: append + draft + reduce) of the
+    headline workload's shape at other code widths: per call device time
+    over graph replays of the x calls of a round, algorithmic bytes and the
+    fraction of the measured HBM rate."""
+    import torch
+    peak, _ = peaks()
+    out = {}
+    for bits in bit_widths:
+        w2 = dict(w, bits=bits)
+        st2 = build(w2, 1234, device)
+        rnd2 = Round(w2, st2, device)
+        calls = rnd2.stage_calls()["draft_step"]
+        us = _graph_us(torch, lambda: [c() for c in calls], 5) / len(calls)
+        nb = float(np.mean([draft_bytes(w2, w2["ctx"] + i + 1) for i in range(len(calls))]))
+        out["%d_bit" % bits] = {"us_per_call": us, "bytes_per_call": nb, "GBps": nb / us / 1e3,
+                                "frac_hbm_measured": nb / us / 1e3 / peak}
+        del st2, rnd2
+        torch.cuda.empty_cache()
+    return out
+
+
 def headline_config(w):
     """The `config` object of the headline line, the same for both arms."""
     N, x = w["ctx"], w["x"]
@@ -490,7 +513,8 @@ def main():
         # the other workloads of the path, timed on the device (CUDA events
         # around graph replays / launches), after the headline's timed region
         extras = {"70b_128k_drop4": big_measure(),
-                  "mixed_32req_3bit": mixed_measure(args.steps, args.warmup, staging=False)}
+                  "mixed_32req_3bit": mixed_measure(args.steps, args.warmup, staging=False),
+                  "draft_8b_32k_other_bits": bits_measure(w, device)}
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "draft_attn_traffic.txt")) as f:
