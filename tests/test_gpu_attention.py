@@ -369,13 +369,15 @@ def test_verify_full_size_sampled(name, n_q):
 
 # --------------------------------------------------------------- mixed
 
-def test_mixed_launch_matches_oracle_and_standalone():
-    """Staggered batch: even requests draft over 3-bit KV_comp, odd requests
-    verify x = 25 over KV_full, in one launch.  Draft and verify rows match
-    the oracle; verify rows are also bit-identical to the standalone
-    verification kernel."""
-    rng = np.random.default_rng(44)
-    d, hkv, grp, n_q, bits = 128, 2, 4, 25, 3
+@pytest.mark.parametrize("bits,d,grp", [(3, 128, 4), (2, 128, 8), (4, 64, 4), (16, 128, 4), (2, 64, 2), (16, 64, 8)])
+def test_mixed_launch_matches_oracle_and_standalone(bits, d, grp):
+    """Staggered batch: even requests draft over KV_comp, odd requests
+    verify x = 25 over KV_full, in one launch (every code width and head
+    size the launch instantiates).  Draft and verify rows match the oracle;
+    verify rows are also bit-identical to the standalone verification
+    kernel."""
+    rng = np.random.default_rng(44 + bits + d + grp)
+    hkv, n_q = 2, 25
     lens = [3000, 2100, 700, 4500, 1234, 90]
     role = np.array([b % 2 for b in range(len(lens))], np.int32)
     full, hf = H.full_cache(rng, lens, hkv, d)
