@@ -12,7 +12,8 @@
 //    tensor copies (one 16-row x 64-channel box per page and 128-byte column
 //    chunk); the TMA unit writes the 128-byte-swizzled layout the tensor core
 //    reads.  Full / empty mbarriers per stage (transaction bytes / MMA
-//    completion).
+//    completion).  The split's page ids are read into shared memory at
+//    set-up, and the producer starts while the other warps stage Q.
 //  - MMA warp: one thread issues every tcgen05.mma:  S = Q K^T (M 128, N 64,
 //    K 16 steps) into TMEM, then O += P V (M 128, N = D) with P read from
 //    TMEM as the A operand and V from shared memory (MN-major).  A one-tile
