@@ -241,7 +241,9 @@ VC_API vc_status vc_compress(const vc_paged_kv *full, const int32_t *kept_offset
  *               max_seq_len) bytes (0 when the format is unsupported)
  * Requires num_q_heads / num_kv_heads <= 8, head_dim in {64, 128}.  A request
  * with seq_len 0 gets zeros.  q must be finite and, for bits < 16, within the
- * fp16 range (|q| <= 65504).
+ * fp16 range (|q| <= 65504).  A block-table entry out of range is reported
+ * (VC_ERR_BAD_INDEX in dev_status); that request's output is then finite but
+ * void.
  */
 VC_API size_t vc_draft_workspace_bytes(const vc_paged_kv *comp, int32_t num_q_heads,
                                 int32_t max_seq_len);

@@ -22,8 +22,11 @@
 //      sum_t p_t v_hat_t = sum_t (p_t s_{t,g}) c_t + sum_t p_t z_{t,g}
 //    so no dequantised value is ever rounded.  bf16 caches (token-drop
 //    KV_comp) feed the bf16 MMA directly.
-//  - Online softmax in fp32 (log2 domain), partial (m, l, o) per chunk in the
-//    workspace, combined by draft_reduce_kernel.
+//  - Online softmax in fp32 (log2 domain) against a lazy reference (moved
+//    3 above a new maximum, so slightly larger later scores do not rescale
+//    again); partial (m, l, o) per chunk in the workspace, combined by
+//    draft_reduce_kernel.  Only a warp's last page can end inside; it is
+//    the one page drafted with the masking code.
 #include "draft_impl.cuh"
 
 namespace vc {

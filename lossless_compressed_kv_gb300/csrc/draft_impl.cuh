@@ -35,6 +35,13 @@ struct DraftArgs {
     const int32_t *slot = nullptr;
 };
 
+// Online softmax with a lazy reference: when a score beats the running
+// reference, the reference moves kLazyRef (log2 units) above the new
+// maximum, so that later, slightly larger scores do not rescale again.
+// Probabilities stay <= 2^-kLazyRef <= 1 (their f16 / bf16 operands cannot
+// overflow), and the partials carry the reference as their m.
+constexpr float kLazyRef = 3.0f;
+
 template <int BITS, int D, int NW>
 struct Cfg {
     static constexpr int NT = D / 16;  // k-steps of QK^T, m-tiles of PV
@@ -244,6 +251,13 @@ __device__ inline void load_halves(const __half *p, float (&f)[NG]) {
     }
 }
 
+// a ring stage given as a compile-time constant or at run time
+template <int N>
+__device__ constexpr int stage_value(std::integral_constant<int, N>) {
+    return N;
+}
+__device__ inline int stage_value(int s) { return s; }
+
 template <int BITS, int D, int NW>
 __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int kvh, int b, int chunk,
                                             uint8_t *smem) {
@@ -331,18 +345,16 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         }
         const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
         if (lane == 0 && !a.skip_copies) {
+            // a bad page id is reported and page 0 copied in its place (the
+            // stage then holds finite data; the request's result is void)
             const int st = k % C::NSTAGE;
             sflag[st] = id >= 0;
-            if (id < 0) {
-                report(a.status, VC_ERR_BAD_INDEX);
-                mbar_arrive(&bars[st]);
-            } else {
-                const int64_t off = ((int64_t)id * a.hkv + kvh) * C::HB;
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(&bars[st], 2 * C::HB);
-                bulk_g2s(ring + st * C::STAGE, a.kp + off, C::HB, &bars[st]);
-                bulk_g2s(ring + st * C::STAGE + C::HB, a.vp + off, C::HB, &bars[st]);
-            }
+            if (id < 0) report(a.status, VC_ERR_BAD_INDEX);
+            const int64_t off = ((int64_t)(id < 0 ? 0 : id) * a.hkv + kvh) * C::HB;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(&bars[st], 2 * C::HB);
+            bulk_g2s(ring + st * C::STAGE, a.kp + off, C::HB, &bars[st]);
+            bulk_g2s(ring + st * C::STAGE + C::HB, a.vp + off, C::HB, &bars[st]);
         }
     };
 
@@ -446,7 +458,8 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             }
-            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const float mn0 = mx0 > m[0] ? mx0 + kLazyRef : m[0];
+            const float mn1 = mx1 > m[1] ? mx1 + kLazyRef : m[1];
             if (__any_sync(0xffffffffu, mn0 > m[0] || mn1 > m[1])) {
                 const float al0 = mn0 == -INFINITY ? 1.0f : ex2(m[0] - mn0);
                 const float al1 = mn1 == -INFINITY ? 1.0f : ex2(m[1] - mn1);
@@ -523,9 +536,15 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         // unrolled driver below.  Two pages share the query-fragment loads,
         // the rescale check and the copy bookkeeping, and give the scheduler
         // two independent MMA chains.
-        auto body = [&](int k, auto s0c, uint32_t parity, auto npc) -> bool {
-            constexpr int S0 = decltype(s0c)::value;
+        // MASK: the pages may end inside (the request's ragged last page,
+        // or a page whose id was bad): scores and V parameters of the slots
+        // past the end are masked.  Every other page is full.  S0 is a
+        // compile-time constant on the unrolled path (an int for the
+        // masked last page).
+        auto body = [&](int k, auto s0c, uint32_t parity, auto npc, auto maskc) -> bool {
+            const int S0 = stage_value(s0c);
             constexpr int NPG = decltype(npc)::value;
+            constexpr bool MASK = decltype(maskc)::value;
             int nvalid[NPG];
 #pragma unroll
             for (int i = 0; i < NPG; ++i) {
@@ -594,14 +613,14 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 const f2 x01 = fma2(s01[i], f2{kscale, kscale}, f2{z[0], z[1]});
                 const f2 x23 = fma2(s23[i], f2{kscale, kscale}, f2{z[2], z[3]});
                 x[i][0] = x01.x; x[i][1] = x01.y; x[i][2] = x23.x; x[i][3] = x23.y;
-                if (nvalid[i] < kPage) {  // ragged last page: mask the scores of empty slots
+                if (MASK && nvalid[i] < kPage) {  // ragged last page: mask the scores of empty slots
                     if (g >= nvalid[i]) x[i][0] = x[i][1] = -INFINITY;
                     if (g + 8 >= nvalid[i]) x[i][2] = x[i][3] = -INFINITY;
                 }
                 mx = fmaxf(mx, fmaxf(fmaxf(x[i][0], x[i][1]), fmaxf(x[i][2], x[i][3])));
             }
 
-            // ---- online softmax: rescale only when a score beats the running max ----
+            // ---- online softmax: rescale only when a score beats the running reference ----
             if (__any_sync(0xffffffffu, mx > 0.0f || fresh)) {
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -615,7 +634,8 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
-                const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+                const float mn0 = mx0 > m[0] ? mx0 + kLazyRef : m[0];
+                const float mn1 = mx1 > m[1] ? mx1 + kLazyRef : m[1];
                 const float al0 = (mn0 == -INFINITY || m[0] == mn0) ? 1.0f : ex2(m[0] - mn0);
                 const float al1 = (mn1 == -INFINITY || m[1] == mn1) ? 1.0f : ex2(m[1] - mn1);
 #pragma unroll
@@ -660,7 +680,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 const uint32_t vone = g == C::NG ? 0x3C003C00u : 0u;
                 uint32_t vza0 = g < C::NG ? u.x : vone;
                 uint32_t vza2 = g < C::NG ? u.y : vone;
-                if (nvalid[i] < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
+                if (MASK && nvalid[i] < kPage) {  // empty slots' V parameters may hold anything (0 x NaN)
                     const int nv = nvalid[i];
                     const uint32_t mlo = (2 * t < nv ? 0x0000FFFFu : 0u) | (2 * t + 1 < nv ? 0xFFFF0000u : 0u);
                     const uint32_t mhi = (2 * t + 8 < nv ? 0x0000FFFFu : 0u) | (2 * t + 9 < nv ? 0xFFFF0000u : 0u);
@@ -711,20 +731,29 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         using I0 = std::integral_constant<int, 0>;
         using I1 = std::integral_constant<int, 1>;
         using I2 = std::integral_constant<int, 2>;
-        for (int k0 = 0; k0 < nw; k0 += C::NSTAGE) {
+        // the warp's last page is masked on its own when the request ends
+        // inside it; all other pages take the unmasked body (a bad page id is
+        // reported, and its stage holds page 0's blocks: finite, the result
+        // of that request void)
+        using NoMask = std::false_type;
+        const int last = nw - 1;
+        const bool mask_last = nw > 0 && len - (p0 + warp + NW * last) * kPage < kPage;
+        const int nfull = mask_last ? last : nw;
+        bool ok = true;
+        for (int k0 = 0; k0 < nfull && ok; k0 += C::NSTAGE) {
             const uint32_t parity = (uint32_t)(k0 / C::NSTAGE) & 1u;
-            bool ok;
-            if (k0 + 1 < nw)
-                ok = body(k0, I0{}, parity, I2{});
+            if (k0 + 1 < nfull)
+                ok = body(k0, I0{}, parity, I2{}, NoMask{});
             else
-                ok = body(k0, I0{}, parity, I1{});
+                ok = body(k0, I0{}, parity, I1{}, NoMask{});
             if (!ok) break;
-            if (k0 + 3 < nw)
-                ok = body(k0 + 2, I2{}, parity, I2{});
-            else if (k0 + 2 < nw)
-                ok = body(k0 + 2, I2{}, parity, I1{});
-            if (!ok) break;
+            if (k0 + 3 < nfull)
+                ok = body(k0 + 2, I2{}, parity, I2{}, NoMask{});
+            else if (k0 + 2 < nfull)
+                ok = body(k0 + 2, I2{}, parity, I1{}, NoMask{});
         }
+        if (ok && mask_last)
+            body(last, last % C::NSTAGE, (uint32_t)(last / C::NSTAGE) & 1u, I1{}, std::true_type{});
         l[0] = __shfl_sync(0xffffffffu, oz[0], C::NG * 4 + t);
         l[1] = __shfl_sync(0xffffffffu, oz[1], C::NG * 4 + t);
         // ---- finish O^T: codes part (2^24, rows g+8 2^(24 - ROW8)) + zero-point part of the group ----
