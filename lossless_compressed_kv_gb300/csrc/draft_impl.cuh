@@ -328,29 +328,36 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         }
     }
 
-    // Page ids of this warp's pages, 32 at a time: lane i holds page 32 blk + i
-    // (-1: past the warp's pages or not a valid page id).  Two blocks are kept
-    // so the table reads run a block ahead of the copies.
-    auto valid_id = [&](int kk, int id) -> int { return (kk < nw && id >= 0 && id < a.n_pages) ? id : -1; };
-    auto load_ids = [&](int blk) -> int {
-        const int kk = 32 * blk + lane;
-        return kk < nw ? valid_id(kk, raw_id(kk)) : -1;
+    // Head blocks (page id x hkv + kv head) of this warp's pages, 32 at a
+    // time: lane i holds page 32 blk + i (-1: past the warp's pages or not a
+    // valid page id).  Two blocks are kept so the table reads run a block
+    // ahead of the copies.  The block is advanced once per four pages by the
+    // loop driver, not per copy: this bookkeeping and the copy issue had cost
+    // about a sixth of the kernel's instructions.
+    auto head_row = [&](int kk, int id) -> int {
+        return (kk < nw && id >= 0 && id < a.n_pages) ? id * a.hkv + kvh : -1;
     };
-    int ids_cur = valid_id(lane, raw0), ids_nxt = valid_id(32 + lane, raw1), cur_blk = 0;
-    auto issue = [&](int k) {  // every lane (k is warp-uniform); lane 0 issues the copies
+    auto load_rows = [&](int blk) -> int {
+        const int kk = 32 * blk + lane;
+        return kk < nw ? head_row(kk, raw_id(kk)) : -1;
+    };
+    int rows_cur = head_row(lane, raw0), rows_nxt = head_row(32 + lane, raw1), cur_blk = 0;
+    auto advance_rows = [&](int k) {  // make page k's block current (k warp-uniform, non-decreasing)
         if ((k >> 5) != cur_blk) {
-            ids_cur = ids_nxt;
-            ids_nxt = load_ids((k >> 5) + 1);
+            rows_cur = rows_nxt;
+            rows_nxt = load_rows((k >> 5) + 1);
             cur_blk = k >> 5;
         }
-        const int id = __shfl_sync(0xffffffffu, ids_cur, k & 31);
+    };
+    auto issue = [&](int k) {  // every lane (k warp-uniform, in the current block); lane 0 issues the copies
+        const int row = __shfl_sync(0xffffffffu, rows_cur, k & 31);
         if (lane == 0 && !a.skip_copies) {
             // a bad page id is reported and page 0 copied in its place (the
             // stage then holds finite data; the request's result is void)
             const int st = k % C::NSTAGE;
-            sflag[st] = id >= 0;
-            if (id < 0) report(a.status, VC_ERR_BAD_INDEX);
-            const int64_t off = ((int64_t)(id < 0 ? 0 : id) * a.hkv + kvh) * C::HB;
+            if constexpr (BITS == 16) sflag[st] = row >= 0;
+            if (row < 0) report(a.status, VC_ERR_BAD_INDEX);
+            const int64_t off = (int64_t)(row < 0 ? kvh : row) * C::HB;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive_expect_tx(&bars[st], 2 * C::HB);
             bulk_g2s(ring + st * C::STAGE, a.kp + off, C::HB, &bars[st]);
@@ -429,9 +436,12 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
             const uint8_t *kb = ring + st * C::STAGE;
             uint8_t *vb = ring + st * C::STAGE + C::HB;
             const int pg = p0 + warp + NW * k;
-            if (!sflag[st]) {  // reported at issue time; nothing landed in this stage
+            if (!sflag[st]) {  // reported at issue time; page 0's blocks landed here
                 __syncwarp();
-                if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+                if (k + C::NSTAGE < nw) {
+                    advance_rows(k + C::NSTAGE);
+                    issue(k + C::NSTAGE);
+                }
                 continue;
             }
             const int slot0 = 2 * g, slot1 = 2 * g + 1;
@@ -497,7 +507,10 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
                 mma_bf16(o[mt], af, b0, b1);
             }
             __syncwarp();
-            if (k + C::NSTAGE < nw) issue(k + C::NSTAGE);
+            if (k + C::NSTAGE < nw) {
+                advance_rows(k + C::NSTAGE);
+                issue(k + C::NSTAGE);
+            }
         }
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -549,10 +562,9 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
 #pragma unroll
             for (int i = 0; i < NPG; ++i) {
                 if (!mbar_wait(&bars[S0 + i], parity, a.status, a.wait_ns)) return false;
-                // slots >= nvalid are past the end; a bad page id (reported
-                // at issue time, nothing copied) masks the whole stage
+                // slots >= nvalid are past the end (used by the masked body only)
                 const int pg = p0 + warp + NW * (k + i);
-                nvalid[i] = sflag[S0 + i] ? len - pg * kPage : 0;
+                nvalid[i] = len - pg * kPage;
             }
 
             // ---- shared-memory reads of the pages' K rows and parameters ----
@@ -742,6 +754,7 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         bool ok = true;
         for (int k0 = 0; k0 < nfull && ok; k0 += C::NSTAGE) {
             const uint32_t parity = (uint32_t)(k0 / C::NSTAGE) & 1u;
+            advance_rows(k0 + C::NSTAGE);  // the copies issued below: pages k0 + 4 .. k0 + 7, one block
             if (k0 + 1 < nfull)
                 ok = body(k0, I0{}, parity, I2{}, NoMask{});
             else
