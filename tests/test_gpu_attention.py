@@ -162,22 +162,32 @@ def test_empty_batch_through_the_binding():
     assert torch.equal(comp.k_pages, k0) and torch.equal(comp.v_pages, v0)
 
 
-def test_draft_bad_page_id_reported():
-    rng = np.random.default_rng(6)
-    full, hf = H.full_cache(rng, [64], 1, 64)
-    comp, ctable = H.comp_cache(rng, 1, 64, 1, 64, 2)
-    compress_all(full, comp, [np.arange(64, dtype=np.int32)])
+@pytest.mark.parametrize("bits,n,bad_page", [(2, 64, 2), (2, 60, 3), (3, 200, 0), (16, 60, 3)])
+def test_draft_bad_page_id_reported(bits, n, bad_page):
+    """An out-of-range block-table entry (a full page in the middle, the
+    ragged last page, the first page) is reported; the request's output
+    stays finite and the other request's rows match the oracle."""
+    rng = np.random.default_rng(6 + bits + n)
+    lens = [n, 90]
+    full, hf = H.full_cache(rng, lens, 1, 64)
+    comp, ctable = H.comp_cache(rng, 2, lens, 1, 64, bits)
+    kept = [np.arange(k, dtype=np.int32) for k in lens]
+    compress_all(full, comp, kept)
     bt = comp.block_table.clone()
-    bt[0, 2] = comp.num_pages + 5                       # out of range: must be skipped, not read
-    bad = vc().PagedKV(comp.k_pages, comp.v_pages, bt, comp.seq_lens, 1, 64, 2)
-    qn, qd = q_bf16(rng, (1, 4, 64))
+    bt[0, bad_page] = comp.num_pages + 5                # out of range: reported, never read
+    bad = vc().PagedKV(comp.k_pages, comp.v_pages, bt, comp.seq_lens, 1, 64, bits)
+    qn, qd = q_bf16(rng, (2, 4, 64))
     m = vc()
-    out = torch.empty((1, 4, 64), dtype=torch.float32, device="cuda")
-    ws = torch.empty(m.draft_workspace_bytes(bad, 4, 64), dtype=torch.uint8, device="cuda")
+    out = torch.empty((2, 4, 64), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.draft_workspace_bytes(bad, 4, max(lens)), dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    m.draft_attn(qd, bad, 0.125, out, 64, ws, status=st)
+    m.draft_attn(qd, bad, 0.125, out, max(lens), ws, status=st)
     torch.cuda.synchronize()
-    assert st.item() == 3 and torch.isfinite(out).all()
+    got = out.cpu().numpy()
+    assert st.item() == 3 and np.isfinite(got).all()
+    k, v = H.logical_full(hf, 1)
+    ref = oracle.draft_attn(qn[1], oracle.compress(k, v, kept[1], bits), float(np.float32(0.125)))
+    assert H.row_err(got[1], ref) <= H.TOL
 
 
 def test_draft_tiny_workload():
