@@ -553,11 +553,10 @@ __device__ __forceinline__ void draft_block(const DraftArgs &a, int split, int k
         // unrolled driver below.  Two pages share the query-fragment loads,
         // the rescale check and the copy bookkeeping, and give the scheduler
         // two independent MMA chains.
-        // MASK: the pages may end inside (the request's ragged last page,
-        // or a page whose id was bad): scores and V parameters of the slots
-        // past the end are masked.  Every other page is full.  S0 is a
-        // compile-time constant on the unrolled path (an int for the
-        // masked last page).
+        // MASK: the page may end inside (the request's ragged last page):
+        // scores and V parameters of the slots past the end are masked.
+        // Every other page is full.  S0 is a compile-time constant on the
+        // unrolled path (an int for the masked last page).
         auto body = [&](int k, auto s0c, uint32_t parity, auto npc, auto maskc) -> bool {
             const int S0 = stage_value(s0c);
             constexpr int NPG = decltype(npc)::value;
