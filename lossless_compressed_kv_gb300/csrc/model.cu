@@ -103,6 +103,84 @@ __global__ void __launch_bounds__(256) linear_kernel(const float *x, const uint1
     }
 }
 
+// The same products for up to MR rows (decode and draft steps): one output
+// column per thread and every row's fp32 FMA chain in increasing k, exactly
+// the tiled kernel's arithmetic (k padded with zeros to a multiple of TK), so
+// a row's bits do not depend on which kernel computed it.  A 64 x 128 tile
+// for a handful of rows wasted most of its work and gave the narrow
+// projections a few CTAs; here one warp owns 32 columns, and its W tile
+// (kChunk rows x 32 columns) is brought into shared memory by asynchronous
+// 16-byte copies one chunk ahead, so enough bytes are in flight per warp
+// (a column read straight from global memory leaves each warp a few
+// hundred bytes in flight: the kernel then ran at ~100 GB/s).
+constexpr int kSmallRows = 16;
+constexpr int kSmallCols = 32;  // threads (= columns) per CTA
+constexpr int kChunk = 256;     // k per W tile
+__device__ inline void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+template <int MR>
+__global__ void __launch_bounds__(kSmallCols) linear_rows_kernel(const float *x, const uint16_t *w, float *out,
+                                                                 int m, int k, int n, int accumulate) {
+    pdl_begin();
+    __shared__ __align__(16) float xs[kChunk][MR];                // bf16-rounded activations, k-major
+    __shared__ __align__(16) uint16_t ws[2][kChunk][kSmallCols];  // W tiles, double-buffered
+    const int lane = threadIdx.x;
+    const int c0 = blockIdx.x * kSmallCols, c = c0 + lane;
+    const int kp = ceil_div(k, TK) * TK;  // the tiled kernel's zero-padded k
+    const int nchunk = ceil_div(kp, kChunk);
+    // 16-byte copies need whole 8-column groups at 16-byte aligned addresses
+    const bool vec = (n % 8 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
+    auto load_w = [&](int buf, int k0) {  // rows [k0, k0 + kChunk), columns [c0, c0 + 32)
+        for (int e = lane; e < kChunk * (kSmallCols / 8); e += kSmallCols) {
+            const int kk = e / (kSmallCols / 8), q = e % (kSmallCols / 8);
+            const int kr = k0 + kk, cq = c0 + 8 * q;
+            uint16_t *dst = &ws[buf][kk][8 * q];
+            if (vec && kr < k && cq + 8 <= n) {
+                cp_async16(dst, w + (int64_t)kr * n + cq);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = (kr < k && cq + j < n) ? w[(int64_t)kr * n + cq + j] : 0;
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float acc[MR];
+#pragma unroll
+    for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
+    load_w(0, 0);
+    for (int i = 0; i < nchunk; ++i) {
+        const int k0 = i * kChunk, kn = min(kChunk, kp - k0);
+        if (i + 1 < nchunk) load_w((i + 1) & 1, k0 + kChunk);
+        for (int e = lane; e < kn * MR; e += kSmallCols) {
+            const int kk = e / MR, r = e % MR;
+            float v = 0.0f;
+            if (r < m && k0 + kk < k) v = __bfloat162float(__float2bfloat16_rn(x[(int64_t)r * k + k0 + kk]));
+            xs[kk][r] = v;
+        }
+        if (i + 1 < nchunk)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const uint16_t(*wt)[kSmallCols] = ws[i & 1];
+#pragma unroll 8
+        for (int kk = 0; kk < kn; ++kk) {
+            const float bv = bf16_bits_to_f32(wt[kk][lane]);
+#pragma unroll
+            for (int r = 0; r < MR; ++r) acc[r] = fmaf(xs[kk][r], bv, acc[r]);
+        }
+        __syncthreads();  // the tiles and xs are rewritten next
+    }
+    if (c >= n) return;
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+        if (r >= m) break;
+        float *o = out + (int64_t)r * n + c;
+        *o = accumulate ? (*o + acc[r]) : acc[r];
+    }
+}
+
 // silu(g) * u, g = gu[:, :f], u = gu[:, f:]
 __global__ void swiglu_kernel(const float *gu, int m, int f, float *out) {
     pdl_begin();
@@ -184,9 +262,20 @@ vc_status vc_linear(const float *x, const void *w_bf16, float *out, int32_t m, i
                     int32_t accumulate, vc_stream_t stream) {
     if (!x || !w_bf16 || !out || m < 0 || k < 1 || n < 1) return VC_ERR_INVALID_ARG;
     if (m == 0) return VC_OK;
-    dim3 grid(ceil_div(n, TN), ceil_div(m, TM));
-    launch_pdl(linear_kernel, grid, 256, 0, (cudaStream_t)stream, x, (const uint16_t *)w_bf16, out, m, k, n,
-               accumulate);
+    const uint16_t *w = (const uint16_t *)w_bf16;
+    const cudaStream_t st = (cudaStream_t)stream;
+    if (m <= kSmallRows) {
+        const dim3 grid(ceil_div(n, kSmallCols));
+        if (m <= 4)
+            launch_pdl(linear_rows_kernel<4>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
+        else if (m <= 8)
+            launch_pdl(linear_rows_kernel<8>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
+        else
+            launch_pdl(linear_rows_kernel<16>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
+    } else {
+        dim3 grid(ceil_div(n, TN), ceil_div(m, TM));
+        launch_pdl(linear_kernel, grid, 256, 0, st, x, w, out, m, k, n, accumulate);
+    }
     return cudaGetLastError() == cudaSuccess ? VC_OK : VC_ERR_CUDA;
 }
 

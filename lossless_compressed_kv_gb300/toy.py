@@ -37,6 +37,21 @@ def _dev_bf16(a: np.ndarray, device):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
 
+def _graph(fn):
+    """CUDA graph of the work `fn` enqueues (run once on a side stream first,
+    which is also the first execution of that work)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
 @dataclass
 class ToyShape:
     layers: int
@@ -171,30 +186,46 @@ class ToyDecoder:
 
     # -- full-KV greedy decoding (the reference) ---------------------------
     def greedy_full(self, first: torch.Tensor, full, start: int, n_tokens: int):
+        """One token per step with the full cache; every step is the same
+        CUDA graph (positions advanced on the device), replayed."""
         s, B = self.s, int(first.numel())
-        out = [first.clone()]
-        tok = first.clone()
+        outs = torch.empty((B, n_tokens), dtype=torch.int32, device=self.dev)
+        outs[:, 0] = first
+        tok = self._buf("g_tok", (B,), torch.int32)
+        tok.copy_(first)
         row_req = torch.arange(B, dtype=torch.int32, device=self.dev)
+        row_pos = self._buf("g_pos", (B,), torch.int32)
+        row_pos.fill_(start)
+        lens = self._buf("g_lens", (B,), torch.int32)
         ws = self._buf("g_vws", (vc.verify_workspace_bytes(full[0], 1, s.hq, start + n_tokens + 1),), torch.uint8)
-        for step in range(n_tokens - 1):
-            pos = start + step
-            row_pos = torch.full((B,), pos, dtype=torch.int32, device=self.dev)
-            lens = torch.full((B,), pos + 1, dtype=torch.int32, device=self.dev)
 
-            def attn(li, q, o):
-                vc.verify_attn(q.view(B, 1, s.hq, s.d), self.view(full[li], lens), self.scale,
-                               o.view(B, 1, s.hq, s.d), start + n_tokens + 1, ws, status=self.status)
+        def attn(li, q, o):
+            vc.verify_attn(q.view(B, 1, s.hq, s.d), self.view(full[li], lens), self.scale,
+                           o.view(B, 1, s.hq, s.d), start + n_tokens + 1, ws, status=self.status)
 
+        def step():
+            torch.add(row_pos, 1, out=lens)
             hidden = self.forward(tok, row_req, row_pos, full, attn)
             ver, _, _ = self.argmax(hidden, B, 1)
-            tok = ver[:, 0].clone()
-            out.append(tok)
-        return torch.stack(out, dim=1)  # [B][n_tokens]
+            tok.copy_(ver[:, 0])
+            row_pos.add_(1)
+
+        if n_tokens > 1:
+            g = _graph(step)  # the first step runs while the graph is captured
+            outs[:, 1] = tok
+            for i in range(2, n_tokens):
+                g.replay()
+                outs[:, i] = tok
+        return outs  # [B][n_tokens]
 
     # -- VeriCache rounds ----------------------------------------------------
     def vericache(self, first: torch.Tensor, full, comp, start: int, n_tokens: int, stats=None):
         """Draft x tokens per round on KV_comp, verify x + 1 on KV_full,
-        accept, commit.  KV_comp must already hold the compressed prompt."""
+        accept, commit.  KV_comp must already hold the compressed prompt.
+        The x draft steps of a round are one CUDA graph and the verification
+        pass another, both replayed every round with the round's positions
+        in device buffers; the host reads the accepted lengths once per
+        round and commits."""
         s, B, x = self.s, int(first.numel()), self.s.x
         dev = self.dev
         P = [start] * B                 # position of the pending token
@@ -208,15 +239,28 @@ class ToyDecoder:
         row_req1 = torch.arange(B, dtype=torch.int32, device=dev)
         row_reqv = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(x + 1)
         offs1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
-        rounds = accepted = 0
-        while min(len(g) for g in gen) < n_tokens:
-            # ---- draft x tokens with the compressed cache ----
-            drafts = torch.empty((B, x), dtype=torch.int32, device=dev)
-            tok = torch.tensor(pending, dtype=torch.int32, device=dev)
+        jv = torch.arange(x + 1, dtype=torch.int32, device=dev)
+        # the round's inputs (set before the graphs run)
+        p_dev = self._buf("r_p", (B,), torch.int32)          # P
+        c_dev = self._buf("r_c", (B,), torch.int32)          # Cn
+        pend = self._buf("r_pend", (B,), torch.int32)        # pending tokens
+        # buffers the graphs use
+        tok = self._buf("r_tok", (B,), torch.int32)
+        drafts = self._buf("r_drafts", (B, x), torch.int32)
+        row_pos = self._buf("r_pos", (B,), torch.int32)
+        clens = self._buf("r_clens", (B,), torch.int32)
+        cstart = self._buf("r_cstart", (B,), torch.int32)
+        ids = self._buf("r_ids", (B, x + 1), torch.int32)
+        vpos = self._buf("r_vpos", (B, x + 1), torch.int32)
+        flens = self._buf("r_flens", (B,), torch.int32)
+        res = {}
+
+        def draft_round():
+            tok.copy_(pend)
             for i in range(x):
-                row_pos = torch.tensor([p + i for p in P], dtype=torch.int32, device=dev)
-                clens = torch.tensor([c + i + 1 for c in Cn], dtype=torch.int32, device=dev)
-                cstart = torch.tensor([c + i for c in Cn], dtype=torch.int32, device=dev)
+                torch.add(p_dev, i, out=row_pos)
+                torch.add(c_dev, i + 1, out=clens)
+                torch.add(c_dev, i, out=cstart)
 
                 def attn(li, q, o):
                     # the token's K/V was just written into KV_full at P + i:
@@ -229,19 +273,34 @@ class ToyDecoder:
                 hidden = self.forward(tok, row_req1, row_pos, full, attn)
                 ver, _, _ = self.argmax(hidden, B, 1)
                 drafts[:, i] = ver[:, 0]
-                tok = ver[:, 0].contiguous()
-            # ---- verify the block [pending, d_0 .. d_{x-1}] with the full cache ----
-            ids = torch.cat([torch.tensor(pending, dtype=torch.int32, device=dev)[:, None], drafts], 1).reshape(-1)
-            row_pos = torch.tensor([p + j for p in P for j in range(x + 1)], dtype=torch.int32, device=dev)
-            flens = torch.tensor([p + x + 1 for p in P], dtype=torch.int32, device=dev)
+                tok.copy_(ver[:, 0])
 
-            def vattn(li, q, o):
-                vc.verify_attn(q.view(B, x + 1, s.hq, s.d), self.view(full[li], flens), self.scale,
-                               o.view(B, x + 1, s.hq, s.d), cap, vws, status=self.status)
+        def vattn(li, q, o):
+            vc.verify_attn(q.view(B, x + 1, s.hq, s.d), self.view(full[li], flens), self.scale,
+                           o.view(B, x + 1, s.hq, s.d), cap, vws, status=self.status)
 
-            hidden = self.forward(ids.contiguous(), row_reqv, row_pos, full, vattn)
-            ver, al, em = self.argmax(hidden, B, x + 1, drafts)
-            al_h, em_h = al.cpu().tolist(), em.cpu().tolist()
+        def verify_round():
+            # verify the block [pending, d_0 .. d_{x-1}] with the full cache
+            ids[:, 0] = pend
+            ids[:, 1:] = drafts
+            torch.add(p_dev[:, None], jv[None, :], out=vpos)
+            torch.add(p_dev, x + 1, out=flens)
+            hidden = self.forward(ids.view(-1), row_reqv, vpos.view(-1), full, vattn)
+            res["ver"], res["al"], res["em"] = self.argmax(hidden, B, x + 1, drafts)
+
+        g_draft = g_verify = None
+        rounds = accepted = 0
+        while min(len(g) for g in gen) < n_tokens:
+            p_dev.copy_(torch.tensor(P, dtype=torch.int32))
+            c_dev.copy_(torch.tensor(Cn, dtype=torch.int32))
+            pend.copy_(torch.tensor(pending, dtype=torch.int32))
+            if g_draft is None:
+                g_draft = _graph(draft_round)  # the first round runs while the graphs are captured
+                g_verify = _graph(verify_round)
+            else:
+                g_draft.replay()
+                g_verify.replay()
+            al_h, em_h = res["al"].cpu().tolist(), res["em"].cpu().tolist()
             # ---- commit: KV_full keeps P..P+a, KV_comp re-filled from it ----
             done = [len(gen[b]) >= n_tokens for b in range(B)]
             kept = [list(range(P[b], P[b] + (0 if done[b] else al_h[b]) + 1)) for b in range(B)]

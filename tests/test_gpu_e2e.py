@@ -62,3 +62,32 @@ def test_e2e_greedy_against_cpu_oracle_model():
             assert am[t] == gpu_next[t], (b, t, am[t], gpu_next[t], margin[t])
     print("oracle e2e check: %d of %d positions excluded as near-ties" % (excluded, 2 * 24))
     assert excluded < 8
+
+
+@pytest.mark.parametrize("k,n", [(1024, 1536), (4096, 1024), (100, 70)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_linear_rows_invariant_across_kernels(k, n, accumulate):
+    """vc_linear computes up to 16 rows with the small-row kernel and more
+    rows with the tiled one; a row's bits must not depend on which (the
+    decode and draft steps use the first, verification blocks and the
+    prefill the second), and both must equal an fp64 product of the
+    bf16-rounded operands to fp32 accuracy."""
+    import torch
+    import lossless_compressed_kv_gb300 as vc
+    g = torch.Generator(device="cuda")
+    g.manual_seed(k * 7 + n + accumulate)
+    x = torch.randn((40, k), generator=g, device="cuda")
+    w = (torch.randn((k, n), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    base = torch.randn((40, n), generator=g, device="cuda")
+    big = base.clone()
+    vc.linear(x, w, big, accumulate=accumulate)          # 40 rows: tiled kernel
+    for m in (1, 3, 4, 5, 8, 13, 16):
+        small = base[:m].clone()
+        vc.linear(x[:m].contiguous(), w, small, accumulate=accumulate)
+        assert torch.equal(small, big[:m]), m
+    torch.cuda.synchronize()
+    xr = x.to(torch.bfloat16).double().cpu().numpy()
+    ref = xr @ w.double().cpu().numpy() + (base.double().cpu().numpy() if accumulate else 0.0)
+    got = big.double().cpu().numpy()
+    scale = np.abs(xr) @ np.abs(w.double().cpu().numpy()) + (np.abs(base.double().cpu().numpy()) if accumulate else 0)
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-6)
