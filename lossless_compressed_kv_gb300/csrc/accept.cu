@@ -144,6 +144,105 @@ __global__ void __launch_bounds__(kThreadsL) logits_argmax_kernel(const float *h
     }
 }
 
+// The same logits for up to MR rows (decode and draft steps of a small
+// batch): one vocabulary column per thread, each row's fp32 FMA chain in
+// increasing k as in the tiled kernel (bit-identical logits), one warp per
+// 32 columns with its W tile (kLK rows x 32 columns, fp32) staged in shared
+// memory by asynchronous 16-byte copies one chunk ahead.  The tiled kernel
+// spends a 16-row tile on a handful of rows and keeps few bytes in flight.
+constexpr int kLRows = 16;
+constexpr int kLCols = 32;
+constexpr int kLK = 128;
+__device__ inline void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+template <int MR, bool STORE>
+__global__ void __launch_bounds__(kLCols) logits_rows_kernel(const float *h, int rows, const float *w, int d,
+                                                            int vocab, unsigned long long *keys, float *logits) {
+    pdl_begin();
+    __shared__ __align__(16) float hs[kLK][MR];
+    __shared__ __align__(16) float ws[2][kLK][kLCols];
+    const int lane = threadIdx.x;
+    const int c0 = blockIdx.x * kLCols, c = c0 + lane;
+    const int nchunk = ceil_div(d, kLK);
+    const bool vec = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
+    auto load_w = [&](int buf, int k0) {
+        for (int e = lane; e < kLK * (kLCols / 4); e += kLCols) {
+            const int kk = e / (kLCols / 4), q = e % (kLCols / 4);
+            const int kr = k0 + kk, cq = c0 + 4 * q;
+            float *dst = &ws[buf][kk][4 * q];
+            if (vec && kr < d && cq + 4 <= vocab) {
+                cp_async16(dst, w + (int64_t)kr * vocab + cq);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = (kr < d && cq + j < vocab) ? w[(int64_t)kr * vocab + cq + j] : 0.0f;
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float acc[MR];
+#pragma unroll
+    for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
+    load_w(0, 0);
+    for (int i = 0; i < nchunk; ++i) {
+        const int k0 = i * kLK, kn = min(kLK, d - k0);
+        if (i + 1 < nchunk) load_w((i + 1) & 1, k0 + kLK);
+        for (int e = lane; e < kn * MR; e += kLCols) {
+            const int kk = e / MR, r = e % MR;
+            hs[kk][r] = r < rows ? h[(int64_t)r * d + k0 + kk] : 0.0f;
+        }
+        if (i + 1 < nchunk)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const float(*wt)[kLCols] = ws[i & 1];
+#pragma unroll 8
+        for (int kk = 0; kk < kn; ++kk) {
+            const float wv = wt[kk][lane];
+#pragma unroll
+            for (int r = 0; r < MR; ++r) acc[r] = fmaf(hs[kk][r], wv, acc[r]);
+        }
+        __syncthreads();
+    }
+    if constexpr (STORE) {
+        if (c < vocab)
+#pragma unroll
+            for (int r = 0; r < MR; ++r)
+                if (r < rows) logits[(int64_t)r * vocab + c] = acc[r];
+        return;
+    }
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+        if (r >= rows) break;
+        unsigned long long best = c < vocab ? argmax_key(acc[r], c) : 0ull;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
+        }
+        if (lane == 0 && best) atomicMax(&keys[r], best);
+    }
+}
+
+// Logits (argmax keys, or stored) of `rows` prediction rows.
+template <bool STORE>
+void launch_logits(const float *h, int rows, const float *w, int d, int vocab, unsigned long long *keys,
+                   float *logits, cudaStream_t st) {
+    if (rows <= kLRows) {
+        const dim3 grid(ceil_div(vocab, kLCols));
+        if (rows <= 4)
+            launch_pdl(logits_rows_kernel<4, STORE>, grid, kLCols, 0, st, h, rows, w, d, vocab, keys, logits);
+        else if (rows <= 8)
+            launch_pdl(logits_rows_kernel<8, STORE>, grid, kLCols, 0, st, h, rows, w, d, vocab, keys, logits);
+        else
+            launch_pdl(logits_rows_kernel<16, STORE>, grid, kLCols, 0, st, h, rows, w, d, vocab, keys, logits);
+        return;
+    }
+    dim3 grid(ceil_div(vocab, kCols), ceil_div(rows, kRowsT));
+    launch_pdl(logits_argmax_kernel<STORE>, grid, kThreadsL, 0, st, h, rows, w, d, vocab, keys, logits);
+}
+
 __global__ void accept_finalize_kernel(const unsigned long long *keys, int n_pred, const int32_t *drafts, int x,
                                        int32_t *verified, int32_t *accept_len, int32_t *emitted) {
     pdl_begin();
@@ -336,8 +435,7 @@ cudaError_t accept_launch(const float *hidden, int batch, int n_pred, int hg, co
     float *h = reinterpret_cast<float *>(keys + rows);
     const int64_t nh = (int64_t)rows * d;
     launch_pdl(group_mean_kernel, (unsigned)((nh + 255) / 256), 256, 0, st, hidden, rows, hg, d, h, keys);
-    dim3 grid(ceil_div(vocab, kCols), ceil_div(rows, kRowsT));
-    launch_pdl(logits_argmax_kernel<false>, grid, kThreadsL, 0, st, h, rows, w, d, vocab, keys, nullptr);
+    launch_logits<false>(h, rows, w, d, vocab, keys, nullptr, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     launch_pdl(accept_finalize_kernel, batch, 128, n_pred * sizeof(int32_t), st, keys, n_pred, drafts, x, verified,
@@ -365,13 +463,11 @@ cudaError_t accept_sampled_launch(const float *target_hidden, const float *draft
     float *ld = lt + (size_t)rt * vocab;
     launch_pdl(group_mean_kernel, (unsigned)(((int64_t)rt * d + 255) / 256), 256, 0, st, target_hidden, rt, hg, d,
                ht, nullptr);
-    launch_pdl(logits_argmax_kernel<true>, dim3(ceil_div(vocab, kCols), ceil_div(rt, kRowsT)), kThreadsL, 0, st,
-               ht, rt, w, d, vocab, nullptr, lt);
+    launch_logits<true>(ht, rt, w, d, vocab, nullptr, lt, st);
     if (rd > 0) {
         launch_pdl(group_mean_kernel, (unsigned)(((int64_t)rd * d + 255) / 256), 256, 0, st, draft_hidden, rd, hg,
                    d, hd, nullptr);
-        launch_pdl(logits_argmax_kernel<true>, dim3(ceil_div(vocab, kCols), ceil_div(rd, kRowsT)), kThreadsL, 0,
-                   st, hd, rd, w, d, vocab, nullptr, ld);
+        launch_logits<true>(hd, rd, w, d, vocab, nullptr, ld, st);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
