@@ -103,81 +103,141 @@ __global__ void __launch_bounds__(256) linear_kernel(const float *x, const uint1
     }
 }
 
-// The same products for up to MR rows (decode and draft steps): one output
-// column per thread and every row's fp32 FMA chain in increasing k, exactly
-// the tiled kernel's arithmetic (k padded with zeros to a multiple of TK), so
-// a row's bits do not depend on which kernel computed it.  A 64 x 128 tile
-// for a handful of rows wasted most of its work and gave the narrow
-// projections a few CTAs; here one warp owns 32 columns, and its W tile
-// (kChunk rows x 32 columns) is brought into shared memory by asynchronous
-// 16-byte copies one chunk ahead, so enough bytes are in flight per warp
-// (a column read straight from global memory leaves each warp a few
-// hundred bytes in flight: the kernel then ran at ~100 GB/s).
+// The same products for up to 16 rows (decode and draft steps), with every
+// (row, column) fp32 FMA chain in increasing k, exactly the tiled kernel's
+// arithmetic (k padded with zeros to a multiple of TK; the further zero
+// products of a chunk's tail leave a sum unchanged, as a sum that starts at
+// +0 is never -0), so a row's bits do not depend on which kernel computed
+// it.  Such a chain is k dependent FMAs long, which bounds the time from
+// below (about 4 cycles per k); with a handful of rows a 64 x 128 tile
+// wastes most of its work and gives the narrow projections a few CTAs.
+// Here a CTA owns 32 columns and has one warp per kRowsPerWarp rows, each
+// thread carrying those rows' chains of one column, fed by one W value; the
+// CTA's warps share the W tile (kChunk x 32 columns) and the x tile (rows
+// x kChunk), both requested by asynchronous 16-byte copies
+// kStages - 1 chunks ahead and x rounded to bf16 in place once per chunk.
+// A chunk is summed as straight-line code that asks for the next 16 k's
+// operands before the current 16 k's FMAs.  Measured at 4 rows, k = 1024:
+// ~15 cycles per k against the chain's ~4, most of it waiting on
+// fixed-latency and shared-memory dependencies (the compiler keeps few
+// operands in flight); one warp carrying all rows of a column spent ~40.
 constexpr int kSmallRows = 16;
-constexpr int kSmallCols = 32;  // threads (= columns) per CTA
-constexpr int kChunk = 256;     // k per W tile
+constexpr int kSmallCols = 32;  // columns per CTA (= lanes of a warp)
+constexpr int kChunk = 256;     // k per tile
+constexpr int kStages = 4;      // tiles in the ring
+// rows (chains) per thread, one W value feeding them all: one up to 8 rows,
+// two above (4 rows, k = 1024: 8.3 us against 14.0 with two; 16 rows: 16.4
+// against 14.0)
+inline int small_rows_per_warp(int m) { return m <= 8 ? 1 : 2; }
+inline int small_rows_smem(int m, int R) {  // x tiles padded to whole warps with zero rows
+    return kStages * (kChunk * kSmallCols * 2 + ceil_div(m, R) * R * kChunk * 4);
+}
 __device__ inline void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-template <int MR>
-__global__ void __launch_bounds__(kSmallCols) linear_rows_kernel(const float *x, const uint16_t *w, float *out,
-                                                                 int m, int k, int n, int accumulate) {
+template <int kRowsPerWarp>
+__global__ void __launch_bounds__(kSmallCols *kSmallRows) linear_rows_kernel(const float *x, const uint16_t *w,
+                                                                            float *out, int m, int k, int n,
+                                                                            int accumulate) {
     pdl_begin();
-    __shared__ __align__(16) float xs[kChunk][MR];                // bf16-rounded activations, k-major
-    __shared__ __align__(16) uint16_t ws[2][kChunk][kSmallCols];  // W tiles, double-buffered
-    const int lane = threadIdx.x;
+    extern __shared__ __align__(16) uint8_t dsm[];
+    uint16_t(*ws)[kChunk][kSmallCols] = reinterpret_cast<uint16_t(*)[kChunk][kSmallCols]>(dsm);
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, r0 = (tid >> 5) * kRowsPerWarp;
+    const int mp = (nt >> 5) * kRowsPerWarp;  // x tile rows; rows from m on are zeros
+    float *xs = reinterpret_cast<float *>(dsm + kStages * kChunk * kSmallCols * 2);  // stage s: [mp][kChunk]
     const int c0 = blockIdx.x * kSmallCols, c = c0 + lane;
     const int kp = ceil_div(k, TK) * TK;  // the tiled kernel's zero-padded k
     const int nchunk = ceil_div(kp, kChunk);
-    // 16-byte copies need whole 8-column groups at 16-byte aligned addresses
-    const bool vec = (n % 8 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
-    auto load_w = [&](int buf, int k0) {  // rows [k0, k0 + kChunk), columns [c0, c0 + 32)
-        for (int e = lane; e < kChunk * (kSmallCols / 8); e += kSmallCols) {
-            const int kk = e / (kSmallCols / 8), q = e % (kSmallCols / 8);
-            const int kr = k0 + kk, cq = c0 + 8 * q;
-            uint16_t *dst = &ws[buf][kk][8 * q];
-            if (vec && kr < k && cq + 8 <= n) {
-                cp_async16(dst, w + (int64_t)kr * n + cq);
-            } else {
+    // 16-byte copies need whole 8-column (W) or 4-element (x) groups at 16-byte aligned addresses
+    const bool wvec = (n % 8 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
+    const bool xvec = (k % 4 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    auto load = [&](int i) {  // chunk i: k in [i kChunk, (i + 1) kChunk), zeros from k on
+        if (i < nchunk) {
+            const int k0 = i * kChunk;
+            float *xd = xs + (i % kStages) * mp * kChunk;
+            for (int e = tid; e < mp * (kChunk / 4); e += nt) {
+                const int rr = e / (kChunk / 4), kk = 4 * (e % (kChunk / 4)), kr = k0 + kk;
+                float *d = xd + rr * kChunk + kk;
+                const float *src = x + (int64_t)rr * k + kr;
+                if (xvec && rr < m && kr + 4 <= k) {
+                    cp_async16(d, src);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = (kr < k && cq + j < n) ? w[(int64_t)kr * n + cq + j] : 0;
+                    for (int j = 0; j < 4; ++j) d[j] = (rr < m && kr + j < k) ? src[j] : 0.0f;
+                }
+            }
+            uint16_t(*wd)[kSmallCols] = ws[i % kStages];
+            for (int e = tid; e < kChunk * (kSmallCols / 8); e += nt) {
+                const int kk = e / (kSmallCols / 8), q = e % (kSmallCols / 8);
+                const int kr = k0 + kk, cq = c0 + 8 * q;
+                if (wvec && kr < k && cq + 8 <= n) {
+                    cp_async16(&wd[kk][8 * q], w + (int64_t)kr * n + cq);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        wd[kk][8 * q + j] = (kr < k && cq + j < n) ? w[(int64_t)kr * n + cq + j] : 0;
+                }
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");  // one group per chunk slot, empty past the end
     };
-    float acc[MR];
-#pragma unroll
-    for (int r = 0; r < MR; ++r) acc[r] = 0.0f;
-    load_w(0, 0);
+    float acc[kRowsPerWarp] = {};
+    for (int i = 0; i < kStages - 1; ++i) load(i);
     for (int i = 0; i < nchunk; ++i) {
-        const int k0 = i * kChunk, kn = min(kChunk, kp - k0);
-        if (i + 1 < nchunk) load_w((i + 1) & 1, k0 + kChunk);
-        for (int e = lane; e < kn * MR; e += kSmallCols) {
-            const int kk = e / MR, r = e % MR;
-            float v = 0.0f;
-            if (r < m && k0 + kk < k) v = __bfloat162float(__float2bfloat16_rn(x[(int64_t)r * k + k0 + kk]));
-            xs[kk][r] = v;
-        }
-        if (i + 1 < nchunk)
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        else
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        load(i + kStages - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");  // chunk i has landed
         __syncthreads();
-        const uint16_t(*wt)[kSmallCols] = ws[i & 1];
-#pragma unroll 8
-        for (int kk = 0; kk < kn; ++kk) {
-            const float bv = bf16_bits_to_f32(wt[kk][lane]);
+        float *xt = xs + (i % kStages) * mp * kChunk;
+        for (int e = tid; e < mp * kChunk; e += nt) xt[e] = __bfloat162float(__float2bfloat16_rn(xt[e]));
+        __syncthreads();
+        const float *xr = xt + r0 * kChunk;
+        const uint16_t(*wt)[kSmallCols] = ws[i % kStages];
+        // register double buffer: sub-block b + 1's operands are loaded
+        // before sub-block b's FMAs, so the loads' latency overlaps the chain
+        constexpr int SB = 16;
+        float4 xv[2][kRowsPerWarp][SB / 4];
+        uint16_t wv[2][SB];
 #pragma unroll
-            for (int r = 0; r < MR; ++r) acc[r] = fmaf(xs[kk][r], bv, acc[r]);
+        for (int j = 0; j < SB; ++j) wv[0][j] = wt[j][lane];
+#pragma unroll
+        for (int q = 0; q < kRowsPerWarp; ++q)
+#pragma unroll
+            for (int j = 0; j < SB / 4; ++j) xv[0][q][j] = *reinterpret_cast<const float4 *>(xr + q * kChunk + 4 * j);
+#pragma unroll
+        for (int b = 0; b < kChunk / SB; ++b) {
+            const int cur = b & 1, nxt = cur ^ 1;
+            if (b + 1 < kChunk / SB) {
+#pragma unroll
+                for (int j = 0; j < SB; ++j) wv[nxt][j] = wt[(b + 1) * SB + j][lane];
+#pragma unroll
+                for (int q = 0; q < kRowsPerWarp; ++q)
+#pragma unroll
+                    for (int j = 0; j < SB / 4; ++j)
+                        xv[nxt][q][j] = *reinterpret_cast<const float4 *>(xr + q * kChunk + (b + 1) * SB + 4 * j);
+            }
+#pragma unroll
+            for (int j = 0; j < SB / 4; ++j) {
+                const float w0 = bf16_bits_to_f32(wv[cur][4 * j]), w1 = bf16_bits_to_f32(wv[cur][4 * j + 1]);
+                const float w2 = bf16_bits_to_f32(wv[cur][4 * j + 2]), w3 = bf16_bits_to_f32(wv[cur][4 * j + 3]);
+#pragma unroll
+                for (int q = 0; q < kRowsPerWarp; ++q) {
+                    acc[q] = fmaf(xv[cur][q][j].x, w0, acc[q]);
+                    acc[q] = fmaf(xv[cur][q][j].y, w1, acc[q]);
+                    acc[q] = fmaf(xv[cur][q][j].z, w2, acc[q]);
+                    acc[q] = fmaf(xv[cur][q][j].w, w3, acc[q]);
+                }
+            }
         }
-        __syncthreads();  // the tiles and xs are rewritten next
+        __syncthreads();  // the stage is refilled next
     }
-    if (c >= n) return;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (c < n) {
 #pragma unroll
-    for (int r = 0; r < MR; ++r) {
-        if (r >= m) break;
-        float *o = out + (int64_t)r * n + c;
-        *o = accumulate ? (*o + acc[r]) : acc[r];
+        for (int q = 0; q < kRowsPerWarp; ++q) {
+            if (r0 + q >= m) break;
+            float *o = out + (int64_t)(r0 + q) * n + c;
+            *o = accumulate ? (*o + acc[q]) : acc[q];
+        }
     }
 }
 
@@ -265,13 +325,20 @@ vc_status vc_linear(const float *x, const void *w_bf16, float *out, int32_t m, i
     const uint16_t *w = (const uint16_t *)w_bf16;
     const cudaStream_t st = (cudaStream_t)stream;
     if (m <= kSmallRows) {
-        const dim3 grid(ceil_div(n, kSmallCols));
-        if (m <= 4)
-            launch_pdl(linear_rows_kernel<4>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
-        else if (m <= 8)
-            launch_pdl(linear_rows_kernel<8>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
+        static bool attr = false;
+        if (!attr) {  // the largest tile sets, once
+            cudaFuncSetAttribute(linear_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 small_rows_smem(8, 1));
+            cudaFuncSetAttribute(linear_rows_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 small_rows_smem(kSmallRows, 2));
+            attr = true;
+        }
+        const int R = small_rows_per_warp(m);
+        const dim3 grid(ceil_div(n, kSmallCols)), block(kSmallCols * ceil_div(m, R));
+        if (R == 1)
+            launch_pdl(linear_rows_kernel<1>, grid, block, small_rows_smem(m, 1), st, x, w, out, m, k, n, accumulate);
         else
-            launch_pdl(linear_rows_kernel<16>, grid, kSmallCols, 0, st, x, w, out, m, k, n, accumulate);
+            launch_pdl(linear_rows_kernel<2>, grid, block, small_rows_smem(m, 2), st, x, w, out, m, k, n, accumulate);
     } else {
         dim3 grid(ceil_div(n, TN), ceil_div(m, TM));
         launch_pdl(linear_kernel, grid, 256, 0, st, x, w, out, m, k, n, accumulate);

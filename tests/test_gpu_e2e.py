@@ -64,7 +64,7 @@ def test_e2e_greedy_against_cpu_oracle_model():
     assert excluded < 8
 
 
-@pytest.mark.parametrize("k,n", [(1024, 1536), (4096, 1024), (100, 70)])
+@pytest.mark.parametrize("k,n", [(1024, 1536), (4096, 1024), (100, 70), (131, 72)])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_linear_rows_invariant_across_kernels(k, n, accumulate):
     """vc_linear computes up to 16 rows with the small-row kernel and more
