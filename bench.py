@@ -27,7 +27,10 @@ workloads of the path on the device (CUDA events): the 70B-shaped layer
 (draft over bf16 token-drop KV_comp, 40-query verify over a 131072-token
 KV_full, GPU token selection) with the 40k-context verify point, one
 staggered mixed launch of the 32-request 3-bit workload, and the headline's
-draft step at 3 and 4 bits.
+draft step at 3 and 4 bits.  Beside each, unless --no-cpu-baseline, a
+`cpu_baseline`: the oracle on a bounded sample of the same shape (about 2 s
+each; drafted tokens/s, or verified query-head rows/s, matching the device
+key it sits beside).
 
 --impl reference: the CPU oracle on this machine's cores, a bounded sample
 of the same workload per step (draft attention of one request).
@@ -316,7 +319,8 @@ def bits_measure(w, device, bit_widths=(3, 4)):
         us = _graph_us(torch, lambda: [c() for c in calls], 5) / len(calls)
         nb = float(np.mean([draft_bytes(w2, w2["ctx"] + i + 1) for i in range(len(calls))]))
         out["%d_bit" % bits] = {"us_per_call": us, "bytes_per_call": nb, "GBps": nb / us / 1e3,
-                                "frac_hbm_measured": nb / us / 1e3 / peak}
+                                "frac_hbm_measured": nb / us / 1e3 / peak,
+                                "tokens_per_s": w["batch"] / (us * 1e-6)}
         del st2, rnd2
         torch.cuda.empty_cache()
     return out
@@ -379,6 +383,101 @@ def oracle_sample(w, st, seconds_target=15.0, max_requests=128):
     return {"value": done / t_total, "unit": "tokens/s", "cores": n_threads, "kind": "oracle",
             "sample": "%d request-steps (cycling over the 8 requests) x 1 draft step (32 query heads over 32768 2-bit KV_comp entries); "
                       "KV_comp from the oracle's own compress; %.1f s of CPU time" % (done, t_total)}
+
+
+def _oracle_reps(fn, seconds):
+    """Call fn until about `seconds` of wall time; (calls, seconds)."""
+    n, t = 0, 0.0
+    while t < seconds:
+        t0 = time.perf_counter()
+        fn()
+        t += time.perf_counter() - t0
+        n += 1
+    return n, t
+
+
+def oracle_extras(seconds=2.0):
+    """Bounded oracle samples beside the other workloads' device numbers, in
+    the same units (drafted tokens/s; verified query-head rows/s), on seeded
+    synthetic inputs of the same shapes (timing only: the values are not
+    compared here).  Each sample runs for about `seconds`."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    import synth
+    nt = oracle.threads()
+
+    def entry(value, unit, sample):
+        return {"value": value, "unit": unit, "cores": nt, "kind": "oracle", "sample": sample}
+
+    def draft_leg(pool, k, v, bits, hq, what):
+        n, hkv, d = k.shape
+        comp = oracle.compress(k, v, np.arange(n, dtype=np.int32), bits)
+        q = synth.normal_bf16(rng, (hq, d))
+        scale = float(np.float32(1 / math.sqrt(d)))
+        c, t = _oracle_reps(lambda: oracle.draft_attn(q, comp, scale, pool=pool), seconds)
+        return entry(c / t, "tokens/s", "%d request-steps x 1 draft step (%d query heads over %d %s entries of "
+                     "one request); %.1f s" % (c, hq, n, what, t))
+
+    def verify_leg(pool, n_ctx, n_q, hq, hkv, d, rows, what):
+        # one kv head's K / V (a row reads only its own head), rows of the
+        # block's last query spread over that head's group
+        k = synth.normal_bf16(rng, (n_ctx, 1, d))
+        v = synth.normal_bf16(rng, (n_ctx, 1, d))
+        grp = hq // hkv
+        q = synth.normal_bf16(rng, (n_q, grp, d))
+        qs = list(range(n_q - rows // grp, n_q)) if rows >= grp else [n_q - 1]
+        scale = float(np.float32(1 / math.sqrt(d)))
+        c, t = _oracle_reps(lambda: oracle.verify_attn(q, k, v, scale, queries=qs, pool=pool), seconds)
+        nrows = c * len(qs) * grp
+        return entry(nrows / t, "query-head rows/s", "%d rows (query x head) over %d keys each (%s); %.1f s"
+                     % (nrows, n_ctx, what, t))
+
+    out = {}
+    with ThreadPoolExecutor(nt) as pool:
+        w = dict(synth.WORKLOADS["70b_128k_drop4"])
+        rng = synth.rng_for("70b_128k_drop4", 11)
+        hq, hkv, d, nk, N, x = w["hq"], w["hkv"], w["d"], w["kept_total"], w["ctx"], w["x"]
+        k = synth.normal_bf16(rng, (nk, hkv, d))
+        v = synth.normal_bf16(rng, (nk, hkv, d))
+        out["70b_draft"] = draft_leg(pool, k, v, 16, hq, "kept bf16")
+        del k, v
+        out["70b_verify"] = verify_leg(pool, N + x, x, hq, hkv, d, 32, "the 70B-shaped block's last queries")
+        out["verify_40k"] = verify_leg(pool, 40960 + 40, 40, 32, hkv, d, 32, "the 40k point's last queries")
+        w = dict(synth.WORKLOADS["mixed_32req_3bit"])
+        rng = synth.rng_for("mixed_32req_3bit", 11)
+        n_mean = (w["ctx_lo"] + w["ctx_hi"]) // 2
+        k = synth.normal_bf16(rng, (n_mean, w["hkv"], w["d"]))
+        v = synth.normal_bf16(rng, (n_mean, w["hkv"], w["d"]))
+        out["mixed_draft"] = draft_leg(pool, k, v, w["bits"], w["hq"], "3-bit (the mean context)")
+        del k, v
+        vr = verify_leg(pool, n_mean + w["x"], w["x"], w["hq"], w["hkv"], w["d"], 32,
+                        "the mean context, the block's last queries")
+        vr.update(value=vr["value"] / w["hq"], unit="verified tokens/s (all query heads of a query)")
+        out["mixed_verify"] = vr
+        w = dict(synth.WORKLOADS[WORKLOAD])
+        rng = synth.rng_for(WORKLOAD, 11)
+        k = synth.normal_bf16(rng, (w["ctx"], w["hkv"], w["d"]))
+        v = synth.normal_bf16(rng, (w["ctx"], w["hkv"], w["d"]))
+        for bits in (3, 4):
+            out["%d_bit" % bits] = draft_leg(pool, k, v, bits, w["hq"], "%d-bit" % bits)
+    return out
+
+
+def attach_oracle(extras, cpu):
+    """Put each oracle sample beside the device number it matches."""
+    big = extras["70b_128k_drop4"]
+    big["draft"]["cpu_baseline"] = cpu["70b_draft"]
+    c = big["config"]
+    big["verify"]["rows_per_s"] = c["batch"] * c["x"] * c["q_heads"] / (big["verify"]["us_per_call"] * 1e-6)
+    big["verify"]["cpu_baseline"] = cpu["70b_verify"]
+    v40 = big["verify_40k"]
+    c = v40["config"]
+    v40["rows_per_s"] = c["batch"] * c["n_q"] * c["q_heads"] / (v40["us_per_call"] * 1e-6)
+    v40["cpu_baseline"] = cpu["verify_40k"]
+    extras["mixed_32req_3bit"]["cpu_baseline"] = {"draft_tokens_per_s": cpu["mixed_draft"],
+                                                  "verify_tokens_per_s": cpu["mixed_verify"]}
+    for bits in (3, 4):
+        extras["draft_8b_32k_other_bits"]["%d_bit" % bits]["cpu_baseline"] = cpu["%d_bit" % bits]
 
 
 def reference_main(args, rank, ws):
@@ -515,6 +614,8 @@ def main():
         extras = {"70b_128k_drop4": big_measure(),
                   "mixed_32req_3bit": mixed_measure(args.steps, args.warmup, staging=False),
                   "draft_8b_32k_other_bits": bits_measure(w, device)}
+        if not args.no_cpu_baseline:
+            attach_oracle(extras, oracle_extras())
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "draft_attn_traffic.txt")) as f:
