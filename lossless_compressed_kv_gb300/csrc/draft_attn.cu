@@ -85,7 +85,7 @@ int occupancy() {
     static int occ = -1;
     if (occ < 0) {
         using C = Cfg<BITS, D, kWarps>;
-        cudaFuncSetAttribute(draft_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        set_smem_limit((const void *)draft_kernel<BITS, D>, C::SMEM);
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<BITS, D>, kWarps * 32, C::SMEM) !=
                 cudaSuccess ||
@@ -160,7 +160,8 @@ Plan plan_any(int bits, int d, int batch, int hkv, int max_seq_len) {
 template <int BITS, int D>
 cudaError_t launch(const DraftArgs &a, int batch, cudaStream_t st) {
     using C = Cfg<BITS, D, kWarps>;
-    occupancy<BITS, D>();  // sets the shared-memory attribute once
+    const cudaError_t e = set_smem_limit((const void *)draft_kernel<BITS, D>, C::SMEM);
+    if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)batch * a.hkv;
     const int64_t ctas = (int64_t)a.lo_units * a.n_lo + (units - a.lo_units) * a.n_hi;
     launch_pdl(draft_kernel<BITS, D>, dim3((unsigned)ctas), kWarps * 32, C::SMEM, st, a);

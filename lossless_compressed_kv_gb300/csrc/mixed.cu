@@ -175,14 +175,11 @@ size_t draft_part(const vc_paged_kv &comp, int hq, int max_seq_len) {
 template <int BITS, int D>
 cudaError_t launch(const MixedArgs &m, int batch, float *out_draft, float *out_verify, cudaStream_t st) {
     using C = MCfg<BITS, D>;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(mixed_kernel<BITS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        attr = true;
-    }
+    cudaError_t e = set_smem_limit((const void *)mixed_kernel<BITS, D>, C::SMEM);
+    if (e != cudaSuccess) return e;
     const int nd = m.d.n_splits * m.d.hkv * batch;
     launch_pdl(mixed_kernel<BITS, D>, m.n_verify_blocks + nd, kThreads, C::SMEM, st, m);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int draft_rows = batch * m.d.hq, verify_rows = batch * m.v.n_q * m.v.hq;
     launch_pdl(mixed_reduce_kernel<D>, draft_rows + verify_rows, D, 0, st, m, out_draft, out_verify, draft_rows);

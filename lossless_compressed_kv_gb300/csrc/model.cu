@@ -325,15 +325,12 @@ vc_status vc_linear(const float *x, const void *w_bf16, float *out, int32_t m, i
     const uint16_t *w = (const uint16_t *)w_bf16;
     const cudaStream_t st = (cudaStream_t)stream;
     if (m <= kSmallRows) {
-        static bool attr = false;
-        if (!attr) {  // the largest tile sets, once
-            cudaFuncSetAttribute(linear_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 small_rows_smem(8, 1));
-            cudaFuncSetAttribute(linear_rows_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 small_rows_smem(kSmallRows, 2));
-            attr = true;
-        }
         const int R = small_rows_per_warp(m);
+        // the largest tile set of each variant
+        const cudaError_t e = R == 1 ? set_smem_limit((const void *)linear_rows_kernel<1>, small_rows_smem(8, 1))
+                                     : set_smem_limit((const void *)linear_rows_kernel<2>,
+                                                      small_rows_smem(kSmallRows, 2));
+        if (e != cudaSuccess) return VC_ERR_CUDA;
         const dim3 grid(ceil_div(n, kSmallCols)), block(kSmallCols * ceil_div(m, R));
         if (R == 1)
             launch_pdl(linear_rows_kernel<1>, grid, block, small_rows_smem(m, 1), st, x, w, out, m, k, n, accumulate);

@@ -7,6 +7,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <tuple>
 #include <utility>
 
 #include "vc.h"
@@ -274,6 +277,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// A kernel's dynamic shared-memory limit (needed above 48 KB), set once per
+// (kernel, device, size): the attribute belongs to the device's context, so a
+// process that drives several devices sets it on each of them.
+inline cudaError_t set_smem_limit(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::set<std::tuple<const void *, int, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_tuple(kernel, dev, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
 }
 
 }  // namespace vc

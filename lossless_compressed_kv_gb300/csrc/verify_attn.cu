@@ -37,11 +37,8 @@ __global__ void verify_reduce_kernel(const float *ws_o, const float *ws_ml, int 
 template <int D, int QT>
 cudaError_t launch(Args a, int batch, int rb0, int n_rb, cudaStream_t st) {
     using C = vtc::Cfg<D, QT>;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(verify_kernel<D, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        attr = true;
-    }
+    const cudaError_t e = set_smem_limit((const void *)verify_kernel<D, QT>, C::SMEM);
+    if (e != cudaSuccess) return e;
     a.rows_per_cta = QT * vtc::kTileRows;
     a.rb0 = rb0;
     dim3 grid(a.n_splits, n_rb, batch * a.hkv);
