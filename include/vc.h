@@ -513,7 +513,9 @@ VC_API vc_status vc_stagger_horizon(const vc_stagger_model *m, int32_t x_lo, int
  *  vc_linear         out[r][n] (+)= sum_k bf16(x[r][k]) * W[k][n]: x fp32 [m][k]
  *                    rounded to bf16 on load (activations are stored as bf16
  *                    between layers), W bf16 [k][n], fp32 FMAs in increasing k;
- *                    accumulate != 0 adds to out (residual connection)
+ *                    accumulate != 0 adds to out (residual connection).  Up to
+ *                    16 rows run on a small-row kernel, more on a tiled one:
+ *                    the same FMA chain, so the same bits either way
  *  vc_swiglu         out[r][c] = silu(gu[r][c]) * gu[r][f + c]  (fp32 [m][2f] -> [m][f])
  *  vc_rope_kv_write  qkv fp32 [m][(Hq + 2 Hkv) D] -> q bf16 [m][Hq][D] after a
  *                    rotary embedding (channel i pairs with i + D/2, angle
