@@ -66,3 +66,9 @@ def test_reference_arm_under_torchrun_two_ranks():
     for key in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "config",
                 "cpu_baseline", "e2e"):
         assert key in d
+    # the same metric, unit, direction and config object as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["config"] == json.loads(json.dumps(bench.headline_config(dict(synth.WORKLOADS[bench.WORKLOAD]))))
